@@ -1,0 +1,196 @@
+"""CPU reference oracle for the QMoE layer and GroupedMatMul (test infrastructure).
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It is a ctypes wrapper over the plain
+double-precision C restatement in ``qmoe_oracle.c``; it shares no code with
+the CUDA library and never calls it.  The wrapper only marshals arrays and
+derives shapes ([QMoE manifest] derive.numTokens / derive.hiddenSize: the
+token count is the product of the leading input dimensions).
+
+Functions whose result has no independent pin say so here and in the design
+notes: ``swiglu_limit`` handling (reading of [QMoE manifest]
+attributeDescriptions.swiglu_limit) is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qmoe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+BAD_INDEX = -1
+BAD_ARG = -2
+
+
+def build(force: bool = False) -> str:
+    """Compile qmoe_oracle.c into liboracle.so with gcc (no CUDA involved)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+           "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        D = ctypes.c_double
+        C = ctypes.c_int
+        lib.oracle_grouped_matmul.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P]
+        lib.oracle_grouped_matmul.restype = C
+        lib.oracle_grouped_matmul_decomposed.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P]
+        lib.oracle_grouped_matmul_decomposed.restype = C
+        lib.oracle_weight_code.argtypes = [P, I64, C]
+        lib.oracle_weight_code.restype = C
+        lib.oracle_dequant.argtypes = [P, P, I64, C, I64]
+        lib.oracle_dequant.restype = D
+        lib.oracle_dequant_rows.argtypes = [P, P, I64, I64, C, I64, P]
+        lib.oracle_dequant_rows.restype = None
+        lib.oracle_route.argtypes = [P, I64, I64, P, P]
+        lib.oracle_route.restype = C
+        lib.oracle_activation.argtypes = [P, I64, C, D, D, C, D, P]
+        lib.oracle_activation.restype = None
+        lib.oracle_qmoe.argtypes = [P, I64, P, I64, P, P, P, P, I64, C, I64, C, D, D,
+                                    C, D, I64, P, I64, C, P, P, P, C]
+        lib.oracle_qmoe.restype = C
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# GroupedMatMul  ([GroupedMatMul-29] Summary)
+# --------------------------------------------------------------------------
+
+def grouped_matmul(inp, weights, group_indices, bias=None, decomposed=False):
+    """output[m, i] = input[m] @ weights[group_indices[m, i]] (+ bias[g]).
+
+    All arithmetic in float64.  Returns (output [M,S,N] float64, status);
+    status is BAD_INDEX when an index lies outside [0, G).
+    """
+    lib = _load()
+    x = _c(inp, np.float64)
+    w = _c(weights, np.float64)
+    idx = _c(group_indices, np.int64)
+    M, K = x.shape
+    G, K2, N = w.shape
+    assert K2 == K
+    S = idx.shape[1] if idx.ndim == 2 else 0
+    b = None if bias is None else _c(bias, np.float64)
+    out = np.zeros((M, S, N), dtype=np.float64)
+    fn = lib.oracle_grouped_matmul_decomposed if decomposed else lib.oracle_grouped_matmul
+    st = fn(_ptr(x), M, K, _ptr(w), G, N, _ptr(idx), S,
+            None if b is None else _ptr(b), _ptr(out))
+    return out, st
+
+
+# --------------------------------------------------------------------------
+# QMoE pieces
+# --------------------------------------------------------------------------
+
+def weight_code(packed_row, j, bits):
+    lib = _load()
+    row = _c(packed_row, np.uint8)
+    return lib.oracle_weight_code(_ptr(row), j, bits)
+
+
+def dequant_rows(packed, scales, K, bits, block_size):
+    """Dequantize a [rows, K/pack] packed matrix with its scales -> [rows, K]."""
+    lib = _load()
+    pk = _c(packed, np.uint8)
+    sc = _c(scales, np.float32)
+    rows = pk.shape[0]
+    out = np.zeros((rows, K), dtype=np.float64)
+    lib.oracle_dequant_rows(_ptr(pk), _ptr(sc), rows, K, bits, block_size, _ptr(out))
+    return out
+
+
+def route(logits, k):
+    """Top-k selection and softmax over the selected logits, per row."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    sel = np.zeros((T, k), dtype=np.int32)
+    p = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        st = lib.oracle_route(_ptr(lg[t]), E, k, _ptr(sel[t]), _ptr(p[t]))
+        if st != OK:
+            raise ValueError(f"oracle_route failed with {st}")
+    return sel, p
+
+
+def activation(h, inter, act, alpha=1.0, beta=0.0, swiglu_limit=None):
+    lib = _load()
+    hh = _c(h, np.float64)
+    a = np.zeros(inter, dtype=np.float64)
+    lib.oracle_activation(_ptr(hh), inter, 1 if act == "swiglu" else 0, alpha, beta,
+                          0 if swiglu_limit is None else 1,
+                          0.0 if swiglu_limit is None else float(swiglu_limit), _ptr(a))
+    return a
+
+
+def qmoe(x, logits, w1, s1, w2, s2, *, k, expert_weight_bits=4, block_size=0,
+         activation_type="relu", activation_alpha=1.0, activation_beta=0.0,
+         swiglu_limit=None, tokens=None, dense=False, nthreads=1):
+    """QMoE layer output for the listed tokens (all tokens when None).
+
+    Returns (y [ntok, H] float64, sel [ntok, k] int32, p [ntok, k] float64).
+    """
+    lib = _load()
+    xs = _c(x, np.float32)
+    H = xs.shape[-1]
+    xs = xs.reshape(-1, H)
+    lg = _c(logits, np.float32)
+    E = lg.shape[1]
+    bits = int(expert_weight_bits)
+    fusion = 2 if activation_type == "swiglu" else 1
+    w1a = _c(w1, np.uint8)
+    w2a = _c(w2, np.uint8)
+    s1a = _c(s1, np.float32)
+    s2a = _c(s2, np.float32)
+    I = w1a.shape[1] // fusion
+    if tokens is None:
+        tok = np.arange(xs.shape[0], dtype=np.int64)
+    else:
+        tok = _c(tokens, np.int64)
+    ntok = tok.shape[0]
+    y = np.zeros((ntok, H), dtype=np.float64)
+    sel = np.zeros((ntok, k), dtype=np.int32)
+    p = np.zeros((ntok, k), dtype=np.float64)
+    st = lib.oracle_qmoe(_ptr(xs), H, _ptr(lg), E, _ptr(w1a), _ptr(s1a), _ptr(w2a),
+                         _ptr(s2a), I, bits, int(block_size),
+                         1 if activation_type == "swiglu" else 0,
+                         float(activation_alpha), float(activation_beta),
+                         0 if swiglu_limit is None else 1,
+                         0.0 if swiglu_limit is None else float(swiglu_limit),
+                         int(k), _ptr(tok), ntok, 1 if dense else 0,
+                         _ptr(y), _ptr(sel), _ptr(p), int(nthreads))
+    if st != OK:
+        raise ValueError(f"oracle_qmoe failed with {st}")
+    return y, sel, p

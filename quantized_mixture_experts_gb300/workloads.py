@@ -1,0 +1,155 @@
+"""Seeded synthetic inputs for the QMoE layer.
+
+This module only draws random numbers with the shapes, value distributions and
+load skew of the five benchmark workloads; it holds none of the layer's
+arithmetic.  Both the CUDA path and the CPU oracle receive the arrays it
+returns, so neither side generates its own inputs.
+
+Recipe (every workload):
+  * activations  fp32 ~ N(0, 1), shaped like the workload's input
+    (rank 2 ``[T, H]`` or rank 3 ``[B, S, H]``);
+  * router logits fp32 ~ N(0, sigma^2) with sigma = 1 or 2 (the workload
+    text writes "N(0,2)", read as a standard deviation of 2);
+  * the many-small-experts workload adds a per-expert bias
+    ``-1.1 * ln(1 + pi(e))`` (pi a seeded permutation) to skew load like a
+    Zipf(s=1.1) popularity law;
+  * any logit row whose k+1 largest values contain a repeated value is
+    redrawn, so the top-k set is unique;
+  * packed expert weights are uniform random bytes (4-bit codes uniform on
+    0..15, 8-bit codes on 0..255);
+  * scales fp32 ~ U[lo, hi] (U[0.005, 0.02] for the tiny workload,
+    U[0.002, 0.01] otherwise).
+Seeds are ``workload_index * 1000 + tensor_id`` with numpy's PCG64.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Tuple
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    input_shape: Tuple[int, ...]
+    hidden: int
+    inter: int
+    experts: int
+    k: int
+    bits: int
+    block_size: int          # 0 = column-wise scales
+    activation: str          # "relu" | "swiglu"
+    logit_sigma: float = 1.0
+    scale_lo: float = 0.002
+    scale_hi: float = 0.01
+    zipf_s: float = 0.0      # 0 = no skew bias
+    alpha: float = 1.0
+    beta: float = 0.0
+    swiglu_limit: Optional[float] = None
+
+    @property
+    def tokens(self) -> int:
+        n = 1
+        for d in self.input_shape[:-1]:
+            n *= d
+        return n
+
+    @property
+    def fusion(self) -> int:
+        return 2 if self.activation == "swiglu" else 1
+
+    @property
+    def pack(self) -> int:
+        return 2 if self.bits == 4 else 1
+
+    def attrs(self) -> dict:
+        return dict(k=self.k, expert_weight_bits=self.bits, block_size=self.block_size,
+                    activation_type=self.activation, activation_alpha=self.alpha,
+                    activation_beta=self.beta, swiglu_limit=self.swiglu_limit)
+
+    def with_tokens(self, T: int, name: Optional[str] = None) -> "Workload":
+        return dataclasses.replace(self, name=name or f"{self.name}_T{T}",
+                                   input_shape=(T, self.hidden))
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 0, (16, 64), 64, 128, 4, 2, 4, 0, "relu",
+                     logit_sigma=1.0, scale_lo=0.005, scale_hi=0.02),
+    "decode": Workload("decode", 1, (8, 4096), 4096, 14336, 8, 2, 4, 32, "swiglu",
+                       logit_sigma=2.0),
+    "prefill": Workload("prefill", 2, (2, 2048, 4096), 4096, 14336, 8, 2, 4, 128,
+                        "swiglu", logit_sigma=2.0),
+    "many_small": Workload("many_small", 3, (2048, 2048), 2048, 1024, 64, 8, 8, 0,
+                           "swiglu", logit_sigma=1.0, zipf_s=1.1),
+    "large_e": Workload("large_e", 4, (4, 4096, 2048), 2048, 768, 128, 8, 4, 64,
+                        "swiglu", logit_sigma=1.0),
+}
+
+
+def _rng(wl: Workload, tensor_id: int, salt: int = 0) -> np.random.Generator:
+    return np.random.default_rng(wl.index * 1000 + tensor_id + 100000 * salt)
+
+
+def _logits(wl: Workload, T: int, salt: int) -> np.ndarray:
+    E, k = wl.experts, wl.k
+    rng = _rng(wl, 2, salt)
+    lg = (rng.standard_normal((T, E), dtype=np.float32) * np.float32(wl.logit_sigma))
+    bias = None
+    if wl.zipf_s > 0:
+        perm = _rng(wl, 7, salt).permutation(E)
+        bias = (-wl.zipf_s * np.log1p(perm.astype(np.float64))).astype(np.float32)
+        lg = lg + bias[None, :]
+    redraw = _rng(wl, 8, salt)
+    m = min(k + 1, E)
+    for _ in range(100):
+        top = -np.sort(-lg, axis=1)[:, :m]
+        bad = np.nonzero(np.any(top[:, 1:] == top[:, :-1], axis=1))[0]
+        if bad.size == 0:
+            break
+        fresh = redraw.standard_normal((bad.size, E), dtype=np.float32) * np.float32(wl.logit_sigma)
+        if bias is not None:
+            fresh = fresh + bias[None, :]
+        lg[bad] = fresh
+    return np.ascontiguousarray(lg, dtype=np.float32)
+
+
+def make_inputs(wl: Workload, salt: int = 0) -> dict:
+    """Draw every input tensor of one QMoE call for workload ``wl``."""
+    T, H, I, E = wl.tokens, wl.hidden, wl.inter, wl.experts
+    f, pk = wl.fusion, wl.pack
+    x = _rng(wl, 1, salt).standard_normal(wl.input_shape, dtype=np.float32)
+    logits = _logits(wl, T, salt)
+    w1 = _rng(wl, 3, salt).integers(0, 256, (E, f * I, H // pk), dtype=np.uint8)
+    w2 = _rng(wl, 5, salt).integers(0, 256, (E, H, I // pk), dtype=np.uint8)
+    if wl.block_size:
+        s1_shape = (E, f * I, H // wl.block_size)
+        s2_shape = (E, H, I // wl.block_size)
+    else:
+        s1_shape = (E, f * I)
+        s2_shape = (E, H)
+    s1 = _rng(wl, 4, salt).uniform(wl.scale_lo, wl.scale_hi, s1_shape).astype(np.float32)
+    s2 = _rng(wl, 6, salt).uniform(wl.scale_lo, wl.scale_hi, s2_shape).astype(np.float32)
+    return dict(input=x, router_probs=logits, fc1_experts_weights=w1, fc1_scales=s1,
+                fc2_experts_weights=w2, fc2_scales=s2)
+
+
+def sample_tokens(logits_sel: np.ndarray, T: int, n: int, seed: int) -> np.ndarray:
+    """Seeded token subset of size >= n that touches every selected expert.
+
+    ``logits_sel`` is the [T, k] selected-expert table of the workload (the
+    oracle's routing), used only to add one token per touched expert.
+    """
+    rng = np.random.default_rng(seed)
+    n = min(n, T)
+    chosen = set(rng.choice(T, size=n, replace=False).tolist())
+    first = {}
+    for t in range(T):
+        for e in logits_sel[t].tolist():
+            first.setdefault(e, t)
+    chosen.update(first.values())
+    return np.array(sorted(chosen), dtype=np.int64)
