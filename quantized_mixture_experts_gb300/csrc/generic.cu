@@ -1,0 +1,177 @@
+// Scalar fp32 kernels of the QMoE layer for shapes the tensor-core paths do
+// not take (no alignment requirements), plus the weighted combine shared by
+// every path.
+//
+// QMoE manifest: inputs[2..5] (packed layouts), derive.quantMidpoint /
+// packSize (w = (q - mid) * scale, low nibble first), attributeDescriptions
+// (ReLU, interleaved SwiGLU, alpha, beta, swiglu_limit), pass QMoE.MixStage.
+#include "qmoe_internal.h"
+
+namespace qmoe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float deq(const uint8_t* __restrict__ row,
+                                     const float* __restrict__ srow, int64_t j, int bits, int mid,
+                                     int64_t bs) {
+    int q;
+    if (bits == 8) {
+        q = row[j];
+    } else {
+        const uint8_t b = row[j >> 1];
+        q = (j & 1) ? (b >> 4) : (b & 15);
+    }
+    const float sc = bs ? srow[j / bs] : srow[0];
+    return float(q - mid) * sc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+
+__device__ __forceinline__ float swiglu(float g, float u, float alpha, float beta, int has_limit,
+                                        float limit) {
+    if (has_limit) {
+        g = fminf(g, limit);
+        u = fminf(fmaxf(u, -limit), limit);
+    }
+    const float sig = 1.f / (1.f + expf(-alpha * g));
+    return g * sig * (u + beta);
+}
+
+// One warp per (sorted row, output column j): FC1 dot product(s) + activation.
+__global__ void generic_fc1_kernel(Problem p, const int32_t* __restrict__ perm,
+                                   const int32_t* __restrict__ sel, float* __restrict__ act,
+                                   int64_t total) {
+    const int64_t widx = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (widx >= total) return;
+    const int64_t slots = total / p.I;
+    const int64_t j = widx / slots, pos = widx % slots;   // weight-row major: rows stay in cache
+    const int32_t s = perm[pos];
+    const int64_t t = s / p.k;
+    const int64_t e = sel[s];
+    const int64_t rows1 = p.fusion * p.I;
+    const int64_t pc = p.H / p.pack;
+    const float* __restrict__ xt = p.x + t * p.H;
+    const uint8_t* __restrict__ we = p.w1 + e * rows1 * pc;
+    const float* __restrict__ se = p.s1 + e * rows1 * p.nb1;
+    float out;
+    if (p.act == QMOE_ACT_SWIGLU) {
+        const int64_t rg = 2 * j, ru = 2 * j + 1;
+        float g = 0.f, u = 0.f;
+        for (int64_t kk = lane; kk < p.H; kk += 32) {
+            const float xv = xt[kk];
+            g += xv * deq(we + rg * pc, se + rg * p.nb1, kk, p.bits, p.mid, p.bs);
+            u += xv * deq(we + ru * pc, se + ru * p.nb1, kk, p.bits, p.mid, p.bs);
+        }
+        g = warp_sum(g);
+        u = warp_sum(u);
+        out = swiglu(g, u, p.alpha, p.beta, p.has_limit, p.limit);
+    } else {
+        float h = 0.f;
+        for (int64_t kk = lane; kk < p.H; kk += 32)
+            h += xt[kk] * deq(we + j * pc, se + j * p.nb1, kk, p.bits, p.mid, p.bs);
+        h = warp_sum(h);
+        out = fmaxf(h, 0.f);
+    }
+    if (lane == 0) act[pos * p.I + j] = out;
+}
+
+// One warp per (sorted row, output column d): FC2 dot product, written to the
+// row of the original slot.
+__global__ void generic_fc2_kernel(Problem p, const int32_t* __restrict__ perm,
+                                   const int32_t* __restrict__ sel,
+                                   const float* __restrict__ act, float* __restrict__ slot_out,
+                                   int64_t total) {
+    const int64_t widx = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (widx >= total) return;
+    const int64_t slots = total / p.H;
+    const int64_t d = widx / slots, pos = widx % slots;
+    const int32_t s = perm[pos];
+    const int64_t e = sel[s];
+    const int64_t pc = p.I / p.pack;
+    const uint8_t* __restrict__ wr = p.w2 + (e * p.H + d) * pc;
+    const float* __restrict__ sr = p.s2 + (e * p.H + d) * p.nb2;
+    const float* __restrict__ ar = act + pos * p.I;
+    float o = 0.f;
+    for (int64_t kk = lane; kk < p.I; kk += 32) o += ar[kk] * deq(wr, sr, kk, p.bits, p.mid, p.bs);
+    o = warp_sum(o);
+    if (lane == 0) slot_out[int64_t(s) * p.H + d] = o;
+}
+
+// y[t, d] = sum_i pw[t,i] * sum_split slot_out[split][t*k+i][d], in ascending
+// i and split order (deterministic, no atomics).
+__global__ void combine_kernel(const float* __restrict__ slot_out, const float* __restrict__ pw,
+                               float* __restrict__ y, int64_t T, int64_t H, int k, int splits,
+                               int64_t slots, int vec) {
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        const int64_t H4 = H / 4;
+        if (idx >= T * H4) return;
+        const int64_t t = idx / H4, d4 = idx % H4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < k; ++i) {
+            const float w = pw[t * k + i];
+            float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < splits; ++sp) {
+                const float4 v = reinterpret_cast<const float4*>(
+                    slot_out + (int64_t(sp) * slots + t * k + i) * H)[d4];
+                part.x += v.x; part.y += v.y; part.z += v.z; part.w += v.w;
+            }
+            acc.x += w * part.x; acc.y += w * part.y; acc.z += w * part.z; acc.w += w * part.w;
+        }
+        reinterpret_cast<float4*>(y + t * H)[d4] = acc;
+    } else {
+        if (idx >= T * H) return;
+        const int64_t t = idx / H, d = idx % H;
+        float acc = 0.f;
+        for (int i = 0; i < k; ++i) {
+            float part = 0.f;
+            for (int sp = 0; sp < splits; ++sp)
+                part += slot_out[(int64_t(sp) * slots + t * k + i) * H + d];
+            acc += pw[t * k + i] * part;
+        }
+        y[t * H + d] = acc;
+    }
+}
+
+unsigned blocks_for(int64_t n, int per) { return unsigned((n + per - 1) / per); }
+
+}  // namespace
+
+cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
+    const int64_t total = pl.slots * p.I;
+    note_launch(QMOE_KERNEL_FC1, s, true);
+    generic_fc1_kernel<<<blocks_for(total, 8), 256, 0, s>>>(p, w.perm, w.sel,
+                                                            static_cast<float*>(w.act), total);
+    note_launch(QMOE_KERNEL_FC1, s, false);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
+    const int64_t total = pl.slots * p.H;
+    note_launch(QMOE_KERNEL_FC2, s, true);
+    generic_fc2_kernel<<<blocks_for(total, 8), 256, 0, s>>>(
+        p, w.perm, w.sel, static_cast<const float*>(w.act), w.slot_out, total);
+    note_launch(QMOE_KERNEL_FC2, s, false);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,
+                           cudaStream_t s) {
+    const int vec = (p.H & 3) == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(w.slot_out) & 15) == 0;
+    const int64_t n = vec ? p.T * (p.H / 4) : p.T * p.H;
+    note_launch(QMOE_KERNEL_COMBINE, s, true);
+    combine_kernel<<<blocks_for(n, 256), 256, 0, s>>>(w.slot_out, w.pw, p.y, p.T, p.H, int(p.k),
+                                                      splits, pl.slots, vec);
+    note_launch(QMOE_KERNEL_COMBINE, s, false);
+    return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,101 @@
+// Internal declarations shared by the host dispatcher and the kernel files.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmoe.h"
+
+namespace qmoe {
+
+// Problem description after host validation (QMoE manifest derive.*).
+struct Problem {
+    int64_t T = 0;        // derive.numTokens
+    int64_t H = 0;        // derive.hiddenSize
+    int64_t I = 0;        // derive.interSize
+    int64_t E = 0;        // dim(router_probs, 1)
+    int64_t k = 0;        // derive.topK
+    int bits = 4;         // derive.weightBits
+    int pack = 2;         // derive.packSize
+    int mid = 8;          // derive.quantMidpoint
+    int64_t bs = 0;       // derive.quantBlockSize (0 = column-wise)
+    int64_t nb1 = 1;      // derive.fc1ScaleBlocks
+    int64_t nb2 = 1;      // derive.fc2ScaleBlocks
+    int act = 0;          // 0 relu, 1 swiglu
+    int fusion = 1;       // derive.fusionSize
+    float alpha = 1.f, beta = 0.f;
+    int has_limit = 0;
+    float limit = 0.f;
+    int path = QMOE_PATH_GENERIC;
+    // device tensors
+    const float* x = nullptr;
+    const float* logits = nullptr;
+    const uint8_t* w1 = nullptr;
+    const float* s1 = nullptr;
+    const uint8_t* w2 = nullptr;
+    const float* s2 = nullptr;
+    float* y = nullptr;
+};
+
+// Sizes that depend only on the problem shape and path.
+struct Plan {
+    int64_t slots = 0;          // T * k
+    int64_t route_chunks = 0;   // CTAs of the routing kernel (tokens per chunk below)
+    int64_t Hp = 0;             // padded row length of the fp16 activations
+    int64_t Ip = 0;             // padded row length of the fp16 FC1 output
+    int64_t max_tiles = 0;      // expert token-tiles upper bound
+    int tile_tokens = 0;        // tokens per expert tile (grouped path)
+    int fc2_splits = 1;         // split-K factor of the decode FC2
+    size_t bytes = 0;           // total workspace bytes
+    // byte offsets into the workspace
+    size_t off_ctrl, off_sel, off_pw, off_counts, off_offsets, off_hist, off_rank, off_perm,
+        off_inv, off_tiles, off_active, off_x16, off_act, off_slot_out;
+};
+
+// Device views of the workspace.
+struct Work {
+    int32_t* ctrl;        // [0] device error word
+    int32_t* sel;         // [T*k] selected experts, selection order
+    float* pw;            // [T*k] routing weights
+    int32_t* counts;      // [E] slots per expert
+    int32_t* offsets;     // [E+1] exclusive scan of counts
+    int32_t* hist;        // [route_chunks*E] per-chunk counts, then chunk bases
+    int32_t* rank;        // [T*k] stable rank of a slot within its chunk and expert
+    int32_t* perm;        // [T*k] sorted position -> slot (t*k+i)
+    int32_t* inv;         // [T*k] slot -> sorted position
+    int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, 0)
+    int32_t* active;      // [E] experts with at least one slot, ascending
+    __half* x16;          // [T*Hp] fp16 copy of the activations
+    void* act;            // [T*k*Ip] FC1 output (fp16; fp32 on the generic path)
+    float* slot_out;      // [fc2_splits*T*k*H] per-slot FC2 output
+};
+
+constexpr int kRouteTokensPerChunk = 64;
+constexpr int kTileHeader = 4;  // tiles[0] = number of tiles, tiles[1] = active experts
+
+// Tuning constants of the paths.
+constexpr int kDecodeMaxTokens = 16;  // AUTO takes the decode path up to this many tokens
+
+// Host-side launch bookkeeping (profiling hooks, launch counter).
+// begin=true before the launch(es) of `kernel_id`, begin=false after them with
+// the number of kernels launched in between.
+void note_launch(int kernel_id, cudaStream_t stream, bool begin, int nkernels = 1);
+
+// Process-wide bound on a single in-kernel spin-wait, in nanoseconds.
+uint64_t wait_limit_ns();
+
+// ---- launchers (return cudaGetLastError()) ----
+cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,
+                         cudaStream_t s);
+cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,
+                           cudaStream_t s);
+cudaError_t launch_grouped_matmul(const void* input, int64_t M, int64_t K, const void* weights,
+                                  int64_t G, int64_t N, const void* idx, int64_t S, int idx64,
+                                  const void* bias, void* out, int dtype, int32_t* err,
+                                  cudaStream_t s);
+
+}  // namespace qmoe

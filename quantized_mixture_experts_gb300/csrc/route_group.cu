@@ -1,0 +1,313 @@
+// Routing (top-k + softmax over the selected logits) and expert grouping
+// (histogram, exclusive scan, stable permutation, tile table).
+//
+// QMoE manifest: `description` ("Routing uses the softmax over the selected
+// top-k logits"), attributeDescriptions.normalize_routing_weights (same
+// routing for 0 and 1), passes QMoE.RouteStage and QMoE.GroupStage
+// (intermediates routeExpert, routeMix, slotList, tileMeta;
+// derive.groupSlots, derive.groupMaxTiles).
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "qmoe_internal.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Total order of the selection: larger logit first, equal logits by lower index.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+// One warp selects the k best logits of row `row` (length E) in selection
+// order and writes experts, logits (temporarily) and routing weights.
+__device__ void route_one_token(const float* __restrict__ row, int E, int k, int32_t* sel,
+                                float* pw, int32_t* s_exp, int lane) {
+    float prev_v = 0.f;
+    int prev_i = -1;
+    float vmax = 0.f;
+    for (int i = 0; i < k; ++i) {
+        float best_v = 0.f;
+        int best_i = -1;
+        for (int e = lane; e < E; e += 32) {
+            float v = row[e];
+            bool after_prev = (prev_i < 0) || better(prev_v, prev_i, v, e);
+            if (after_prev && (best_i < 0 || better(v, e, best_v, best_i))) {
+                best_v = v;
+                best_i = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(kFull, best_v, off);
+            int oi = __shfl_xor_sync(kFull, best_i, off);
+            if (oi >= 0 && (best_i < 0 || better(ov, oi, best_v, best_i))) {
+                best_v = ov;
+                best_i = oi;
+            }
+        }
+        prev_v = best_v;
+        prev_i = best_i;
+        if (i == 0) vmax = best_v;
+        if (lane == 0) {
+            sel[i] = best_i;
+            pw[i] = best_v;
+            s_exp[i] = best_i;
+        }
+    }
+    __syncwarp();
+    // softmax over the k selected logits, max subtracted first
+    float part = 0.f;
+    for (int i = lane; i < k; i += 32) part += expf(pw[i] - vmax);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    __syncwarp();
+    for (int i = lane; i < k; i += 32) pw[i] = expf(pw[i] - vmax) / part;
+}
+
+// fp16 copy of one activation row, zero padded to Hp.  With interleave8 the
+// eight values of each aligned group are stored in the order
+// 0,4,1,5,2,6,3,7 (the operand order of the decode GEMV).
+__device__ void convert_row(const float* __restrict__ xr, int64_t H, __half* __restrict__ dst,
+                            int64_t Hp, int interleave8, int lane) {
+    if ((H & 7) == 0 && ((reinterpret_cast<uintptr_t>(xr) & 15) == 0)) {
+        for (int64_t g = lane; g < Hp / 8; g += 32) {
+            float v[8];
+            if (g * 8 < H) {
+                float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
+                float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = 0.f;
+            }
+            __half2 h[4];
+            if (interleave8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+            }
+            reinterpret_cast<uint4*>(dst)[g] = *reinterpret_cast<uint4*>(h);
+        }
+    } else {
+        for (int64_t j = lane; j < Hp; j += 32) {
+            int64_t src = j;
+            if (interleave8) {
+                int64_t base = j & ~int64_t(7);
+                int q = int(j & 7);
+                src = base + ((q & 1) ? 4 + (q >> 1) : (q >> 1));
+            }
+            dst[j] = __float2half_rn(src < H ? xr[src] : 0.f);
+        }
+    }
+}
+
+// One CTA per chunk of kRouteTokensPerChunk tokens.  Each warp routes tokens;
+// warp 0 then ranks the chunk's slots per expert (stable, in slot order) and
+// writes the chunk histogram.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(
+    const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
+    float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
+    const float* __restrict__ x, int64_t H, __half* __restrict__ x16, int64_t Hp,
+    int interleave8, int32_t* __restrict__ ctrl) {
+    extern __shared__ int32_t smem[];
+    int32_t* s_cnt = smem;        // [E]
+    int32_t* s_exp = smem + E;    // [chunk tokens * k]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = int64_t(blockIdx.x) * kRouteTokensPerChunk;
+    const int ntok = int(T - t0 < kRouteTokensPerChunk ? T - t0 : kRouteTokensPerChunk);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && ctrl) ctrl[0] = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    for (int lt = warp; lt < ntok; lt += kRouteThreads / 32) {
+        const int64_t t = t0 + lt;
+        route_one_token(logits + t * E, E, k, sel + t * k, pw + t * k, s_exp + lt * k, lane);
+        if (x16) convert_row(x + t * H, H, x16 + t * Hp, Hp, interleave8, lane);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nslots = ntok * k;
+        int32_t* rank_out = rank + t0 * k;
+        for (int base = 0; base < nslots; base += 32) {
+            const int j = base + lane;
+            const int e = j < nslots ? s_exp[j] : -1 - lane;   // distinct dummies
+            const unsigned mask = __match_any_sync(kFull, e);
+            const int leader = __ffs(mask) - 1;
+            const int r = __popc(mask & ((1u << lane) - 1u));
+            int c = (lane == leader && e >= 0) ? s_cnt[e] : 0;
+            c = __shfl_sync(kFull, c, leader);
+            if (e >= 0) rank_out[j] = c + r;
+            __syncwarp();
+            if (lane == leader && e >= 0) s_cnt[e] = c + __popc(mask);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[int64_t(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// Single CTA: per-expert totals, chunk bases (in place over `hist`), offsets,
+// active-expert list and the expert tile table.
+__global__ void __launch_bounds__(1024) group_scan_kernel(
+    int32_t* __restrict__ hist, int64_t chunks, int E, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ tiles, int32_t* __restrict__ active,
+    int tile_tokens) {
+    extern __shared__ int32_t sh[];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    // Phase 1: parts x experts partial sums.  P parts split the chunk range.
+    const int P = E >= nthr ? 1 : nthr / E;
+    int32_t* s_part = sh;                 // [P * E]
+    for (int e0 = 0; e0 < E; e0 += nthr / P) {
+        const int e = e0 + tid % (nthr / P);
+        const int part = tid / (nthr / P);
+        const bool on = (e < E) && (part < P) && (e - e0 < nthr / P);
+        const int64_t c_lo = chunks * part / P, c_hi = chunks * (part + 1) / P;
+        int32_t sum = 0;
+        if (on)
+            for (int64_t c = c_lo; c < c_hi; ++c) sum += hist[c * E + e];
+        if (on) s_part[part * E + e] = sum;
+    }
+    __syncthreads();
+    // Phase 2: exclusive scan over parts for each expert; totals.
+    for (int e = tid; e < E; e += nthr) {
+        int32_t run = 0;
+        for (int part = 0; part < P; ++part) {
+            int32_t v = s_part[part * E + e];
+            s_part[part * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+    }
+    __syncthreads();
+    // Phase 3: chunk bases within each part.
+    for (int e0 = 0; e0 < E; e0 += nthr / P) {
+        const int e = e0 + tid % (nthr / P);
+        const int part = tid / (nthr / P);
+        const bool on = (e < E) && (part < P) && (e - e0 < nthr / P);
+        if (on) {
+            const int64_t c_lo = chunks * part / P, c_hi = chunks * (part + 1) / P;
+            int32_t run = s_part[part * E + e];
+            for (int64_t c = c_lo; c < c_hi; ++c) {
+                int32_t v = hist[c * E + e];
+                hist[c * E + e] = run;
+                run += v;
+            }
+        }
+    }
+    __syncthreads();
+    // Phase 4: one warp scans counts -> offsets, tile bases, active list.
+    int32_t* s_tile_base = sh;            // reuse: [E]
+    if (tid < 32) {
+        const int lane = tid;
+        int32_t off_run = 0, tile_run = 0, act_run = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int32_t cnt = e < E ? counts[e] : 0;
+            const int32_t nt = tile_tokens > 0 ? (cnt + tile_tokens - 1) / tile_tokens : 0;
+            const int32_t is_act = cnt > 0 ? 1 : 0;
+            int32_t a = cnt, b = nt, c = is_act;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                int32_t ya = __shfl_up_sync(kFull, a, off);
+                int32_t yb = __shfl_up_sync(kFull, b, off);
+                int32_t yc = __shfl_up_sync(kFull, c, off);
+                if (lane >= off) { a += ya; b += yb; c += yc; }
+            }
+            if (e < E) {
+                offsets[e] = off_run + a - cnt;
+                s_tile_base[e] = tile_run + b - nt;
+                if (is_act) active[act_run + c - 1] = e;
+            }
+            off_run += __shfl_sync(kFull, a, 31);
+            tile_run += __shfl_sync(kFull, b, 31);
+            act_run += __shfl_sync(kFull, c, 31);
+        }
+        if (lane == 0) {
+            offsets[E] = off_run;
+            tiles[0] = tile_run;
+            tiles[1] = act_run;
+            tiles[2] = tile_tokens;
+            tiles[3] = 0;
+        }
+    }
+    __syncthreads();
+    // Phase 5: tile table entries (expert, first sorted row, rows, 0).
+    if (tile_tokens > 0) {
+        for (int e = tid; e < E; e += nthr) {
+            const int32_t cnt = counts[e];
+            const int32_t base = s_tile_base[e];
+            const int32_t row0 = offsets[e];
+            for (int32_t j = 0; j * tile_tokens < cnt; ++j) {
+                int32_t* tt = tiles + kTileHeader + 4 * (base + j);
+                tt[0] = e;
+                tt[1] = row0 + j * tile_tokens;
+                tt[2] = min(tile_tokens, cnt - j * tile_tokens);
+                tt[3] = 0;
+            }
+        }
+    }
+}
+
+// perm[pos] = slot, inv[slot] = pos, pos = offsets[e] + chunk base + rank.
+__global__ void group_scatter_kernel(const int32_t* __restrict__ sel,
+                                     const int32_t* __restrict__ rank,
+                                     const int32_t* __restrict__ hist,
+                                     const int32_t* __restrict__ offsets, int64_t slots, int k,
+                                     int E, int32_t* __restrict__ perm,
+                                     int32_t* __restrict__ inv) {
+    const int64_t s = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (s >= slots) return;
+    const int e = sel[s];
+    const int64_t chunk = (s / k) / kRouteTokensPerChunk;
+    const int32_t pos = offsets[e] + hist[chunk * E + e] + rank[s];
+    perm[pos] = int32_t(s);
+    inv[s] = pos;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,
+                         cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * (size_t(p.E) + size_t(kRouteTokensPerChunk) * p.k);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    note_launch(QMOE_KERNEL_ROUTE, s, true);
+    route_kernel<<<unsigned(pl.route_chunks), kRouteThreads, smem, s>>>(
+        p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
+        x16_interleaved ? 1 : 0, w.ctrl);
+    note_launch(QMOE_KERNEL_ROUTE, s, false);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
+    const int E = int(p.E);
+    const int nthr = 1024;
+    const int P = E >= nthr ? 1 : nthr / E;
+    const size_t smem = sizeof(int32_t) * std::max<size_t>(size_t(P) * E, size_t(E));
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(group_scan_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    note_launch(QMOE_KERNEL_GROUP, s, true);
+    group_scan_kernel<<<1, nthr, smem, s>>>(w.hist, pl.route_chunks, E, w.counts, w.offsets,
+                                            w.tiles, w.active, pl.tile_tokens);
+    const int64_t slots = pl.slots;
+    group_scatter_kernel<<<unsigned((slots + 255) / 256), 256, 0, s>>>(
+        w.sel, w.rank, w.hist, w.offsets, slots, int(p.k), E, w.perm, w.inv);
+    note_launch(QMOE_KERNEL_GROUP, s, false, 2);
+    return cudaGetLastError();
+}
+
+}  // namespace qmoe

@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load and export every function include/qmoe.h declares;
+attribute defaults must equal the QMoE manifest's `attributes`; shape and
+attribute validation (manifest derive.quantContract and
+attributeConstraints) must reject bad calls before anything is launched, so
+these calls never touch a device.
+"""
+import ctypes
+
+import pytest
+
+import __graft_entry__
+import quantized_mixture_experts_gb300 as q
+from quantized_mixture_experts_gb300 import binding as b
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return q.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = q.declared_functions()
+    assert "qmoe_forward" in names and "grouped_matmul" in names
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+
+
+def test_attr_defaults_match_manifest(lib):
+    a = b.Attrs()
+    lib.qmoe_attrs_default(ctypes.byref(a))
+    assert a.k == 1 and a.expert_weight_bits == 4 and a.activation_type == 0
+    assert a.block_size == 0 and a.swiglu_fusion == 0
+    assert a.activation_alpha == 1.0 and a.activation_beta == 0.0
+    assert a.has_swiglu_limit == 0 and a.normalize_routing_weights == 0
+    assert a.use_sparse_mixer == 0 and a.weights_prepacked == -1 and a.quant_type_is_int == 1
+    assert ctypes.sizeof(b.Attrs) == 64
+
+
+def _call(attrs, T=8, H=64, I=32, E=4, bits=4, bs=0, fusion=None, scales_rank=None,
+          router=None, fc2=None, s1=None, s2=None, input_shape=None, ws_bytes=1 << 30):
+    fusion = fusion if fusion is not None else (2 if attrs.activation_type == 1 else 1)
+    pack = 2 if bits == 4 else 1
+    input_shape = input_shape or (T, H)
+    router = router or (T, E)
+    fc1 = (E, fusion * I, H // pack)
+    fc2 = fc2 or (E, H, I // pack)
+    r = scales_rank or (3 if bs else 2)
+    s1 = s1 or ((E, fusion * I, H // bs) if bs else (E, fusion * I))
+    s2 = s2 or ((E, H, I // bs) if bs else (E, H))
+    fake = 0x1000  # never dereferenced: validation fails before any launch
+    return q.load().qmoe_forward(
+        fake, b._shape(input_shape), len(input_shape), fake, b._shape(router),
+        fake, b._shape(fc1), fake, b._shape(s1), r, fake, b._shape(fc2), fake, b._shape(s2), r,
+        fake, ctypes.byref(attrs), 0x10000, ws_bytes, None, None, None)
+
+
+def A(**kw):
+    return q.make_attrs(**kw)
+
+
+@pytest.mark.parametrize("kw,call,status", [
+    (dict(k=5), {}, b.ERR_INVALID_ARGUMENT),                       # k > E
+    (dict(k=0), {}, b.ERR_INVALID_ARGUMENT),                       # k < 1
+    (dict(k=2, block_size=24), {}, b.ERR_INVALID_ARGUMENT),        # not a power of two
+    (dict(k=2, block_size=8), {}, b.ERR_INVALID_ARGUMENT),         # below 16
+    (dict(k=2, block_size=64), dict(I=32), b.ERR_INVALID_ARGUMENT),  # does not divide inter
+    (dict(k=2, activation_type="swiglu", swiglu_fusion=0), {}, b.ERR_INVALID_ARGUMENT),
+    (dict(k=2, activation_type="relu", swiglu_fusion=1), {}, b.ERR_INVALID_ARGUMENT),
+    (dict(k=2, activation_type="swiglu", swiglu_fusion=2), {}, b.ERR_NOT_SUPPORTED),
+    (dict(k=2, activation_type="gelu"), {}, b.ERR_NOT_SUPPORTED),
+    (dict(k=2, expert_weight_bits=2), dict(bits=4), b.ERR_NOT_SUPPORTED),
+    (dict(k=2, use_sparse_mixer=1), {}, b.ERR_NOT_SUPPORTED),
+    (dict(k=2, weights_prepacked=1), {}, b.ERR_NOT_SUPPORTED),
+    (dict(k=2, weights_prepacked=3), {}, b.ERR_INVALID_ARGUMENT),
+    (dict(k=2, quant_type="fp4"), {}, b.ERR_NOT_SUPPORTED),
+    (dict(k=2, normalize_routing_weights=2), {}, b.ERR_INVALID_ARGUMENT),
+    (dict(k=2), dict(router=(7, 4)), b.ERR_INVALID_ARGUMENT),      # router rows != tokens
+    (dict(k=2), dict(fc2=(4, 64, 8)), b.ERR_INVALID_ARGUMENT),     # fc2 packed cols
+    (dict(k=2), dict(scales_rank=3, s1=(4, 32, 2), s2=(4, 64, 1)), b.ERR_INVALID_ARGUMENT),
+    (dict(k=2, block_size=16), dict(bs=16, scales_rank=2, s1=(4, 32), s2=(4, 64)),
+     b.ERR_INVALID_ARGUMENT),
+    (dict(k=2, block_size=16), dict(bs=16, s1=(4, 32, 3)), b.ERR_INVALID_ARGUMENT),
+    (dict(k=2), dict(input_shape=(2, 4, 64, 1)), b.ERR_INVALID_ARGUMENT),  # rank 4
+    (dict(k=2), dict(ws_bytes=16), b.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_contract_rejections(lib, kw, call, status):
+    assert _call(A(**kw), **call) == status
+
+
+def test_workspace_size_and_path(lib):
+    a = A(k=2, expert_weight_bits=4, block_size=32, activation_type="swiglu")
+    n = q.workspace_size((8, 4096), (8, 2 * 14336, 2048), a)
+    assert n > 0 and n % 256 == 0
+    nh = q.workspace_size((8, 4096), (8, 2 * 14336, 2048), a, hostio=True)
+    assert nh >= n + 8 * 4096 * 4 * 2
+    p = q.choose_path((8, 4096), (8, 2 * 14336, 2048), a)
+    assert p in (q.PATH_DECODE, q.PATH_GROUPED, q.PATH_GENERIC)
+    a.path = q.PATH_GENERIC
+    assert q.choose_path((8, 4096), (8, 2 * 14336, 2048), a) == q.PATH_GENERIC
+
+
+def test_gmm_rejections(lib):
+    ws = 0x10000
+    f = q.load().grouped_matmul
+    assert f(0x1000, -1, 2, 0x1000, 1, 1, 0x1000, 1, 0, None, 0x1000, 0, ws, 256, None) == \
+        b.ERR_INVALID_ARGUMENT
+    assert f(0x1000, 1, 2, 0x1000, 1, 1, 0x1000, 1, 7, None, 0x1000, 0, ws, 256, None) == \
+        b.ERR_INVALID_ARGUMENT
+    assert f(0x1000, 1, 2, 0x1000, 1, 1, 0x1000, 1, 0, None, 0x1000, 9, ws, 256, None) == \
+        b.ERR_INVALID_ARGUMENT
+    assert f(0x1000, 1, 2, 0x1000, 1, 1, 0x1000, 1, 0, None, 0x1000, 0, ws, 8, None) == \
+        b.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_status_strings(lib):
+    assert q.binding.status_string(0) == "ok"
+    assert "workspace" in q.binding.status_string(3)

@@ -1,0 +1,98 @@
+"""GPU parity of grouped_matmul (ONNX GroupedMatMul-29) through the C ABI.
+
+The page's worked examples run for every element type and index type; random
+cases are compared with the oracle under the bound of the accumulation type:
+|out - ref| <= c * eps_acc * K * sum_k |x_k||w_k| (+ output rounding for 16-bit
+outputs), with eps_acc = 2^-24 (fp32 accumulate) or 2^-53 (fp64).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "grouped_matmul_examples.json")
+DTYPES = {"f32": "float32", "f16": "float16", "bf16": "bfloat16", "f64": "float64"}
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _examples():
+    with open(GOLDEN) as f:
+        return json.load(f)["examples"]
+
+
+@pytest.mark.parametrize("dt", list(DTYPES))
+@pytest.mark.parametrize("idt", ["int32", "int64"])
+@pytest.mark.parametrize("ex", _examples(), ids=lambda e: e["name"])
+def test_page_examples(dev, ex, dt, idt):
+    import quantized_mixture_experts_gb300 as q
+    tdt = getattr(torch, DTYPES[dt])
+    if "expected" not in ex:
+        x = torch.zeros(ex["input_shape"], dtype=tdt, device=dev)
+        w = torch.zeros(ex["weights_shape"], dtype=tdt, device=dev)
+        idx = torch.zeros(ex["group_indices_shape"], dtype=getattr(torch, idt), device=dev)
+        out = q.grouped_matmul(x, w, idx)
+        torch.cuda.synchronize()
+        assert list(out.shape) == ex["expected_shape"]
+        return
+    x = torch.tensor(ex["input"], dtype=tdt, device=dev)
+    w = torch.tensor(ex["weights"], dtype=tdt, device=dev)
+    idx = torch.tensor(ex["group_indices"], dtype=getattr(torch, idt), device=dev)
+    bias = None if ex["bias"] is None else torch.tensor(ex["bias"], dtype=tdt, device=dev)
+    ws = q.alloc_workspace(256)
+    out = q.grouped_matmul(x, w, idx, bias, workspace=ws)
+    torch.cuda.synchronize()
+    exp = torch.tensor(ex["expected"], dtype=tdt).double().numpy()   # expected, rounded to T
+    np.testing.assert_array_equal(out.double().cpu().numpy(), exp)
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+
+
+@pytest.mark.parametrize("dt", list(DTYPES))
+@pytest.mark.parametrize("shape", [(37, 70, 5, 33, 3), (128, 256, 8, 96, 2), (1, 1, 1, 1, 1),
+                                   (65, 0, 3, 9, 2)])
+def test_random_vs_oracle(dev, dt, shape):
+    import quantized_mixture_experts_gb300 as q
+    M, K, G, N, S = shape
+    rng = np.random.default_rng(sum(shape))
+    tdt = getattr(torch, DTYPES[dt])
+    x = torch.from_numpy(rng.standard_normal((M, K))).to(tdt)
+    w = torch.from_numpy(rng.standard_normal((G, K, N))).to(tdt)
+    b = torch.from_numpy(rng.standard_normal((G, N))).to(tdt)
+    idx = torch.from_numpy(rng.integers(0, G, (M, S)))
+    out = q.grouped_matmul(x.to(dev), w.to(dev), idx.to(dev), b.to(dev))
+    torch.cuda.synchronize()
+    xr, wr, br = x.double().numpy(), w.double().numpy(), b.double().numpy()
+    ref, st = oracle.grouped_matmul(xr, wr, idx.numpy(), br)
+    assert st == oracle.OK
+    mag = np.einsum("mk,mskn->msn", np.abs(xr), np.abs(wr)[idx.numpy()]) + np.abs(br)[idx.numpy()]
+    eps_acc = 2.0 ** -53 if dt == "f64" else 2.0 ** -24
+    eps_out = {"f32": 2.0 ** -24, "f64": 2.0 ** -53, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dt]
+    bound = 2 * (K + 2) * eps_acc * mag + eps_out * np.abs(ref) + 1e-300
+    err = np.abs(out.double().cpu().numpy() - ref)
+    assert np.all(err <= bound), float(np.max(err / bound))
+
+
+def test_out_of_range_index_sets_error_and_zero_row(dev):
+    import quantized_mixture_experts_gb300 as q
+    x = torch.ones((3, 4), device=dev)
+    w = torch.ones((2, 4, 5), device=dev)
+    idx = torch.tensor([[0], [2], [-1]], dtype=torch.int64, device=dev)
+    ws = q.alloc_workspace(256)
+    out = q.grouped_matmul(x, w, idx, workspace=ws)
+    assert q.get_device_error(ws) == q.DEVERR_INDEX
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 4.0) and np.all(o[1] == 0.0) and np.all(o[2] == 0.0)
+    assert q.get_device_error(ws) == q.DEVERR_NONE   # read clears the word

@@ -1,0 +1,204 @@
+"""GPU parity of the QMoE layer against the fp64 oracle, through the C ABI.
+
+Small layers (several tiles, ragged tails) are compared on every token; the
+five benchmark workloads at full size are compared on every token (tiny,
+decode) or on a seeded token sample that touches every selected expert
+(prefill, many-small, large-E), in the launch configuration the bench uses.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import check_outputs, check_routing, run_cuda, to_dev
+from quantized_mixture_experts_gb300.workloads import WORKLOADS, Workload, make_inputs, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _paths(wl: Workload):
+    """Every kernel path that accepts this shape (AUTO included)."""
+    import quantized_mixture_experts_gb300 as q
+    out = []
+    for path in (q.PATH_AUTO, q.PATH_DECODE, q.PATH_GROUPED, q.PATH_GENERIC):
+        a = q.make_attrs(path=path, **wl.attrs())
+        try:
+            q.choose_path(wl.input_shape, (wl.experts, wl.fusion * wl.inter, wl.hidden // wl.pack),
+                          a)
+        except q.QmoeError as e:
+            assert e.status == q.binding.ERR_NOT_SUPPORTED
+            continue
+        out.append(path)
+    return out
+
+
+SMALL = [
+    WORKLOADS["tiny"],
+    Workload("ragged_swiglu_bs32", 20, (300, 256), 256, 192, 8, 2, 4, 32, "swiglu"),
+    Workload("relu_8bit_col", 21, (100, 128), 128, 128, 16, 4, 8, 0, "relu"),
+    Workload("k1_bs64", 22, (40, 128), 128, 64, 6, 1, 4, 64, "swiglu"),
+    Workload("k_eq_E_8bit_bs16", 23, (24, 64), 64, 64, 4, 4, 8, 16, "swiglu"),
+    Workload("limit_alpha_beta", 24, (50, 128), 128, 64, 8, 2, 4, 0, "swiglu",
+             alpha=1.7, beta=0.3, swiglu_limit=0.4),
+    Workload("decode_like", 25, (8, 512), 512, 1024, 8, 2, 4, 32, "swiglu", logit_sigma=2.0),
+    Workload("prefill_like_rank3", 26, (2, 96, 256), 256, 256, 8, 2, 4, 128, "swiglu",
+             logit_sigma=2.0),
+    Workload("many_small_like", 27, (256, 256), 256, 128, 64, 8, 8, 0, "swiglu", zipf_s=1.1),
+    Workload("large_e_like", 28, (2, 256, 256), 256, 128, 128, 8, 4, 64, "swiglu"),
+    Workload("odd_hidden_generic", 29, (33, 48), 48, 32, 5, 2, 4, 16, "swiglu"),
+]
+
+
+def _small_cases():
+    cases = []
+    for wl in SMALL:
+        for path in _paths(wl):
+            cases.append(pytest.param(wl, path, id=f"{wl.name}-p{path}"))
+    return cases
+
+
+_ref_cache = {}
+
+
+def _reference(wl: Workload, inp: dict, tokens=None):
+    key = (wl.name, None if tokens is None else tuple(tokens.tolist()))
+    if key not in _ref_cache:
+        _ref_cache[key] = oracle.qmoe(inp["input"], inp["router_probs"],
+                                      inp["fc1_experts_weights"], inp["fc1_scales"],
+                                      inp["fc2_experts_weights"], inp["fc2_scales"],
+                                      tokens=tokens, nthreads=os.cpu_count() or 1, **wl.attrs())
+    return _ref_cache[key]
+
+
+@pytest.mark.parametrize("wl,path", _small_cases())
+def test_small_parity_all_tokens(dev, wl, path):
+    inp = make_inputs(wl)
+    y_ref, sel_ref, p_ref = _reference(wl, inp)
+    y, sel, p = run_cuda(inp, wl.attrs(), path, dev)
+    check_routing(sel, p, sel_ref, p_ref, wl.name)
+    check_outputs(y, y_ref, f"{wl.name} path {path}")
+    if wl.k == 1:
+        assert np.all(p == 1.0)
+
+
+def test_repeat_is_bit_identical(dev):
+    wl = SMALL[1]
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    a = run_cuda(inp, wl.attrs(), 0, dev, t=t)
+    b = run_cuda(inp, wl.attrs(), 0, dev, t=t)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+def test_zero_scales_exact_zero(dev):
+    wl = SMALL[1]
+    inp = make_inputs(wl)
+    inp["fc1_scales"] = np.zeros_like(inp["fc1_scales"])
+    for path in _paths(wl):
+        y, _, _ = run_cuda(inp, dict(wl.attrs(), activation_beta=0.5), path, dev)
+        assert np.all(y == 0.0), path
+
+
+def test_zero_tokens_is_noop(dev):
+    import quantized_mixture_experts_gb300 as q
+    wl = WORKLOADS["tiny"].with_tokens(0)
+    inp = make_inputs(WORKLOADS["tiny"])
+    inp["input"] = np.zeros((0, 64), np.float32)
+    inp["router_probs"] = np.zeros((0, 4), np.float32)
+    t = to_dev(inp, dev)
+    y = q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], t["fc1_scales"],
+                       t["fc2_experts_weights"], t["fc2_scales"], **wl.attrs())
+    torch.cuda.synchronize()
+    assert y.shape == (0, 64)
+
+
+def test_inter_zero_writes_zeros(dev):
+    import quantized_mixture_experts_gb300 as q
+    T, H, E = 12, 64, 4
+    x = torch.randn(T, H, device=dev)
+    lg = torch.randn(T, E, device=dev)
+    w1 = torch.zeros((E, 0, H // 2), dtype=torch.uint8, device=dev)
+    s1 = torch.zeros((E, 0), device=dev)
+    w2 = torch.zeros((E, H, 0), dtype=torch.uint8, device=dev)
+    s2 = torch.zeros((E, H), device=dev)
+    y = torch.full((T, H), 3.0, device=dev)
+    sel = torch.full((T, 2), -1, dtype=torch.int32, device=dev)
+    q.qmoe_forward(x, lg, w1, s1, w2, s2, output=y, topk_idx=sel, k=2)
+    torch.cuda.synchronize()
+    assert torch.all(y == 0)
+    ref_sel, _ = oracle.route(lg.cpu().numpy(), 2)
+    assert np.array_equal(sel.cpu().numpy(), ref_sel)
+
+
+def test_hostio_matches_device_path(dev):
+    import quantized_mixture_experts_gb300 as q
+    wl = SMALL[6]
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(**wl.attrs())
+    y_dev = q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"],
+                           t["fc1_scales"], t["fc2_experts_weights"], t["fc2_scales"],
+                           attrs=attrs)
+    hx = torch.from_numpy(inp["input"]).pin_memory()
+    hl = torch.from_numpy(inp["router_probs"]).pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape,
+                                            attrs, hostio=True))
+    q.qmoe_forward_hostio(hx, hl, t["fc1_experts_weights"], t["fc1_scales"],
+                          t["fc2_experts_weights"], t["fc2_scales"], hy, attrs=attrs,
+                          workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(hy.numpy(), y_dev.cpu().numpy())
+
+
+def test_device_error_clean_after_forward(dev):
+    import quantized_mixture_experts_gb300 as q
+    wl = SMALL[1]
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(**wl.attrs())
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape, attrs))
+    ws.fill_(0xAB)   # stale garbage: the call must clear its error word
+    q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], t["fc1_scales"],
+                   t["fc2_experts_weights"], t["fc2_scales"], attrs=attrs, workspace=ws)
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads
+# ----------------------------------------------------------------------------
+
+FULL = ["tiny", "decode", "prefill", "many_small", "large_e"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_parity(dev, name):
+    import quantized_mixture_experts_gb300 as q
+    wl = WORKLOADS[name]
+    path = q.choose_path(wl.input_shape, (wl.experts, wl.fusion * wl.inter, wl.hidden // wl.pack),
+                         q.make_attrs(**wl.attrs()))
+    if wl.tokens > 64 and path == q.PATH_GENERIC:
+        pytest.skip("full-size run needs a tensor-core path for this shape")
+    inp = make_inputs(wl)
+    y, sel, p = run_cuda(inp, wl.attrs(), q.PATH_AUTO, dev)
+    sel_all, p_all = oracle.route(inp["router_probs"], wl.k)
+    check_routing(sel, p, sel_all, p_all, name + " (all tokens)")
+    tokens = None if wl.tokens <= 64 else sample_tokens(sel_all, wl.tokens, 256,
+                                                        seed=1234 + wl.index)
+    y_ref, sel_ref, p_ref = _reference(wl, inp, tokens)
+    if tokens is not None:
+        y, sel, p = y[tokens], sel[tokens], p[tokens]
+    check_routing(sel, p, sel_ref, p_ref, name)
+    check_outputs(y, y_ref, name)
