@@ -1,0 +1,424 @@
+"""Throughput of the GB300 QMoE layer on one synthetic workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+One step is one full qmoe_forward call (routing, grouping, FC1 + activation,
+FC2, combine) over one batch of the workload's tokens, with inputs and
+weights resident in HBM.  `value` is whole-job tokens/s.  `e2e` measures the
+same metric through qmoe_forward_hostio: page-locked host activations and
+logits copied in, the layer, and the output copied back, every step.
+Under torchrun each rank runs an independent replica (weak scaling; the
+layer has no cross-GPU exchange); the elapsed time is the max over ranks.
+
+`--impl reference` times the CPU oracle (the double-precision C restatement
+of the operator pages) on the host cores on a bounded token sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_mixture_experts_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "QMoE layer tokens/sec"
+UNIT = "tokens/s"
+DEFAULT_STEPS = {"tiny": 2000, "decode": 8000, "prefill": 100, "many_small": 1000,
+                 "large_e": 100}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic work (bytes and FLOPs the method must move or compute)
+# ----------------------------------------------------------------------------
+
+def expert_bytes(wl, which):
+    """Packed weight + scale bytes of one expert for FC1 or FC2."""
+    H, I, f, pk = wl.hidden, wl.inter, wl.fusion, wl.pack
+    if which == 1:
+        rows, K, nb = f * I, H, (H // wl.block_size if wl.block_size else 1)
+    else:
+        rows, K, nb = H, I, (I // wl.block_size if wl.block_size else 1)
+    return rows * (K // pk) + rows * nb * 4
+
+
+def layer_flops(wl, slots):
+    return 2.0 * slots * (wl.fusion * wl.inter * wl.hidden + wl.hidden * wl.inter)
+
+
+def fc1_flops(wl, slots):
+    return 2.0 * slots * wl.fusion * wl.inter * wl.hidden
+
+
+# ----------------------------------------------------------------------------
+# Clocks during the timed region
+# ----------------------------------------------------------------------------
+
+QUERY = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv"), "w") \
+                if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
+                open(f"/tmp/.qmoe_clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.out is not None:
+            self.out.close()
+
+    def summary(self):
+        if self.out is None or self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.out.name) as f:
+            for r in csv.reader(f):
+                r = [x.strip() for x in r]
+                if len(r) < 10:
+                    continue
+                if self.uuid and self.uuid not in r[1]:
+                    continue
+                rows.append(r)
+        try:
+            os.remove(self.out.name)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        loaded = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# Measured peaks and the ncu traffic record
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "quantized_mixture_experts_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(profile_name, kernel_files):
+    """Per-launch DRAM bytes recorded under profiles/, if the kernel source still
+    matches the one the counters were taken from."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_sha(kernel_files):
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ----------------------------------------------------------------------------
+
+def run_reference(args, wl):
+    import oracle
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return
+    inp = make_inputs(wl)
+    cores = os.cpu_count() or 1
+    sample = min(wl.tokens, 16)
+    rng = np.random.default_rng(7)
+    times = []
+    for step in range(args.warmup + args.steps):
+        tok = np.sort(rng.choice(wl.tokens, size=sample, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.qmoe(inp["input"], inp["router_probs"], inp["fc1_experts_weights"],
+                    inp["fc1_scales"], inp["fc2_experts_weights"], inp["fc2_scales"],
+                    tokens=tok, nthreads=cores, **wl.attrs())
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = sample * len(times) / total
+    used = min(cores, sample)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": f"{sample} of {wl.tokens} tokens per step, seeded"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(wl):
+    return {"workload": f"QMoE {wl.name}", "input_shape": list(wl.input_shape),
+            "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
+            "experts": wl.experts, "k": wl.k, "bits": wl.bits,
+            "block_size": wl.block_size or "column-wise", "activation": wl.activation}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline (oracle) beside the GPU number
+# ----------------------------------------------------------------------------
+
+def cpu_baseline(wl, inp):
+    import oracle
+    cores = os.cpu_count() or 1
+    sample = min(wl.tokens, 16)
+    tok = np.arange(sample, dtype=np.int64) if sample == wl.tokens else \
+        np.sort(np.random.default_rng(3).choice(wl.tokens, size=sample, replace=False))
+    t0 = time.perf_counter()
+    oracle.qmoe(inp["input"], inp["router_probs"], inp["fc1_experts_weights"], inp["fc1_scales"],
+                inp["fc2_experts_weights"], inp["fc2_scales"], tokens=tok.astype(np.int64),
+                nthreads=cores, **wl.attrs())
+    dt = time.perf_counter() - t0
+    return {"value": sample / dt, "unit": UNIT, "cores": min(cores, sample), "kind": "oracle",
+            "sample": f"{sample} of {wl.tokens} tokens, {dt:.2f} s"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import quantized_mixture_experts_gb300 as q
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    q.load()
+
+    inp = make_inputs(wl, salt=rank)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    attrs = q.make_attrs(**wl.attrs())
+    path = q.choose_path(wl.input_shape, tuple(t["fc1_experts_weights"].shape), attrs)
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, tuple(t["fc1_experts_weights"].shape),
+                                            attrs), dev)
+    y = torch.empty_like(t["input"])
+    sel = torch.empty((wl.tokens, wl.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], t["fc1_scales"],
+                       t["fc2_experts_weights"], t["fc2_scales"], attrs=attrs, output=y,
+                       workspace=ws, topk_idx=sel, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    err = q.get_device_error(ws, stream)
+    touched = int(torch.unique(sel).numel())
+
+    bound = "hbm" if path == q.PATH_DECODE else "tensor"
+    dominant = q.KERNEL_FC1
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = q.launch_count()
+    q.profile_begin(dominant)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    n_launch, fc1_ms = q.profile_end()
+    launches = q.launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    tokens_total = wl.tokens * args.steps * world
+    value = tokens_total / (elapsed_ms / 1e3)
+
+    # end to end through the host-IO entry point
+    hx = torch.from_numpy(inp["input"]).pin_memory()
+    hl = torch.from_numpy(inp["router_probs"]).pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    ws_io = q.alloc_workspace(q.workspace_size(wl.input_shape,
+                                               tuple(t["fc1_experts_weights"].shape), attrs,
+                                               hostio=True), dev)
+    e2e_steps = max(1, min(args.steps, 2000))
+
+    def step_io():
+        q.qmoe_forward_hostio(hx, hl, t["fc1_experts_weights"], t["fc1_scales"],
+                              t["fc2_experts_weights"], t["fc2_scales"], hy, attrs=attrs,
+                              workspace=ws_io, stream=stream)
+        stream.synchronize()
+
+    for _ in range(3):
+        step_io()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_io()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = wl.tokens * e2e_steps * world / e2e_s
+    if not np.array_equal(hy.numpy(), y.cpu().numpy()):
+        raise RuntimeError("host-IO output differs from the device-resident output")
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks = measured_peaks()
+    avg_ms = fc1_ms / max(1, n_launch)
+    if bound == "hbm":
+        per_unit = expert_bytes(wl, 1)
+        algo = per_unit * touched + wl.tokens * wl.hidden * 2
+        achieved = algo / (avg_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+        profile_name = "decode_fc1_decode.md"
+        files = ["gemv_decode.cu", "ptx.cuh"]
+    else:
+        slots = wl.tokens * wl.k
+        algo = fc1_flops(wl, slots)
+        achieved = algo / (avg_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] if args.steps * avg_ms > 1000 else peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+        profile_name = f"grouped_fc1_{wl.name}.md"
+        files = ["gemm_tc.cu", "ptx.cuh"]
+    traffic = ncu_traffic(profile_name, files) if os.path.exists(
+        os.path.join(ROOT, "quantized_mixture_experts_gb300", "csrc", files[0])) else None
+
+    cfg = config_dict(wl)
+    cfg.update({"path": q.PATH_NAMES.get(path, str(path)), "touched_experts": touched,
+                "l2": ("weights of touched experts exceed the 129 MB L2; no flush"
+                       if expert_bytes(wl, 1) * touched > L2_BYTES else "L2 flush not applied"),
+                "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                "logits_sigma": wl.logit_sigma, "device_error": err})
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; random packed weights)", "config": cfg,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak if peak else None, "traffic": traffic,
+                     "kernel": "FC1", "kernel_ms": avg_ms, "launches": n_launch,
+                     "algorithmic": algo, "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(inp["input"].nbytes + inp["router_probs"].nbytes),
+                "d2h_bytes_per_step": int(inp["input"].nbytes), "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = 10 if args.impl == "reference" else DEFAULT_STEPS[wl.name]
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -142,16 +142,20 @@ qmoe_status check_shapes(const Problem& p, const int64_t* router_shape,
     return QMOE_OK;
 }
 
-// Whether the tensor-core paths can take this shape (fast-path alignment).
-bool fast_shape_ok(const Problem& p) {
-    (void)p;
-    return false;   // tensor-core paths not built yet
+// Whether a kernel path can take this shape.
+bool path_ok(const Problem& p, int path) {
+    switch (path) {
+        case QMOE_PATH_GENERIC: return true;
+        case QMOE_PATH_DECODE: return decode_shape_ok(p);
+        default: return false;
+    }
 }
 
 int choose_path(const Problem& p, int requested) {
     if (requested != QMOE_PATH_AUTO) return requested;
-    if (!fast_shape_ok(p)) return QMOE_PATH_GENERIC;
-    return p.T <= kDecodeMaxTokens ? QMOE_PATH_DECODE : QMOE_PATH_GROUPED;
+    if (p.T <= kDecodeMaxTokens && path_ok(p, QMOE_PATH_DECODE)) return QMOE_PATH_DECODE;
+    if (path_ok(p, QMOE_PATH_GROUPED)) return QMOE_PATH_GROUPED;
+    return QMOE_PATH_GENERIC;
 }
 
 qmoe_status make_plan(const Problem& p, Plan* pl) {
@@ -162,7 +166,7 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.Ip = round_up(std::max<int64_t>(p.I, 1), 64);
     q.tile_tokens = 0;
     q.max_tiles = 0;
-    q.fc2_splits = 1;
+    q.fc2_splits = p.path == QMOE_PATH_DECODE ? decode_fc2_splits(p) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -216,8 +220,7 @@ qmoe_status plan_for(const int64_t* input_shape, int32_t input_rank, const int64
     qmoe_status st = derive(input_shape, input_rank, fc1_w_shape, attrs, p);
     if (st != QMOE_OK) return st;
     p->path = choose_path(*p, attrs->path);
-    if ((p->path == QMOE_PATH_DECODE || p->path == QMOE_PATH_GROUPED) && !fast_shape_ok(*p))
-        return QMOE_ERR_NOT_SUPPORTED;
+    if (!path_ok(*p, p->path)) return QMOE_ERR_NOT_SUPPORTED;
     return make_plan(*p, pl);
 }
 
@@ -254,6 +257,14 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             if ((e = launch_generic_fc1(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_generic_fc2(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_combine(p, pl, w, 1, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            return QMOE_OK;
+        }
+        case QMOE_PATH_DECODE: {
+            if ((e = launch_route(p, pl, w, p.bits == 4, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_decode_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_decode_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_combine(p, pl, w, pl.fc2_splits, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             return QMOE_OK;
         }
         default:

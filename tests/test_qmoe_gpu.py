@@ -58,6 +58,14 @@ SMALL = [
     Workload("many_small_like", 27, (256, 256), 256, 128, 64, 8, 8, 0, "swiglu", zipf_s=1.1),
     Workload("large_e_like", 28, (2, 256, 256), 256, 128, 128, 8, 4, 64, "swiglu"),
     Workload("odd_hidden_generic", 29, (33, 48), 48, 32, 5, 2, 4, 16, "swiglu"),
+    # decode-sized layers: 8-bit, column-wise, ReLU, two token tiles per expert,
+    # partial K chunk, block sizes 16/64/128, clamp
+    Workload("decode_8bit_col_relu", 30, (12, 256), 256, 384, 6, 2, 8, 0, "relu"),
+    Workload("decode_bs16_two_tiles", 31, (16, 640), 640, 256, 2, 2, 4, 16, "swiglu"),
+    Workload("decode_bs128_k1", 32, (5, 1024), 1024, 512, 16, 1, 4, 128, "swiglu"),
+    Workload("decode_8bit_bs64", 33, (9, 512), 512, 256, 4, 3, 8, 64, "swiglu"),
+    Workload("decode_limit", 34, (4, 256), 256, 256, 4, 2, 4, 0, "swiglu", alpha=1.3,
+             beta=-0.2, swiglu_limit=0.3),
 ]
 
 
