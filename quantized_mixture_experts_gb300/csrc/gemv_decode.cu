@@ -30,16 +30,23 @@
 namespace qmoe {
 namespace {
 
-constexpr int kDecConsumers = 8;
+constexpr int kDecRowGroups = 8;               // 16-row MMA groups per unit
+constexpr int kDecConsumers = 2 * kDecRowGroups; // two K halves per row group
 constexpr int kDecThreads = 32 * (1 + kDecConsumers);
-constexpr int kDecStages = 3;
-constexpr int kDecRows = 16 * kDecConsumers;   // 128 weight rows per unit
+constexpr int kDecStages = 4;                  // upper bound; the launch picks what fits
+constexpr int kDecRows = 16 * kDecRowGroups;   // 128 weight rows per unit
+constexpr int kDecRedBytes = 2 * kDecRowGroups * 32 * 8 * 4;
 constexpr int kChunkBytes = 256;               // packed bytes per row per stage
 constexpr int kBoxBytes = 128;                 // one 128-byte swizzle span
 constexpr int kBoxTile = kBoxBytes * kDecRows; // 16 KB per weight box
 constexpr int kDecMaxTokens = 16;
 constexpr int kTargetUnitsPerSm = 10;
 constexpr unsigned kFull = 0xffffffffu;
+
+// Where the dequantization scale is applied.
+constexpr int kScaleCol = 0;    // column-wise: once per output, after the K loop
+constexpr int kScalePost = 1;   // block-wise, each 32-K MMA pair inside one block: fp32 per pair
+constexpr int kScalePre = 2;    // block size 16 with 4-bit codes: fp16 weights pre-scaled
 
 struct DecodeArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], 128B swizzle
@@ -54,7 +61,7 @@ struct DecodeArgs {
     const int32_t* tiles;       // tiles[1] = number of touched experts
     int64_t N, K;
     int topk, n_rb, nkc, splits, cps, lbs, nsc;
-    uint32_t stage_bytes, off_s, off_b, pitch_b;
+    uint32_t stage_bytes, off_s, off_b, pitch_b, nstages;
     __half* act_out;
     int64_t act_pitch;
     int act, interleave8, has_limit;
@@ -70,10 +77,20 @@ __device__ __forceinline__ void record_error(int32_t* err, int code) {
 }
 
 // Eight 4-bit codes of `w` (low nibble first) -> four fp16 pairs
-// ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) of (q - 8) * scale.  1024 + q is built
-// exactly by OR-ing the nibble into the fp16 mantissa of 1024.
-__device__ __forceinline__ void dequant4(uint32_t w, __half2 s, uint32_t* h) {
+// ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) holding q - 8 exactly: 1024 + q is built
+// by OR-ing the nibble into the mantissa of fp16 1024, then 1032 is subtracted.
+__device__ __forceinline__ void dequant4(uint32_t w, uint32_t* h) {
     const __half2 bias = ptx::u32_as_h2(0x64086408u);   // (1032, 1032)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
+        h[q] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(v), bias));
+    }
+}
+
+// As dequant4, multiplied by the fp16 scale (for block sizes below 32).
+__device__ __forceinline__ void dequant4_scaled(uint32_t w, __half2 s, uint32_t* h) {
+    const __half2 bias = ptx::u32_as_h2(0x64086408u);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
@@ -81,13 +98,13 @@ __device__ __forceinline__ void dequant4(uint32_t w, __half2 s, uint32_t* h) {
     }
 }
 
-// Four 8-bit codes -> two fp16 pairs ((q0,q1),(q2,q3)) of (q - 128) * scale.
-__device__ __forceinline__ void dequant8(uint32_t w, __half2 s, uint32_t* h) {
+// Four 8-bit codes -> two fp16 pairs ((q0,q1),(q2,q3)) holding q - 128 exactly.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t* h) {
     const __half2 bias = ptx::u32_as_h2(0x64806480u);   // (1152, 1152)
     const uint32_t lo = ptx::prmt(w, 0x64646464u, 0x4140u);
     const uint32_t hi = ptx::prmt(w, 0x64646464u, 0x4342u);
-    h[0] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(lo), bias), s));
-    h[1] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(hi), bias), s));
+    h[0] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(lo), bias));
+    h[1] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(hi), bias));
 }
 
 __device__ __forceinline__ float swiglu(float g, float u, float alpha, float beta, int has_limit,
@@ -106,22 +123,29 @@ __device__ __forceinline__ int64_t perm8(int64_t j) {
     return (j & ~int64_t(7)) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
 }
 
-template <int BITS, bool SCOL, bool FC1>
+template <int BITS, int SMODE, bool FC1>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[kDecStages];
     __shared__ __align__(8) uint64_t empty_bar[kDecStages];
+    __shared__ __align__(8) uint64_t red_full[2];    // K-half 1 -> K-half 0 partial sums
+    __shared__ __align__(8) uint64_t red_empty[2];
     __shared__ int abort_flag;
     constexpr int KC = kChunkBytes * (BITS == 4 ? 2 : 1);   // K values per chunk
     constexpr int SEGK = BITS == 4 ? 128 : 64;              // K values per 64-byte segment
+    constexpr bool SCOL = SMODE == kScaleCol;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kDecStages; ++s) {
+        for (uint32_t s = 0; s < a.nstages; ++s) {
             ptx::mbar_init(&full_bar[s], 1);
             ptx::mbar_init(&empty_bar[s], kDecConsumers);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&red_full[s], kDecRowGroups);
+            ptx::mbar_init(&red_empty[s], kDecRowGroups);
         }
         abort_flag = 0;
         ptx::fence_mbar_init();
@@ -151,13 +175,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             int64_t brow = 0;
             if (lane < ne) brow = FC1 ? int64_t(a.perm[off + lane] / a.topk) : int64_t(off + lane);
             for (int kc = c0; kc < c1; ++kc, ++it) {
-                const int st = int(it % kDecStages);
-                const uint32_t ph = (it / kDecStages) & 1u;
+                const int st = int(it % a.nstages);
+                const uint32_t ph = (it / a.nstages) & 1u;
                 if (!ptx::mbar_wait(&empty_bar[st], ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int kvalid = int(a.K - int64_t(kc) * KC < KC ? a.K - int64_t(kc) * KC : KC);
+                const int64_t krem = a.K - int64_t(kc) * KC;
+                const int kvalid = int(krem < KC ? krem : KC);
                 uint8_t* sbase = smem + size_t(st) * a.stage_bytes;
                 const uint32_t bbytes = uint32_t(kvalid) * 2u;
                 if (lane == 0) {
@@ -177,27 +202,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                                   &full_bar[st]);
             }
         }
-        if (!ok) {
-            if (lane == 0) {
-                record_error(a.err, QMOE_DEVERR_TIMEOUT);
-                abort_flag = 1;
-                // drain copies still in flight (bounded) before the CTA exits
-                for (uint32_t j = it > kDecStages ? it - kDecStages : 0; j < it; ++j) {
-                    volatile int never = 0;
-                    ptx::mbar_wait(&full_bar[j % kDecStages], (j / kDecStages) & 1u, a.wait_ns,
-                                   &never);
-                }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+            // drain copies still in flight (bounded) before the CTA exits
+            for (uint32_t j = it > a.nstages ? it - a.nstages : 0; j < it; ++j) {
+                volatile int never = 0;
+                ptx::mbar_wait(&full_bar[j % a.nstages], (j / a.nstages) & 1u, a.wait_ns, &never);
             }
         }
         return;
     }
 
     // -------------------------------- consumers --------------------------------
+    // Warps 1..16: row group rgi (16 rows) x K half kh (alternate 64-byte segments).
     const int cw = warp - 1;
+    const int rgi = cw % kDecRowGroups, kh = cw / kDecRowGroups;
     const int g = lane >> 2, c = lane & 3;
-    const int r_g = 16 * cw + g;   // row of this thread inside the 128-row box (and r_g + 8)
+    const int r_g = 16 * rgi + g;   // row of this thread inside the 128-row box (and r_g + 8)
+    float* red = reinterpret_cast<float*>(smem + size_t(a.nstages) * a.stage_bytes);
+    const uint32_t sbase0 = ptx::smem_u32(smem);
     uint32_t it = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    uint32_t un = 0;   // units processed by this CTA (reduction buffer parity)
+    // B fragments keep stale values for token columns >= ne; those columns of
+    // the MMA result are never stored.
+    uint4 bq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++un) {
         const int ks = int(u % a.splits);
         const int rb = int((u / a.splits) % a.n_rb);
         const int ai = int(u / (int64_t(a.splits) * a.n_rb));
@@ -207,22 +237,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
         const int c0 = ks * a.cps, c1 = min(a.nkc, c0 + a.cps);
         const int64_t rg = int64_t(rb) * kDecRows + r_g;   // row within the expert
         const int64_t rg8 = rg + 8;
-        __half2 scol_g = __float2half2_rn(0.f), scol_g8 = scol_g;
+        float scol_g = 1.f, scol_g8 = 1.f;
         if (SCOL) {
             const float* sc = a.scales_col + int64_t(e) * a.N;
-            scol_g = __float2half2_rn(rg < a.N ? sc[rg] : 0.f);
-            scol_g8 = __float2half2_rn(rg8 < a.N ? sc[rg8] : 0.f);
+            scol_g = rg < a.N ? sc[rg] : 0.f;
+            scol_g8 = rg8 < a.N ? sc[rg8] : 0.f;
         }
-        float acc[2][4];
+        float acc[2][4], accB[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] = 0.f;
+            for (int q = 0; q < 4; ++q) acc[nt][q] = accB[nt][q] = 0.f;
         const bool two = ne > 8;
+        const bool ld0 = g < ne, ld1 = g + 8 < ne;
 
         for (int kc = c0; kc < c1; ++kc, ++it) {
-            const int st = int(it % kDecStages);
-            const uint32_t ph = (it / kDecStages) & 1u;
+            const int st = int(it % a.nstages);
+            const uint32_t ph = (it / a.nstages) & 1u;
             if (!ptx::mbar_wait(&full_bar[st], ph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -230,65 +261,150 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                 }
                 return;
             }
-            const uint8_t* sA = smem + size_t(st) * a.stage_bytes;
-            const float* sS = reinterpret_cast<const float*>(sA + a.off_s);
-            const uint8_t* sB = sA + a.off_b;
-            const int kvalid = int(a.K - int64_t(kc) * KC < KC ? a.K - int64_t(kc) * KC : KC);
-            const int nseg = kvalid / SEGK;
-            for (int s = 0; s < nseg; ++s) {
-                const int jchunk = ((s & 1) << 2) + c;
-                const uint32_t offA = uint32_t(s >> 1) * kBoxTile + uint32_t((jchunk ^ g) << 4);
-                const uint4 wg = *reinterpret_cast<const uint4*>(sA + offA + r_g * kBoxBytes);
-                const uint4 wg8 = *reinterpret_cast<const uint4*>(sA + offA + (r_g + 8) * kBoxBytes);
-                const uint32_t wv[4] = {wg.x, wg.y, wg.z, wg.w};
-                const uint32_t wv8[4] = {wg8.x, wg8.y, wg8.z, wg8.w};
-                __half2 sc_g = scol_g, sc_g8 = scol_g8;
-                int si_prev = -1;
+            const uint32_t sA = ptx::launder(sbase0 + uint32_t(st) * a.stage_bytes);
+            const uint32_t sS = sA + a.off_s;
+            const uint32_t sB = sA + a.off_b;
+            const uint32_t rowA = sA + uint32_t(r_g) * kBoxBytes;
+            const uint32_t rowA8 = rowA + 8u * kBoxBytes;
+            const int64_t krem = a.K - int64_t(kc) * KC;
+            const int nseg = int(krem < KC ? krem : KC) / SEGK;
+            for (int s = kh; s < nseg; s += 2) {
+                const uint32_t half = uint32_t(s >> 1) * kBoxTile;
+                float sgv[4], sg8v[4];
+                if (SMODE == kScalePost) {
+                    // word i of every lane lies in scale block (SEGK*s + SEGK/4*i) >> lbs;
+                    // the seg spans 4, 2 or 1 blocks (block sizes SEGK/4, SEGK/2, >= SEGK)
+                    const int nbs = SEGK >> a.lbs;   // blocks per segment (0 when bs > SEGK)
+                    const int si0 = (SEGK * s) >> a.lbs;
+                    const uint32_t a0 = sS + uint32_t(r_g * a.nsc + si0) * 4u;
+                    const uint32_t a8 = a0 + uint32_t(8 * a.nsc) * 4u;
+                    if (nbs >= 4) {
+                        const float4 v0 = ptx::ld_f32x4(a0), v8 = ptx::ld_f32x4(a8);
+                        sgv[0] = v0.x; sgv[1] = v0.y; sgv[2] = v0.z; sgv[3] = v0.w;
+                        sg8v[0] = v8.x; sg8v[1] = v8.y; sg8v[2] = v8.z; sg8v[3] = v8.w;
+                    } else if (nbs == 2) {
+                        const float2 v0 = ptx::ld_f32x2(a0), v8 = ptx::ld_f32x2(a8);
+                        sgv[0] = sgv[1] = v0.x; sgv[2] = sgv[3] = v0.y;
+                        sg8v[0] = sg8v[1] = v8.x; sg8v[2] = sg8v[3] = v8.y;
+                    } else {
+                        const float v0 = ptx::ld_f32(a0), v8 = ptx::ld_f32(a8);
+                        sgv[0] = sgv[1] = sgv[2] = sgv[3] = v0;
+                        sg8v[0] = sg8v[1] = sg8v[2] = sg8v[3] = v8;
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int kin = BITS == 4 ? (SEGK * s + 32 * c + 8 * i) : (SEGK * s + 16 * c + 4 * i);
-                    if (!SCOL) {
-                        // the block index changes with i in the same way for every lane
-                        const int si = kin >> a.lbs;
-                        if (si != si_prev) {
-                            sc_g = __float2half2_rn(sS[r_g * a.nsc + si]);
-                            sc_g8 = __float2half2_rn(sS[(r_g + 8) * a.nsc + si]);
-                            si_prev = si;
-                        }
-                    }
+                    // word i of lane c: packed bytes 16i + 4c of this 64-byte segment
+                    const int jchunk = ((s & 1) << 2) + i;
+                    const uint32_t offw = half + uint32_t((jchunk ^ g) << 4) + uint32_t(c) * 4u;
+                    const uint32_t wa = ptx::ld_u32(rowA + offw);
+                    const uint32_t wb = ptx::ld_u32(rowA8 + offw);
+                    const int kin = BITS == 4 ? (SEGK * s + 32 * i + 8 * c) : (SEGK * s + 16 * i + 4 * c);
+                    const uint32_t boff = uint32_t(kin) * 2u;
                     if (BITS == 4) {
                         uint32_t hg[4], hg8[4];
-                        dequant4(wv[i], sc_g, hg);
-                        dequant4(wv8[i], sc_g8, hg8);
+                        if (SMODE == kScalePre) {
+                            const int si = kin >> a.lbs;
+                            const __half2 s0 = __float2half2_rn(ptx::ld_f32(sS + uint32_t(r_g * a.nsc + si) * 4u));
+                            const __half2 s8 = __float2half2_rn(ptx::ld_f32(sS + uint32_t((r_g + 8) * a.nsc + si) * 4u));
+                            dequant4_scaled(wa, s0, hg);
+                            dequant4_scaled(wb, s8, hg8);
+                        } else {
+                            dequant4(wa, hg);
+                            dequant4(wb, hg8);
+                        }
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             if (nt == 1 && !two) break;
-                            const int tok = nt * 8 + g;
-                            uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-                            if (tok < ne)
-                                bv = *reinterpret_cast<const uint4*>(sB + tok * a.pitch_b + kin * 2);
-                            ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bv.x, bv.y);
-                            ptx::mma_16816(acc[nt], hg[2], hg8[2], hg[3], hg8[3], bv.z, bv.w);
+                            ptx::ld128_pred(bq[nt], sB + uint32_t(g + 8 * nt) * a.pitch_b + boff,
+                                            nt == 0 ? ld0 : ld1);
+                            if (SMODE == kScalePost) {
+                                float tmp[4];
+                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
+                                ptx::mma_16816(tmp, hg[2], hg8[2], hg[3], hg8[3], bq[nt].z, bq[nt].w);
+                                acc[nt][0] = fmaf(sgv[i], tmp[0], acc[nt][0]);
+                                acc[nt][1] = fmaf(sgv[i], tmp[1], acc[nt][1]);
+                                acc[nt][2] = fmaf(sg8v[i], tmp[2], acc[nt][2]);
+                                acc[nt][3] = fmaf(sg8v[i], tmp[3], acc[nt][3]);
+                            } else {
+                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
+                                ptx::mma_16816(accB[nt], hg[2], hg8[2], hg[3], hg8[3], bq[nt].z, bq[nt].w);
+                            }
                         }
                     } else {
                         uint32_t hg[2], hg8[2];
-                        dequant8(wv[i], sc_g, hg);
-                        dequant8(wv8[i], sc_g8, hg8);
+                        dequant8(wa, hg);
+                        dequant8(wb, hg8);
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             if (nt == 1 && !two) break;
-                            const int tok = nt * 8 + g;
-                            uint2 bv = make_uint2(0u, 0u);
-                            if (tok < ne)
-                                bv = *reinterpret_cast<const uint2*>(sB + tok * a.pitch_b + kin * 2);
-                            ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bv.x, bv.y);
+                            ptx::ld64_pred(bq[nt].x, bq[nt].y,
+                                           sB + uint32_t(g + 8 * nt) * a.pitch_b + boff,
+                                           nt == 0 ? ld0 : ld1);
+                            if (SMODE == kScalePost) {
+                                float tmp[4];
+                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
+                                acc[nt][0] = fmaf(sgv[i], tmp[0], acc[nt][0]);
+                                acc[nt][1] = fmaf(sgv[i], tmp[1], acc[nt][1]);
+                                acc[nt][2] = fmaf(sg8v[i], tmp[2], acc[nt][2]);
+                                acc[nt][3] = fmaf(sg8v[i], tmp[3], acc[nt][3]);
+                            } else if (i & 1) {
+                                ptx::mma_16816(accB[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
+                            } else {
+                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
+                            }
                         }
                     }
                 }
             }
+            // every shared load of this stage feeds the accumulators: finish them first
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    ptx::depend(acc[nt][q]);
+                    ptx::depend(accB[nt][q]);
+                }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty_bar[st]);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[nt][q] += accB[nt][q];
+            if (SCOL) {
+                acc[nt][0] *= scol_g; acc[nt][1] *= scol_g;
+                acc[nt][2] *= scol_g8; acc[nt][3] *= scol_g8;
+            }
+        }
+
+        // ---- K-half 1 hands its partial sums to K-half 0 through shared memory ----
+        const int rb_buf = int(un & 1u);
+        const uint32_t rph = (un >> 1) & 1u;
+        float* slot = red + ((rb_buf * kDecRowGroups + rgi) * 32 + lane) * 8;
+        if (kh == 1) {
+            if (!ptx::mbar_wait(&red_empty[rb_buf], rph ^ 1u, a.wait_ns, &abort_flag)) {
+                if (lane == 0) { record_error(a.err, QMOE_DEVERR_TIMEOUT); abort_flag = 1; }
+                return;
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) slot[nt * 4 + q] = acc[nt][q];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&red_full[rb_buf]);
+            continue;
+        }
+        if (!ptx::mbar_wait(&red_full[rb_buf], rph, a.wait_ns, &abort_flag)) {
+            if (lane == 0) { record_error(a.err, QMOE_DEVERR_TIMEOUT); abort_flag = 1; }
+            return;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[nt][q] += slot[nt * 4 + q];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&red_empty[rb_buf]);
 
         // -------------------------------- epilogue --------------------------------
         if (FC1) {
@@ -349,8 +465,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                 for (int q = 0; q < 2; ++q) {
                     const int n = nt * 8 + 2 * c + q;
                     if (n >= ne) continue;
-                    const int64_t slot = a.perm[off + n];
-                    float* dst = a.slot_out + (int64_t(ks) * a.slots + slot) * a.N;
+                    const int64_t slot_id = a.perm[off + n];
+                    float* dst = a.slot_out + (int64_t(ks) * a.slots + slot_id) * a.N;
                     if (rg < a.N) dst[rg] = acc[nt][q];
                     if (rg8 < a.N) dst[rg8] = acc[nt][2 + q];
                 }
@@ -359,9 +475,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     }
 }
 
-template <int BITS, bool SCOL, bool FC1>
+template <int BITS, int SMODE, bool FC1>
 cudaError_t launch_variant(const DecodeArgs& args, int grid, size_t smem, cudaStream_t s) {
-    auto kern = decode_gemv_kernel<BITS, SCOL, FC1>;
+    auto kern = decode_gemv_kernel<BITS, SMODE, FC1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, kDecThreads, smem, s>>>(args);
@@ -438,10 +554,12 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     a.cps = (a.nkc + a.splits - 1) / a.splits;
     const uint32_t bytes_a = 2 * kBoxTile;
     const uint32_t bytes_s = scol ? 0u : uint32_t(kDecRows) * a.nsc * 4u;
-    a.pitch_b = uint32_t(KC * 2 + 16);
+    // token-row pitch chosen so that one quarter/half warp reads distinct banks
+    a.pitch_b = uint32_t(KC * 2 + (p.bits == 4 ? 64 : 32));
     a.off_s = bytes_a;
     a.off_b = bytes_a + ((bytes_s + 127u) & ~127u);
-    a.stage_bytes = (a.off_b + kDecMaxTokens * a.pitch_b + 1023u) & ~1023u;
+    const int max_tok = int(std::min<int64_t>(p.T, kDecMaxTokens));
+    a.stage_bytes = (a.off_b + uint32_t(max_tok) * a.pitch_b + 1023u) & ~1023u;
     a.act_out = static_cast<__half*>(w.act);
     a.act_pitch = pl.Ip;
     a.act = p.act;
@@ -454,20 +572,26 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     a.slots = pl.slots;
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
-    const size_t smem = 1024 + size_t(kDecStages) * a.stage_bytes;
+    const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
+    a.nstages = uint32_t(std::min<size_t>(kDecStages, (smem_cap - 1024 - kDecRedBytes) / a.stage_bytes));
+    if (a.nstages < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes + kDecRedBytes;
     const int64_t experts = std::min<int64_t>(p.E, pl.slots);
     const int64_t units_max = experts * a.n_rb * a.splits;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(units_max, device_sm_count())));
     const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
     note_launch(kid, s, true);
     cudaError_t e;
+    const int smode = scol ? kScaleCol : (p.bits == 4 && p.bs < 32 ? kScalePre : kScalePost);
+#define QMOE_DEC_LAUNCH(B, M) \
+    (fc1 ? launch_variant<B, M, true>(a, grid, smem, s) : launch_variant<B, M, false>(a, grid, smem, s))
     if (p.bits == 4) {
-        if (scol) e = fc1 ? launch_variant<4, true, true>(a, grid, smem, s) : launch_variant<4, true, false>(a, grid, smem, s);
-        else e = fc1 ? launch_variant<4, false, true>(a, grid, smem, s) : launch_variant<4, false, false>(a, grid, smem, s);
+        e = smode == kScaleCol ? QMOE_DEC_LAUNCH(4, kScaleCol)
+            : smode == kScalePost ? QMOE_DEC_LAUNCH(4, kScalePost) : QMOE_DEC_LAUNCH(4, kScalePre);
     } else {
-        if (scol) e = fc1 ? launch_variant<8, true, true>(a, grid, smem, s) : launch_variant<8, true, false>(a, grid, smem, s);
-        else e = fc1 ? launch_variant<8, false, true>(a, grid, smem, s) : launch_variant<8, false, false>(a, grid, smem, s);
+        e = smode == kScaleCol ? QMOE_DEC_LAUNCH(8, kScaleCol) : QMOE_DEC_LAUNCH(8, kScalePost);
     }
+#undef QMOE_DEC_LAUNCH
     note_launch(kid, s, false);
     return e;
 }

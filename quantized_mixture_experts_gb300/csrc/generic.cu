@@ -117,11 +117,25 @@ __global__ void combine_kernel(const float* __restrict__ slot_out, const float* 
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int i = 0; i < k; ++i) {
             const float w = pw[t * k + i];
+            const float4* src = reinterpret_cast<const float4*>(slot_out + (t * k + i) * H) + d4;
+            const int64_t sstride = slots * H / 4;
             float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < splits; ++sp) {
-                const float4 v = reinterpret_cast<const float4*>(
-                    slot_out + (int64_t(sp) * slots + t * k + i) * H)[d4];
-                part.x += v.x; part.y += v.y; part.z += v.z; part.w += v.w;
+            if (splits <= 8) {
+                // issue every split's load first; the sum stays in split order
+                float4 v[8];
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp)
+                    if (sp < splits) v[sp] = __ldg(src + sp * sstride);
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp)
+                    if (sp < splits) {
+                        part.x += v[sp].x; part.y += v[sp].y; part.z += v[sp].z; part.w += v[sp].w;
+                    }
+            } else {
+                for (int sp = 0; sp < splits; ++sp) {
+                    const float4 v = __ldg(src + sp * sstride);
+                    part.x += v.x; part.y += v.y; part.z += v.z; part.w += v.w;
+                }
             }
             acc.x += w * part.x; acc.y += w * part.y; acc.z += w * part.z; acc.w += w * part.w;
         }
@@ -168,8 +182,9 @@ cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int 
                     (reinterpret_cast<uintptr_t>(w.slot_out) & 15) == 0;
     const int64_t n = vec ? p.T * (p.H / 4) : p.T * p.H;
     note_launch(QMOE_KERNEL_COMBINE, s, true);
-    combine_kernel<<<blocks_for(n, 256), 256, 0, s>>>(w.slot_out, w.pw, p.y, p.T, p.H, int(p.k),
-                                                      splits, pl.slots, vec);
+    const int threads = n < 152 * 256 ? 64 : 256;   // spread small batches over more SMs
+    combine_kernel<<<blocks_for(n, threads), threads, 0, s>>>(w.slot_out, w.pw, p.y, p.T, p.H,
+                                                              int(p.k), splits, pl.slots, vec);
     note_launch(QMOE_KERNEL_COMBINE, s, false);
     return cudaGetLastError();
 }

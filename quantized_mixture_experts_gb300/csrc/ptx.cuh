@@ -96,6 +96,94 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Shared loads that the compiler may reorder among themselves.  Their address
+// must derive from launder() of a value produced after the mbarrier wait that
+// guards the data, which keeps them after that wait.
+__device__ __forceinline__ uint32_t launder(uint32_t x) {
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(x) : "memory");
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(uint32_t addr) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_f32x4(uint32_t addr) {
+    float4 v;
+    asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_f32x2(uint32_t addr) {
+    float2 v;
+    asm("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float ld_f32(uint32_t addr) {
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void ld128_pred(uint4& v, uint32_t addr, bool p) {
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+        "@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "r"(addr), "r"(uint32_t(p)));
+}
+
+__device__ __forceinline__ void ld64_pred(uint32_t& x, uint32_t& y, uint32_t addr, bool p) {
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+        "@q ld.shared.v2.u32 {%0,%1}, [%2];\n\t}"
+        : "+r"(x), "+r"(y)
+        : "r"(addr), "r"(uint32_t(p)));
+}
+
+// Orders everything that produced `v` before the next volatile statement.
+__device__ __forceinline__ void depend(float v) { asm volatile("" ::"f"(v) : "memory"); }
+
+// Loads when p is set; otherwise the destination keeps its previous value.
+__device__ __forceinline__ void lds128_pred(uint4& v, uint32_t addr, bool p) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+        "@q ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n\t}"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "r"(addr), "r"(uint32_t(p)));
+}
+
+__device__ __forceinline__ void lds64_pred(uint32_t& x, uint32_t& y, uint32_t addr, bool p) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+        "@q ld.shared.v2.u32 {%0,%1}, [%2];\n\t}"
+        : "+r"(x), "+r"(y)
+        : "r"(addr), "r"(uint32_t(p)));
+}
+
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t r;
@@ -119,11 +207,21 @@ __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
 // D = A(16x16, f16, row) * B(16x8, f16, col) + C (f32).
 __device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A * B with a zero accumulator.
+__device__ __forceinline__ void mma_16816_z(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
 }  // namespace ptx

@@ -260,8 +260,13 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             return QMOE_OK;
         }
         case QMOE_PATH_DECODE: {
-            if ((e = launch_route(p, pl, w, p.bits == 4, s)) != cudaSuccess) return QMOE_ERR_CUDA;
-            if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if (small_route_ok(p, pl)) {
+                if ((e = launch_route_group_small(p, pl, w, p.bits == 4, s)) != cudaSuccess)
+                    return QMOE_ERR_CUDA;
+            } else {
+                if ((e = launch_route(p, pl, w, p.bits == 4, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            }
             if ((e = launch_decode_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_decode_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_combine(p, pl, w, pl.fc2_splits, s)) != cudaSuccess) return QMOE_ERR_CUDA;

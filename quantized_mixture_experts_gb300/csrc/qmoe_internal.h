@@ -89,6 +89,11 @@ uint64_t wait_limit_ns();
 cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,
                          cudaStream_t s);
 cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+// Routing and grouping in a single launch for small batches.
+constexpr int kSmallRouteSlots = 4096;
+bool small_route_ok(const Problem& p, const Plan& pl);
+cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Work& w,
+                                     bool x16_interleaved, cudaStream_t s);
 cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,

@@ -69,49 +69,53 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
     for (int i = lane; i < k; i += 32) pw[i] = expf(pw[i] - vmax) / part;
 }
 
-// fp16 copy of one activation row, zero padded to Hp.  With interleave8 the
-// eight values of each aligned group are stored in the order
-// 0,4,1,5,2,6,3,7 (the operand order of the decode GEMV).
-__device__ void convert_row(const float* __restrict__ xr, int64_t H, __half* __restrict__ dst,
-                            int64_t Hp, int interleave8, int lane) {
-    if ((H & 7) == 0 && ((reinterpret_cast<uintptr_t>(xr) & 15) == 0)) {
-        for (int64_t g = lane; g < Hp / 8; g += 32) {
-            float v[8];
+// fp16 copy of rows [t0, t0+ntok) of the activations, columns [g_lo, g_hi)
+// in groups of eight, zero padded to Hp.  With interleave8 the eight values of
+// each aligned group are stored in the order 0,4,1,5,2,6,3,7 (the operand
+// order of the decode GEMV).  Threads stride over the (row, group) pairs.
+__device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, int64_t H,
+                             __half* __restrict__ x16, int64_t Hp, int interleave8, int64_t g_lo,
+                             int64_t g_hi, int tid, int nthr) {
+    const int64_t width = g_hi - g_lo;
+    if (width <= 0) return;
+    const int64_t total = int64_t(ntok) * width;
+    const bool vec = (H & 7) == 0 && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+#pragma unroll 4
+    for (int64_t idx = tid; idx < total; idx += nthr) {
+        const int64_t t = t0 + idx / width;
+        const int64_t g = g_lo + idx % width;
+        const float* __restrict__ xr = x + t * H;
+        float v[8];
+        if (vec) {
             if (g * 8 < H) {
-                float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
-                float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
+                const float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
+                const float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
                 v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
                 v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
             } else {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) v[q] = 0.f;
             }
-            __half2 h[4];
-            if (interleave8) {
+        } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
-            } else {
+            for (int q = 0; q < 8; ++q) v[q] = (g * 8 + q < H) ? xr[g * 8 + q] : 0.f;
+        }
+        __half2 h[4];
+        if (interleave8) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
-            }
-            reinterpret_cast<uint4*>(dst)[g] = *reinterpret_cast<uint4*>(h);
+            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
         }
-    } else {
-        for (int64_t j = lane; j < Hp; j += 32) {
-            int64_t src = j;
-            if (interleave8) {
-                int64_t base = j & ~int64_t(7);
-                int q = int(j & 7);
-                src = base + ((q & 1) ? 4 + (q >> 1) : (q >> 1));
-            }
-            dst[j] = __float2half_rn(src < H ? xr[src] : 0.f);
-        }
+        reinterpret_cast<uint4*>(x16 + t * Hp)[g] = *reinterpret_cast<uint4*>(h);
     }
 }
 
-// One CTA per chunk of kRouteTokensPerChunk tokens.  Each warp routes tokens;
-// warp 0 then ranks the chunk's slots per expert (stable, in slot order) and
-// writes the chunk histogram.
+// Grid (chunks, conv_split).  CTA (c, 0) routes the chunk's tokens (one warp
+// per token), then warp 0 ranks the chunk's slots per expert (stable, in slot
+// order) and writes the chunk histogram.  Every CTA (c, y) also converts its
+// share of the chunk's activation columns to fp16.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
     float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
@@ -123,12 +127,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = int64_t(blockIdx.x) * kRouteTokensPerChunk;
     const int ntok = int(T - t0 < kRouteTokensPerChunk ? T - t0 : kRouteTokensPerChunk);
+    if (x16) {
+        const int64_t G8 = Hp / 8;
+        const int64_t per = (G8 + gridDim.y - 1) / gridDim.y;
+        const int64_t g_lo = int64_t(blockIdx.y) * per;
+        const int64_t g_hi = g_lo + per < G8 ? g_lo + per : G8;
+        convert_rows(x, t0, ntok, H, x16, Hp, interleave8, g_lo, g_hi, threadIdx.x, blockDim.x);
+    }
+    if (blockIdx.y != 0) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && ctrl) ctrl[0] = 0;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
     for (int lt = warp; lt < ntok; lt += kRouteThreads / 32) {
         const int64_t t = t0 + lt;
         route_one_token(logits + t * E, E, k, sel + t * k, pw + t * k, s_exp + lt * k, lane);
-        if (x16) convert_row(x + t * H, H, x16 + t * Hp, Hp, interleave8, lane);
     }
     __syncthreads();
     if (warp == 0) {
@@ -150,6 +161,112 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[int64_t(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// Whole routing + grouping for small batches in one launch.  CTA 0 (1024
+// threads) routes every token, ranks the slots per expert, scans the counts
+// and writes offsets, the active-expert list, the tile table and the
+// permutation; CTAs 1.. convert the activations to fp16.
+__global__ void __launch_bounds__(1024) route_group_small_kernel(
+    const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
+    float* __restrict__ pw, const float* __restrict__ x, int64_t H, __half* __restrict__ x16,
+    int64_t Hp, int interleave8, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ tiles, int32_t* __restrict__ active, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int tile_tokens, int32_t* __restrict__ ctrl) {
+    extern __shared__ int32_t smem[];
+    if (blockIdx.x > 0) {
+        if (x16) {
+            const int64_t G8 = Hp / 8;
+            const int64_t nconv = gridDim.x - 1;
+            const int64_t total = T * G8;
+            const int64_t per = (total + nconv - 1) / nconv;
+            const int64_t lo = int64_t(blockIdx.x - 1) * per;
+            const int64_t hi = lo + per < total ? lo + per : total;
+            // rows are whole groups; walk the flat (token, group) range
+            for (int64_t idx = lo + threadIdx.x; idx < hi; idx += blockDim.x)
+                convert_rows(x, idx / G8, 1, H, x16, Hp, interleave8, idx % G8, idx % G8 + 1, 0, 1);
+        }
+        return;
+    }
+    const int slots = int(T) * k;
+    int32_t* s_cnt = smem;              // [E]
+    int32_t* s_off = s_cnt + E;         // [E + 1]
+    int32_t* s_tb = s_off + E + 1;      // [E]
+    int32_t* s_exp = s_tb + E;          // [slots]
+    int32_t* s_rank = s_exp + slots;    // [slots]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0 && ctrl) ctrl[0] = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    for (int t = warp; t < T; t += nw)
+        route_one_token(logits + int64_t(t) * E, E, k, sel + int64_t(t) * k, pw + int64_t(t) * k,
+                        s_exp + t * k, lane);
+    __syncthreads();
+    if (warp == 0) {
+        for (int base = 0; base < slots; base += 32) {
+            const int j = base + lane;
+            const int e = j < slots ? s_exp[j] : -1 - lane;
+            const unsigned mask = __match_any_sync(kFull, e);
+            const int leader = __ffs(mask) - 1;
+            const int r = __popc(mask & ((1u << lane) - 1u));
+            int c = (lane == leader && e >= 0) ? s_cnt[e] : 0;
+            c = __shfl_sync(kFull, c, leader);
+            if (e >= 0) s_rank[j] = c + r;
+            __syncwarp();
+            if (lane == leader && e >= 0) s_cnt[e] = c + __popc(mask);
+            __syncwarp();
+        }
+        int32_t off_run = 0, tile_run = 0, act_run = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int32_t cnt = e < E ? s_cnt[e] : 0;
+            const int32_t nt = tile_tokens > 0 ? (cnt + tile_tokens - 1) / tile_tokens : 0;
+            const int32_t is_act = cnt > 0 ? 1 : 0;
+            int32_t a = cnt, b = nt, c = is_act;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t ya = __shfl_up_sync(kFull, a, off);
+                const int32_t yb = __shfl_up_sync(kFull, b, off);
+                const int32_t yc = __shfl_up_sync(kFull, c, off);
+                if (lane >= off) { a += ya; b += yb; c += yc; }
+            }
+            if (e < E) {
+                s_off[e] = off_run + a - cnt;
+                s_tb[e] = tile_run + b - nt;
+                counts[e] = cnt;
+                offsets[e] = off_run + a - cnt;
+                if (is_act) active[act_run + c - 1] = e;
+            }
+            off_run += __shfl_sync(kFull, a, 31);
+            tile_run += __shfl_sync(kFull, b, 31);
+            act_run += __shfl_sync(kFull, c, 31);
+        }
+        if (lane == 0) {
+            s_off[E] = off_run;
+            offsets[E] = off_run;
+            tiles[0] = tile_run;
+            tiles[1] = act_run;
+            tiles[2] = tile_tokens;
+            tiles[3] = 0;
+        }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < slots; j += blockDim.x) {
+        const int32_t pos = s_off[s_exp[j]] + s_rank[j];
+        perm[pos] = j;
+        inv[j] = pos;
+    }
+    if (tile_tokens > 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int32_t cnt = s_cnt[e];
+            for (int32_t j = 0; j * tile_tokens < cnt; ++j) {
+                int32_t* tt = tiles + kTileHeader + 4 * (s_tb[e] + j);
+                tt[0] = e;
+                tt[1] = s_off[e] + j * tile_tokens;
+                tt[2] = min(tile_tokens, cnt - j * tile_tokens);
+                tt[3] = 0;
+            }
+        }
+    }
 }
 
 // Single CTA: per-expert totals, chunk bases (in place over `hist`), offsets,
@@ -281,10 +398,37 @@ cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
+    // split the fp16 conversion of each chunk over several CTAs (~256 groups of 8 each)
+    int ysplit = 1;
+    if (w.x16) ysplit = int(std::min<int64_t>(32, std::max<int64_t>(1, (pl.Hp / 8) / 256)));
     note_launch(QMOE_KERNEL_ROUTE, s, true);
-    route_kernel<<<unsigned(pl.route_chunks), kRouteThreads, smem, s>>>(
+    route_kernel<<<dim3(unsigned(pl.route_chunks), unsigned(ysplit)), kRouteThreads, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
         x16_interleaved ? 1 : 0, w.ctrl);
+    note_launch(QMOE_KERNEL_ROUTE, s, false);
+    return cudaGetLastError();
+}
+
+bool small_route_ok(const Problem& p, const Plan& pl) {
+    return pl.slots <= kSmallRouteSlots && p.E <= 1024;
+}
+
+cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Work& w,
+                                     bool x16_interleaved, cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * (3 * size_t(p.E) + 1 + 2 * size_t(pl.slots));
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_group_small_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    int conv = 0;
+    if (w.x16) conv = int(std::min<int64_t>(64, std::max<int64_t>(1, p.T * (pl.Hp / 8) / 2048)));
+    note_launch(QMOE_KERNEL_ROUTE, s, true);
+    route_group_small_kernel<<<unsigned(1 + conv), 1024, smem, s>>>(
+        p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, p.x, p.H, w.x16, pl.Hp,
+        x16_interleaved ? 1 : 0, w.counts, w.offsets, w.tiles, w.active, w.perm, w.inv,
+        pl.tile_tokens, w.ctrl);
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
 }
