@@ -180,6 +180,44 @@ qmoe_status qmoe_forward_hostio(const float *host_input, const int64_t *input_sh
                                 float *host_output, const qmoe_attrs *attrs,
                                 void *workspace, size_t workspace_bytes, void *cuda_stream);
 
+/*
+ * qmoe_forward for callers that cannot allocate device memory -- for example
+ * an extension hosted by a runtime that owns the whole device memory pool and
+ * gives its plugins no allocator, or a latency-critical loop that cannot
+ * afford the implicit device synchronization of cudaMalloc.  The operator
+ * pages define no such call; it is an addition of this library.
+ *
+ * Same arguments and results as qmoe_forward, without the workspace: the
+ * layer's scratch is a fixed array of qmoe_noalloc_scratch_bytes() (4 MiB)
+ * compiled into the library's device image, so every GPU that loads the
+ * library holds that memory until the process exits.  The call allocates
+ * nothing and calls no allocating routine.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - Shapes whose qmoe_workspace_size exceeds the array are rejected with
+ *    QMOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (decode-sized
+ *    batches fit; large prefill batches do not).
+ *  - Every call uses the same array, which keeps the previous call's
+ *    contents (the layer rewrites everything it reads, including the device
+ *    error word).  Calls that can overlap on the GPU -- different streams, or
+ *    host threads without ordering -- race on it and must be serialized by
+ *    the caller.  qmoe_get_device_error is not available for these calls.
+ */
+size_t qmoe_noalloc_scratch_bytes(void);
+
+qmoe_status qmoe_forward_noalloc(const float *input, const int64_t *input_shape,
+                                 int32_t input_rank,
+                                 const float *router_probs, const int64_t *router_shape,
+                                 const uint8_t *fc1_w, const int64_t *fc1_w_shape,
+                                 const float *fc1_scales, const int64_t *fc1_scales_shape,
+                                 int32_t fc1_scales_rank,
+                                 const uint8_t *fc2_w, const int64_t *fc2_w_shape,
+                                 const float *fc2_scales, const int64_t *fc2_scales_shape,
+                                 int32_t fc2_scales_rank,
+                                 float *output, const qmoe_attrs *attrs,
+                                 int32_t *topk_idx_out, float *topk_w_out, void *cuda_stream);
+
 /* Element types of grouped_matmul (GroupedMatMul-29, Type Constraints). */
 typedef enum { QMOE_DT_F32 = 0, QMOE_DT_F16 = 1, QMOE_DT_BF16 = 2, QMOE_DT_F64 = 3 } qmoe_dtype;
 typedef enum { QMOE_IDX_I32 = 0, QMOE_IDX_I64 = 1 } qmoe_index_dtype;

@@ -87,6 +87,10 @@ def load():
     lib.qmoe_forward.restype = ctypes.c_int
     lib.qmoe_forward_hostio.argtypes = fwd + [P]
     lib.qmoe_forward_hostio.restype = ctypes.c_int
+    lib.qmoe_noalloc_scratch_bytes.argtypes = []
+    lib.qmoe_noalloc_scratch_bytes.restype = SZ
+    lib.qmoe_forward_noalloc.argtypes = fwd[:-2] + [P, P, P]
+    lib.qmoe_forward_noalloc.restype = ctypes.c_int
     lib.grouped_matmul_workspace_size.argtypes = [ctypes.POINTER(SZ)]
     lib.grouped_matmul_workspace_size.restype = ctypes.c_int
     lib.grouped_matmul.argtypes = [P, I64, I64, P, I64, I64, P, I64, I32, P, P, I32, P, SZ, P]
@@ -222,6 +226,23 @@ def qmoe_forward(input, router_probs, fc1_experts_weights, fc1_scales, fc2_exper
         _ptr(output), ctypes.byref(attrs), _ptr(workspace), workspace.numel(),
         _ptr(topk_idx), _ptr(topk_w), _stream(stream))
     _check(st, "qmoe_forward")
+    return output
+
+
+def qmoe_forward_noalloc(input, router_probs, fc1_experts_weights, fc1_scales,
+                         fc2_experts_weights, fc2_scales, *, attrs: Attrs, output,
+                         topk_idx=None, topk_w=None, stream=None):
+    """qmoe_forward_noalloc: the layer with the library's fixed scratch array
+    instead of a workspace, for callers that cannot allocate device memory."""
+    st = load().qmoe_forward_noalloc(
+        _ptr(input), _shape(input.shape), input.dim(),
+        _ptr(router_probs), _shape(router_probs.shape),
+        _ptr(fc1_experts_weights), _shape(fc1_experts_weights.shape),
+        _ptr(fc1_scales), _shape(fc1_scales.shape), fc1_scales.dim(),
+        _ptr(fc2_experts_weights), _shape(fc2_experts_weights.shape),
+        _ptr(fc2_scales), _shape(fc2_scales.shape), fc2_scales.dim(),
+        _ptr(output), ctypes.byref(attrs), _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    _check(st, "qmoe_forward_noalloc")
     return output
 
 
