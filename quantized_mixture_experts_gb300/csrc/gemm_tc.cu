@@ -1,0 +1,571 @@
+// Grouped path of the QMoE layer: expert-grouped GEMMs on the 5th-generation
+// tensor cores (tcgen05) with TMEM accumulators.
+//
+// QMoE manifest passes QMoE.FC1ActivationStageGrouped / QMoE.OutputStageGrouped
+// (tiles of one expert's routed tokens against that expert's weights,
+// derive.groupMaxTiles) and GroupedMatMul-29 Summary (a runtime should fuse
+// DequantizeLinear + GroupedMatMul so the dequantized [G, K, N] weights are
+// never materialised).
+//
+// One work item = (token tile of one expert: up to 256 expert-sorted rows,
+// 128-row weight tile).  The MMA computes D[128 weight rows, N tokens] =
+// deq(W)[128, K] * X[N, K]^T with the weights as the A operand (M = 128) and
+// the tokens as the B operand (N = tile rows rounded up to 16), so a sparsely
+// routed expert costs a narrow MMA instead of a padded one.
+//
+// Per CTA (one per SM, persistent), warp-specialised:
+//   warp 0      TMA producer: the weight tile's packed bytes for a 64-wide K
+//               block (2-D box) and the tile's token rows (tile::gather4 of
+//               the fp16 activations, 128-byte swizzle) into a 3-stage ring;
+//   warp 1      TMEM allocator and MMA issuer (one lane): 4 x tcgen05.mma
+//               (K = 16) per stage into one of two 256-column accumulators;
+//   warps 2-9   dequantisers: packed codes -> (q - mid) * scale in fp16,
+//               written to shared memory in the 128-byte-swizzled K-major
+//               layout the MMA descriptor expects;
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator, FC1 ReLU / SwiGLU to
+//               fp16 activations, FC2 fp32 rows per routing slot.
+// Every wait is a bounded mbarrier wait; on expiry the CTA records
+// QMOE_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cstring>
+
+#include "ptx.cuh"
+#include "qmoe_internal.h"
+#include "tma_host.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kTcM = 128;            // weight rows per tile (MMA M)
+constexpr int kTcMaxN = 256;         // tokens per tile (MMA N upper bound)
+constexpr int kTcK = 64;             // K per stage: one 128-byte row of fp16
+constexpr int kTcStages = 3;
+constexpr int kDeqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kTcWarps = 2 + kDeqWarps + kEpiWarps;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr int kAccCols = 256;        // TMEM columns per accumulator buffer
+constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr uint32_t kBBytes = kTcMaxN * 128;   // token tile, fp16, swizzled
+constexpr uint32_t kABytes = kTcM * 128;      // dequantised weight tile, fp16, swizzled
+constexpr unsigned kFull = 0xffffffffu;
+
+struct TcArgs {
+    CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
+    CUtensorMap tm_b;           // fp16 token rows [rows, Kp], box {64, 1}, 128B swizzle
+    const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
+    const int32_t* tiles;       // header + (expert, first sorted row, rows, 0)
+    const int32_t* perm;        // sorted position -> slot
+    int64_t N, K;
+    int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
+    int topk, n_mtiles, gm;
+    __half* act_out;
+    int64_t act_pitch;
+    int act, has_limit;
+    float alpha, beta, limit;
+    float* slot_out;
+    int32_t* err;
+    uint64_t wait_ns;
+    uint32_t raw_bytes, off_b, off_a, stage_bytes;
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t(1) << 16;                 // leading byte offset (unused for this layout)
+    d |= uint64_t(1024 >> 4) << 32;         // stride byte offset between 8-row atoms
+    d |= uint64_t(1) << 46;                 // descriptor version
+    d |= uint64_t(2) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: fp16 A and B (K-major), fp32 accumulator, M x N.
+__device__ __forceinline__ uint32_t f16_idesc(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(ptx::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int32_t col,
+                                        int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                        uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+          "r"(ptx::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float swiglu(float g, float u, float alpha, float beta, int has_limit,
+                                        float limit) {
+    if (has_limit) {
+        g = fminf(g, limit);
+        u = fminf(fmaxf(u, -limit), limit);
+    }
+    return g * (1.f / (1.f + expf(-alpha * g))) * (u + beta);
+}
+
+struct Item {
+    int e, row0, rows, m, nt;   // expert, first sorted row, token rows, weight tile, MMA N
+};
+
+__device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntiles) {
+    const int64_t per_group = int64_t(ntiles) * a.gm;
+    const int mg = int(i / per_group);
+    const int64_t rem = i % per_group;
+    const int tau = int(rem / a.gm);
+    const int mm = int(rem % a.gm);
+    const int32_t* t = a.tiles + kTileHeader + 4 * tau;
+    Item it;
+    it.e = t[0];
+    it.row0 = t[1];
+    it.rows = t[2];
+    it.m = mg * a.gm + mm;
+    it.nt = (it.rows + 15) & ~15;
+    return it;
+}
+
+// Four packed 4-bit codes pairs -> natural-order fp16 pairs of (q - 8) * s:
+// out[0] = (q0,q1), out[1] = (q2,q3), out[2] = (q4,q5), out[3] = (q6,q7).
+__device__ __forceinline__ void deq4_natural(uint32_t w, __half2 s, uint32_t* out) {
+    const __half2 bias = ptx::u32_as_h2(0x64086408u);
+    uint32_t h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
+        h[q] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(v), bias), s));
+    }
+    out[0] = ptx::prmt(h[0], h[1], 0x5410u);
+    out[1] = ptx::prmt(h[2], h[3], 0x5410u);
+    out[2] = ptx::prmt(h[0], h[1], 0x7632u);
+    out[3] = ptx::prmt(h[2], h[3], 0x7632u);
+}
+
+// Four 8-bit codes -> natural-order fp16 pairs of (q - 128) * s.
+__device__ __forceinline__ void deq8_natural(uint32_t w, __half2 s, uint32_t* out) {
+    const __half2 bias = ptx::u32_as_h2(0x64806480u);
+    out[0] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4140u)), bias), s));
+    out[1] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4342u)), bias), s));
+}
+
+template <int BITS, bool FC1>
+__global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __grid_constant__ TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t load_full[kTcStages];
+    __shared__ __align__(8) uint64_t deq_full[kTcStages];
+    __shared__ __align__(8) uint64_t stage_empty[kTcStages];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag;
+    constexpr int PACK = BITS == 4 ? 2 : 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            ptx::mbar_init(&load_full[s], 1);
+            ptx::mbar_init(&deq_full[s], kDeqWarps);
+            ptx::mbar_init(&stage_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], kEpiWarps);
+        }
+        ptx::mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(ptx::smem_u32(&tmem_base_s)), "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_s;
+
+    const int ntiles = a.tiles[0];
+    const int64_t items = int64_t(ntiles) * a.n_mtiles;
+    const int nkb = int(a.K / kTcK);
+    const uint32_t sbase = ptx::smem_u32(smem);
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            ptx::prefetch_tmap(&a.tm_w);
+            ptx::prefetch_tmap(&a.tm_b);
+        }
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
+            const Item w = decode_item(a, i, ntiles);
+            const int ngather = w.nt / 4;
+            const int32_t wrow0 = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTcM);
+            // token rows of this lane's gather groups (groups lane and lane + 32)
+            int32_t rr[2][4];
+#pragma unroll
+            for (int gsel = 0; gsel < 2; ++gsel)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int p = min((lane + 32 * gsel) * 4 + q, w.rows - 1);
+                    rr[gsel][q] = FC1 ? a.perm[w.row0 + p] / a.topk : w.row0 + p;
+                }
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int st = int(it % kTcStages);
+                const uint32_t ph = (it / kTcStages) & 1u;
+                if (!ptx::mbar_wait(&stage_empty[st], ph ^ 1u, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sp = smem + size_t(st) * a.stage_bytes;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(&load_full[st],
+                                               a.raw_bytes + uint32_t(ngather) * 512u);
+                    ptx::tma_load_2d(sp, &a.tm_w, kb * (kTcK / PACK), wrow0, &load_full[st]);
+                }
+                __syncwarp();
+                const uint32_t bdst = ptx::smem_u32(sp + a.off_b);
+#pragma unroll
+                for (int gsel = 0; gsel < 2; ++gsel) {
+                    const int gq = lane + 32 * gsel;
+                    if (gq < ngather)
+                        gather4(bdst + uint32_t(gq) * 512u, &a.tm_b, kb * kTcK, rr[gsel][0],
+                                rr[gsel][1], rr[gsel][2], rr[gsel][3], &load_full[st]);
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+            for (uint32_t j = it > kTcStages ? it - kTcStages : 0; j < it; ++j) {
+                volatile int never = 0;
+                ptx::mbar_wait(&load_full[j % kTcStages], (j / kTcStages) & 1u, a.wait_ns, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------- MMA issuer -------------------------------
+        uint32_t it = 0, acc_it = 0;
+        bool ok = true;
+        bool issued = false;
+        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x, ++acc_it) {
+            const Item w = decode_item(a, i, ntiles);
+            const int buf = int(acc_it & 1u);
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, a.wait_ns, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t idesc = f16_idesc(kTcM, w.nt);
+            const uint32_t d_tmem = tmem_base + uint32_t(buf * kAccCols);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int st = int(it % kTcStages);
+                const uint32_t ph = (it / kTcStages) & 1u;
+                if (!ptx::mbar_wait(&deq_full[st], ph, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sa = sbase + uint32_t(st) * a.stage_bytes + a.off_a;
+                    const uint32_t sb = sbase + uint32_t(st) * a.stage_bytes + a.off_b;
+#pragma unroll
+                    for (int kk = 0; kk < kTcK / 16; ++kk)
+                        mma_f16(d_tmem, sw128_desc(sa + 32u * kk), sw128_desc(sb + 32u * kk), idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+                    mma_commit(&stage_empty[st]);
+                    issued = true;
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(&acc_full[buf]);
+            __syncwarp();
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        if (lane == 0 && issued) {
+            // all MMAs this thread issued complete before TMEM is released
+            mma_commit(&drain_bar);
+            volatile int never = 0;
+            ptx::mbar_wait(&drain_bar, 0, a.wait_ns, &never);
+        }
+        __syncwarp();
+    } else if (warp < 2 + kDeqWarps) {
+        // ------------------------------ dequantisers ------------------------------
+        const int dt = threadIdx.x - 64;           // 0..255
+        const int r = dt % kTcM;                   // weight row in the tile
+        const int kh = dt / kTcM;                  // K half (32 values) of the stage
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
+            const Item w = decode_item(a, i, ntiles);
+            const int64_t row = int64_t(w.m) * kTcM + r;   // weight row within the expert
+            const bool valid = row < a.N;
+            const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
+            __half2 sc = __float2half2_rn(valid && a.lbs < 0 ? __ldg(srow) : 0.f);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int st = int(it % kTcStages);
+                const uint32_t ph = (it / kTcStages) & 1u;
+                if (!ptx::mbar_wait(&load_full[st], ph, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sp = ptx::launder(sbase + uint32_t(st) * a.stage_bytes);
+                const uint32_t arow = sp + a.off_a + uint32_t(r) * 128u;
+                uint32_t outv[16];
+                if (BITS == 4) {
+                    const uint4 raw = ptx::lds128(sp + uint32_t(r) * 32u + uint32_t(kh) * 16u);
+                    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (a.lbs >= 0) {
+                            const int k0 = kb * kTcK + kh * 32 + q * 8;
+                            sc = __float2half2_rn(valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                        }
+                        deq4_natural(wv[q], sc, outv + 4 * q);
+                    }
+                } else {
+                    const uint4 raw0 = ptx::lds128(sp + uint32_t(r) * 64u + uint32_t(kh) * 32u);
+                    const uint4 raw1 = ptx::lds128(sp + uint32_t(r) * 64u + uint32_t(kh) * 32u + 16u);
+                    const uint32_t wv[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (a.lbs >= 0) {
+                            const int k0 = kb * kTcK + kh * 32 + q * 4;
+                            sc = __float2half2_rn(valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                        }
+                        deq8_natural(wv[q], sc, outv + 2 * q);
+                    }
+                }
+                // 32 fp16 = four 16-byte chunks (kh*4 .. kh*4+3) of the 128-byte row, swizzled
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = kh * 4 + c;
+                    const uint32_t addr = arow + uint32_t((chunk ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+                                 "r"(outv[4 * c]), "r"(outv[4 * c + 1]), "r"(outv[4 * c + 2]),
+                                 "r"(outv[4 * c + 3])
+                                 : "memory");
+                }
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&deq_full[st]);
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+        }
+    } else {
+        // -------------------------------- epilogue --------------------------------
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int r = quad * 32 + lane;            // weight row in the tile
+        uint32_t acc_it = 0;
+        for (int64_t i = blockIdx.x; i < items; i += gridDim.x, ++acc_it) {
+            const Item w = decode_item(a, i, ntiles);
+            const int buf = int(acc_it & 1u);
+            const uint32_t aph = (acc_it >> 1) & 1u;
+            if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
+                if (lane == 0) {
+                    record_error(a.err, QMOE_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int64_t row = int64_t(w.m) * kTcM + r;
+            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(buf * kAccCols);
+            for (int c0 = 0; c0 < w.nt; c0 += 32) {
+                float v[32];
+                tmem_ld32(tbase + uint32_t(c0), v);
+                if (FC1) {
+                    if (a.act == QMOE_ACT_SWIGLU) {
+                        // even lane: gate row, tokens c0..c0+15; odd lane: tokens c0+16..c0+31
+                        const bool even = (lane & 1) == 0;
+                        const int64_t j = row >> 1;
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float send = even ? v[16 + q] : v[q];
+                            const float recv = __shfl_xor_sync(kFull, send, 1);
+                            const float gate = even ? v[q] : recv;
+                            const float lin = even ? recv : v[16 + q];
+                            const int col = c0 + (even ? q : 16 + q);
+                            if (col < w.rows && row < a.N) {
+                                const float o = swiglu(gate, lin, a.alpha, a.beta, a.has_limit, a.limit);
+                                if (!(fabsf(o) <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
+                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + j] = __float2half_rn(o);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const int col = c0 + q;
+                            if (col < w.rows && row < a.N) {
+                                const float o = fmaxf(v[q], 0.f);
+                                if (!(o <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
+                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + row] = __float2half_rn(o);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int col = c0 + q;
+                        if (col < w.rows && row < a.N) {
+                            const int64_t slot = a.perm[w.row0 + col];
+                            a.slot_out[slot * a.N + row] = v[q];
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+template <int BITS, bool FC1>
+cudaError_t launch_tc(const TcArgs& args, int grid, size_t smem, cudaStream_t s) {
+    auto kern = grouped_gemm_kernel<BITS, FC1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTcThreads, smem, s>>>(args);
+    return cudaGetLastError();
+}
+
+int ilog2(int64_t v) {
+    int l = 0;
+    while ((int64_t(1) << l) < v) ++l;
+    return l;
+}
+
+int pick_group(int n_mtiles) {
+    for (int g = 8; g > 1; --g)
+        if (n_mtiles % g == 0) return g;
+    return 1;
+}
+
+}  // namespace
+
+int grouped_tile_tokens() { return kTcMaxN; }
+
+bool grouped_shape_ok(const Problem& p) {
+    if (p.H % kTcK != 0 || p.I % kTcK != 0) return false;
+    return true;
+}
+
+cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
+                              cudaStream_t s) {
+    TcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const uint8_t* wt = fc1 ? p.w1 : p.w2;
+    a.N = fc1 ? p.fusion * p.I : p.H;
+    a.K = fc1 ? p.H : p.I;
+    a.nb = int(fc1 ? p.nb1 : p.nb2);
+    a.lbs = p.bs ? ilog2(p.bs) : -1;
+    a.scales = fc1 ? p.s1 : p.s2;
+    const int pack = p.pack;
+    if (!encode_tmap_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, uint64_t(a.K / pack),
+                        uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kTcK / pack), kTcM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    const __half* bsrc = fc1 ? w.x16 : static_cast<const __half*>(w.act);
+    const int64_t brows = fc1 ? p.T : pl.slots;
+    const int64_t bpitch = fc1 ? pl.Hp : pl.Ip;
+    if (!encode_tmap_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsrc, uint64_t(bpitch),
+                        uint64_t(brows), uint64_t(bpitch) * 2, kTcK, 1,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    a.tiles = w.tiles;
+    a.perm = w.perm;
+    a.topk = int(p.k);
+    a.n_mtiles = int((a.N + kTcM - 1) / kTcM);
+    a.gm = pick_group(a.n_mtiles);
+    a.act_out = static_cast<__half*>(w.act);
+    a.act_pitch = pl.Ip;
+    a.act = p.act;
+    a.has_limit = p.has_limit;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.limit = p.limit;
+    a.slot_out = w.slot_out;
+    a.err = w.ctrl;
+    a.wait_ns = wait_limit_ns();
+    a.raw_bytes = uint32_t(kTcM * (kTcK / pack));
+    const uint32_t raw_pad = (a.raw_bytes + 1023u) & ~1023u;
+    a.off_b = raw_pad;
+    a.off_a = raw_pad + kBBytes;
+    a.stage_bytes = a.off_a + kABytes;
+    const size_t smem = 1024 + size_t(kTcStages) * a.stage_bytes;
+    const int64_t items_max = pl.max_tiles * a.n_mtiles;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
+    const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
+    note_launch(kid, s, true);
+    cudaError_t e;
+    if (p.bits == 4) e = fc1 ? launch_tc<4, true>(a, grid, smem, s) : launch_tc<4, false>(a, grid, smem, s);
+    else e = fc1 ? launch_tc<8, true>(a, grid, smem, s) : launch_tc<8, false>(a, grid, smem, s);
+    note_launch(kid, s, false);
+    return e;
+}
+
+}  // namespace qmoe

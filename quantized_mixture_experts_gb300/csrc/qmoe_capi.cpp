@@ -147,6 +147,7 @@ bool path_ok(const Problem& p, int path) {
     switch (path) {
         case QMOE_PATH_GENERIC: return true;
         case QMOE_PATH_DECODE: return decode_shape_ok(p);
+        case QMOE_PATH_GROUPED: return grouped_shape_ok(p);
         default: return false;
     }
 }
@@ -164,8 +165,8 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.route_chunks = (p.T + kRouteTokensPerChunk - 1) / kRouteTokensPerChunk;
     q.Hp = round_up(p.H, 64);
     q.Ip = round_up(std::max<int64_t>(p.I, 1), 64);
-    q.tile_tokens = 0;
-    q.max_tiles = 0;
+    q.tile_tokens = p.path == QMOE_PATH_GROUPED ? grouped_tile_tokens() : 0;
+    q.max_tiles = q.tile_tokens ? (q.slots + q.tile_tokens - 1) / q.tile_tokens + p.E : 0;
     q.fc2_splits = p.path == QMOE_PATH_DECODE ? decode_fc2_splits(p) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -270,6 +271,19 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             if ((e = launch_decode_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_decode_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_combine(p, pl, w, pl.fc2_splits, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            return QMOE_OK;
+        }
+        case QMOE_PATH_GROUPED: {
+            if (small_route_ok(p, pl)) {
+                if ((e = launch_route_group_small(p, pl, w, false, s)) != cudaSuccess)
+                    return QMOE_ERR_CUDA;
+            } else {
+                if ((e = launch_route(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            }
+            if ((e = launch_grouped_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_grouped_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_combine(p, pl, w, 1, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             return QMOE_OK;
         }
         default:

@@ -103,6 +103,11 @@ bool decode_shape_ok(const Problem& p);
 int decode_fc2_splits(const Problem& p);
 cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
                              cudaStream_t s);
+// Grouped path (many tokens): tcgen05 expert-grouped GEMMs.
+int grouped_tile_tokens();
+bool grouped_shape_ok(const Problem& p);
+cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
+                              cudaStream_t s);
 cudaError_t launch_grouped_matmul(const void* input, int64_t M, int64_t K, const void* weights,
                                   int64_t G, int64_t N, const void* idx, int64_t S, int idx64,
                                   const void* bias, void* out, int dtype, int32_t* err,
