@@ -15,8 +15,9 @@
 //
 // Per CTA (one per SM, persistent), warp-specialised:
 //   warp 0      TMA producer: the weight tile's packed bytes for a 64-wide K
-//               block (2-D box) and the tile's token rows (tile::gather4 of
-//               the fp16 activations, 128-byte swizzle) into a 3-stage ring;
+//               block and its block scales (2-D boxes) and the tile's token
+//               rows (16-row boxes of the expert-sorted fp16 activations,
+//               128-byte swizzle) into a 3-stage ring;
 //   warp 1      TMEM allocator and MMA issuer (one lane): 4 x tcgen05.mma
 //               (K = 16) per stage into one of two 256-column accumulators;
 //   warps 2-9   dequantisers: packed codes -> (q - mid) * scale in fp16,
@@ -52,7 +53,9 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct TcArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
-    CUtensorMap tm_b;           // fp16 token rows [rows, Kp], box {64, 1}, 128B swizzle
+    CUtensorMap tm_b;           // expert-sorted fp16 token rows [slots, Kp], box {64, 16},
+                                // 128-byte swizzle
+    CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 128}
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, 0)
     const int32_t* perm;        // sorted position -> slot
@@ -66,7 +69,8 @@ struct TcArgs {
     float* slot_out;
     int32_t* err;
     uint64_t wait_ns;
-    uint32_t raw_bytes, off_b, off_a, stage_bytes;
+    int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
+    uint32_t raw_bytes, off_s, off_b, off_a, stage_bytes;
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -128,17 +132,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int32_t col,
-                                        int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                        uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        ::"r"(dst), "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-          "r"(ptx::smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ float swiglu(float g, float u, float alpha, float beta, int has_limit,
                                         float limit) {
     if (has_limit) {
@@ -146,6 +139,10 @@ __device__ __forceinline__ float swiglu(float g, float u, float alpha, float bet
         u = fminf(fmaxf(u, -limit), limit);
     }
     return g * (1.f / (1.f + expf(-alpha * g))) * (u + beta);
+}
+
+__device__ __forceinline__ float pick4(float4 v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
 struct Item {
@@ -247,17 +244,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         bool ok = true;
         for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
-            const int ngather = w.nt / 4;
             const int32_t wrow0 = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTcM);
-            // token rows of this lane's gather groups (groups lane and lane + 32)
-            int32_t rr[2][4];
-#pragma unroll
-            for (int gsel = 0; gsel < 2; ++gsel)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int p = min((lane + 32 * gsel) * 4 + q, w.rows - 1);
-                    rr[gsel][q] = FC1 ? a.perm[w.row0 + p] / a.topk : w.row0 + p;
-                }
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = int(it % kTcStages);
                 const uint32_t ph = (it / kTcStages) & 1u;
@@ -267,19 +254,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 }
                 uint8_t* sp = smem + size_t(st) * a.stage_bytes;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&load_full[st],
-                                               a.raw_bytes + uint32_t(ngather) * 512u);
+                    ptx::mbar_arrive_expect_tx(&load_full[st], a.raw_bytes +
+                                               (a.scale_tma ? 2048u : 0u) +
+                                               uint32_t(w.nt) * 128u);
                     ptx::tma_load_2d(sp, &a.tm_w, kb * (kTcK / PACK), wrow0, &load_full[st]);
+                    if (a.scale_tma)
+                        ptx::tma_load_2d(sp + a.off_s, &a.tm_s, ((kb * kTcK) >> a.lbs) & ~3,
+                                         wrow0, &load_full[st]);
                 }
                 __syncwarp();
-                const uint32_t bdst = ptx::smem_u32(sp + a.off_b);
-#pragma unroll
-                for (int gsel = 0; gsel < 2; ++gsel) {
-                    const int gq = lane + 32 * gsel;
-                    if (gq < ngather)
-                        gather4(bdst + uint32_t(gq) * 512u, &a.tm_b, kb * kTcK, rr[gsel][0],
-                                rr[gsel][1], rr[gsel][2], rr[gsel][3], &load_full[st]);
-                }
+                // expert-sorted token rows are contiguous: one 16-row box per lane
+                if (lane < w.nt / 16)
+                    ptx::tma_load_2d(sp + a.off_b + lane * 2048, &a.tm_b, kb * kTcK,
+                                     w.row0 + lane * 16, &load_full[st]);
             }
         }
         if (!ok && lane == 0) {
@@ -354,6 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             const bool valid = row < a.N;
             const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
             __half2 sc = __float2half2_rn(valid && a.lbs < 0 ? __ldg(srow) : 0.f);
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = int(it % kTcStages);
                 const uint32_t ph = (it / kTcStages) & 1u;
@@ -363,6 +351,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 }
                 const uint32_t sp = ptx::launder(sbase + uint32_t(st) * a.stage_bytes);
                 const uint32_t arow = sp + a.off_a + uint32_t(r) * 128u;
+                const int sx0 = ((kb * kTcK) >> (a.lbs < 0 ? 0 : a.lbs)) & ~3;   // first staged block
+                if (a.scale_tma) s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
                 uint32_t outv[16];
                 if (BITS == 4) {
                     const uint4 raw = ptx::lds128(sp + uint32_t(r) * 32u + uint32_t(kh) * 16u);
@@ -371,7 +361,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     for (int q = 0; q < 4; ++q) {
                         if (a.lbs >= 0) {
                             const int k0 = kb * kTcK + kh * 32 + q * 8;
-                            sc = __float2half2_rn(valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                            const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
+                                                         : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                            sc = __float2half2_rn(sv);
                         }
                         deq4_natural(wv[q], sc, outv + 4 * q);
                     }
@@ -383,7 +375,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     for (int q = 0; q < 8; ++q) {
                         if (a.lbs >= 0) {
                             const int k0 = kb * kTcK + kh * 32 + q * 4;
-                            sc = __float2half2_rn(valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                            const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
+                                                         : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
+                            sc = __float2half2_rn(sv);
                         }
                         deq8_natural(wv[q], sc, outv + 2 * q);
                     }
@@ -459,13 +453,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         }
                     }
                 } else {
+                    const int my_col = c0 + lane;
+                    const int my_slot = my_col < w.rows ? a.perm[w.row0 + my_col] : 0;
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const int col = c0 + q;
-                        if (col < w.rows && row < a.N) {
-                            const int64_t slot = a.perm[w.row0 + col];
-                            a.slot_out[slot * a.N + row] = v[q];
-                        }
+                        const int64_t slot = __shfl_sync(kFull, my_slot, q);
+                        if (col < w.rows && row < a.N) a.slot_out[slot * a.N + row] = v[q];
                     }
                 }
             }
@@ -482,6 +476,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(kTmemCols)
                      : "memory");
+}
+
+// xs16[pos] = x16[perm[pos] / k]: the fp16 activations in expert-sorted slot
+// order, so every token tile is a contiguous block of rows.
+__global__ void sort_rows_kernel(const uint4* __restrict__ x16, int64_t row_vec,
+                                 const int32_t* __restrict__ perm, int k, int64_t slots,
+                                 uint4* __restrict__ xs16) {
+    const int64_t total = slots * row_vec;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t pos = i / row_vec, q = i % row_vec;
+        const int64_t t = perm[pos] / k;
+        xs16[i] = x16[t * row_vec + q];
+    }
 }
 
 template <int BITS, bool FC1>
@@ -509,6 +517,18 @@ int pick_group(int n_mtiles) {
 
 int grouped_tile_tokens() { return kTcMaxN; }
 
+cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
+    const int64_t row_vec = pl.Hp / 8;
+    const int64_t total = pl.slots * row_vec;
+    const int blocks = int(std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 16));
+    note_launch(QMOE_KERNEL_GROUP, s, true);
+    sort_rows_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(w.x16), row_vec, w.perm, int(p.k), pl.slots,
+        reinterpret_cast<uint4*>(w.xs16));
+    note_launch(QMOE_KERNEL_GROUP, s, false);
+    return cudaGetLastError();
+}
+
 bool grouped_shape_ok(const Problem& p) {
     if (p.H % kTcK != 0 || p.I % kTcK != 0) return false;
     return true;
@@ -529,12 +549,18 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
                         uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kTcK / pack), kTcM,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    const __half* bsrc = fc1 ? w.x16 : static_cast<const __half*>(w.act);
-    const int64_t brows = fc1 ? p.T : pl.slots;
+    const __half* bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
+    const int64_t brows = pl.slots;
     const int64_t bpitch = fc1 ? pl.Hp : pl.Ip;
     if (!encode_tmap_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsrc, uint64_t(bpitch),
-                        uint64_t(brows), uint64_t(bpitch) * 2, kTcK, 1,
+                        uint64_t(brows), uint64_t(bpitch) * 2, kTcK, 16,
                         CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    a.scale_tma = (p.bs != 0 && a.nb % 4 == 0) ? 1 : 0;
+    if (a.scale_tma &&
+        !encode_tmap_2d(&a.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, uint64_t(a.nb),
+                        uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kTcM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     a.tiles = w.tiles;
     a.perm = w.perm;
@@ -552,7 +578,8 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
     a.raw_bytes = uint32_t(kTcM * (kTcK / pack));
-    const uint32_t raw_pad = (a.raw_bytes + 1023u) & ~1023u;
+    a.off_s = a.raw_bytes;                       // 128 rows x 4 scales
+    const uint32_t raw_pad = (a.raw_bytes + 2048u + 1023u) & ~1023u;
     a.off_b = raw_pad;
     a.off_a = raw_pad + kBBytes;
     a.stage_bytes = a.off_a + kABytes;

@@ -189,6 +189,7 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.off_active = take(4 * E);
     const bool generic = p.path == QMOE_PATH_GENERIC;
     q.off_x16 = take(generic ? 0 : 2 * size_t(p.T) * size_t(q.Hp));
+    q.off_xs16 = take(p.path == QMOE_PATH_GROUPED ? 2 * slots * size_t(q.Hp) : 0);
     q.off_act = take(generic ? 4 * slots * size_t(p.I) : 2 * slots * size_t(q.Ip));
     q.off_slot_out = take(4 * size_t(q.fc2_splits) * slots * size_t(p.H));
     q.bytes = off;
@@ -211,6 +212,7 @@ Work carve(const Plan& pl, void* ws) {
     w.tiles = reinterpret_cast<int32_t*>(b + pl.off_tiles);
     w.active = reinterpret_cast<int32_t*>(b + pl.off_active);
     w.x16 = reinterpret_cast<__half*>(b + pl.off_x16);
+    w.xs16 = reinterpret_cast<__half*>(b + pl.off_xs16);
     w.act = b + pl.off_act;
     w.slot_out = reinterpret_cast<float*>(b + pl.off_slot_out);
     return w;
@@ -281,6 +283,7 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
                 if ((e = launch_route(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
                 if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
+            if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_combine(p, pl, w, 1, s)) != cudaSuccess) return QMOE_ERR_CUDA;

@@ -50,7 +50,7 @@ struct Plan {
     size_t bytes = 0;           // total workspace bytes
     // byte offsets into the workspace
     size_t off_ctrl, off_sel, off_pw, off_counts, off_offsets, off_hist, off_rank, off_perm,
-        off_inv, off_tiles, off_active, off_x16, off_act, off_slot_out;
+        off_inv, off_tiles, off_active, off_x16, off_xs16, off_act, off_slot_out;
 };
 
 // Device views of the workspace.
@@ -67,6 +67,7 @@ struct Work {
     int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, 0)
     int32_t* active;      // [E] experts with at least one slot, ascending
     __half* x16;          // [T*Hp] fp16 copy of the activations
+    __half* xs16;         // [T*k*Hp] fp16 activations in expert-sorted slot order (grouped path)
     void* act;            // [T*k*Ip] FC1 output (fp16; fp32 on the generic path)
     float* slot_out;      // [fc2_splits*T*k*H] per-slot FC2 output
 };
@@ -105,6 +106,7 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
                              cudaStream_t s);
 // Grouped path (many tokens): tcgen05 expert-grouped GEMMs.
 int grouped_tile_tokens();
+cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 bool grouped_shape_ok(const Problem& p);
 cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
                               cudaStream_t s);
