@@ -261,6 +261,16 @@ qmoe_status qmoe_get_device_error(void *workspace, void *cuda_stream, int32_t *c
  */
 void qmoe_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Test hook for the timeout path (no counterpart on the operator pages).
+ * When stage >= 0, the TMA producer of every pipelined kernel launched after
+ * this call skips the copies of its pipeline stage number `stage` (counted
+ * from 0 per CTA), so the consumers' wait on that stage never completes and
+ * must end through the wait limit with QMOE_DEVERR_TIMEOUT.  -1 (the default)
+ * turns it off.  Process-wide.
+ */
+void qmoe_debug_drop_stage(int64_t stage);
+
 /* Kernel identifiers for qmoe_profile_begin. */
 typedef enum {
     QMOE_KERNEL_ROUTE = 0,

@@ -99,6 +99,8 @@ def load():
     lib.qmoe_get_device_error.restype = ctypes.c_int
     lib.qmoe_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.qmoe_set_wait_limit_ns.restype = None
+    lib.qmoe_debug_drop_stage.argtypes = [ctypes.c_int64]
+    lib.qmoe_debug_drop_stage.restype = None
     lib.qmoe_profile_begin.argtypes = [I32]
     lib.qmoe_profile_begin.restype = ctypes.c_int
     lib.qmoe_profile_end.argtypes = [ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)]
@@ -306,6 +308,11 @@ def get_device_error(workspace, stream=None) -> int:
 
 def set_wait_limit_ns(ns: int):
     load().qmoe_set_wait_limit_ns(int(ns))
+
+
+def debug_drop_stage(stage: int):
+    """Test hook: producers skip the copies of pipeline stage `stage` (-1: off)."""
+    load().qmoe_debug_drop_stage(int(stage))
 
 
 def profile_begin(kernel_id: int):

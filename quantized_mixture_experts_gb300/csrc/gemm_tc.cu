@@ -50,6 +50,9 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint32_t kBBytes = kTcMaxN * 128;   // token tile, fp16, swizzled
 constexpr uint32_t kABytes = kTcM * 128;      // dequantised weight tile, fp16, swizzled
 constexpr unsigned kFull = 0xffffffffu;
+// Bound on the waits that drain a CTA's own copies / MMAs before it exits after
+// a timeout: independent of the (possibly tiny) configured wait limit.
+constexpr uint64_t kDrainWaitNs = 200000000ull;
 
 struct TcArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
@@ -70,6 +73,7 @@ struct TcArgs {
     int32_t* err;
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
+    int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t raw_bytes, off_s, off_b, off_a, stage_bytes;
 };
 
@@ -252,6 +256,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     ok = false;
                     break;
                 }
+                if (int64_t(it) == a.drop_it) continue;   // test hook: this stage never fills
                 uint8_t* sp = smem + size_t(st) * a.stage_bytes;
                 if (lane == 0) {
                     ptx::mbar_arrive_expect_tx(&load_full[st], a.raw_bytes +
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             abort_flag = 1;
             for (uint32_t j = it > kTcStages ? it - kTcStages : 0; j < it; ++j) {
                 volatile int never = 0;
-                ptx::mbar_wait(&load_full[j % kTcStages], (j / kTcStages) & 1u, a.wait_ns, &never);
+                ptx::mbar_wait(&load_full[j % kTcStages], (j / kTcStages) & 1u, kDrainWaitNs, &never);
             }
         }
     } else if (warp == 1) {
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             // all MMAs this thread issued complete before TMEM is released
             mma_commit(&drain_bar);
             volatile int never = 0;
-            ptx::mbar_wait(&drain_bar, 0, a.wait_ns, &never);
+            ptx::mbar_wait(&drain_bar, 0, kDrainWaitNs, &never);
         }
         __syncwarp();
     } else if (warp < 2 + kDeqWarps) {
@@ -577,6 +582,7 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.slot_out = w.slot_out;
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
+    a.drop_it = drop_stage();
     a.raw_bytes = uint32_t(kTcM * (kTcK / pack));
     a.off_s = a.raw_bytes;                       // 128 rows x 4 scales
     const uint32_t raw_pad = (a.raw_bytes + 2048u + 1023u) & ~1023u;

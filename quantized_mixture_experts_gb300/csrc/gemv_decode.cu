@@ -42,6 +42,9 @@ constexpr int kBoxTile = kBoxBytes * kDecRows; // 16 KB per weight box
 constexpr int kDecMaxTokens = 16;
 constexpr int kTargetUnitsPerSm = 10;
 constexpr unsigned kFull = 0xffffffffu;
+// Bound on the waits that drain a CTA's own copies / MMAs before it exits after
+// a timeout: independent of the (possibly tiny) configured wait limit.
+constexpr uint64_t kDrainWaitNs = 200000000ull;
 
 // Where the dequantization scale is applied.
 constexpr int kScaleCol = 0;    // column-wise: once per output, after the K loop
@@ -70,6 +73,7 @@ struct DecodeArgs {
     int64_t slots;
     int32_t* err;
     uint64_t wait_ns;
+    int64_t drop_it;            // test hook: stage whose copies the producer skips
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) {
@@ -181,6 +185,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                     ok = false;
                     break;
                 }
+                if (int64_t(it) == a.drop_it) continue;   // test hook: this stage never fills
                 const int64_t krem = a.K - int64_t(kc) * KC;
                 const int kvalid = int(krem < KC ? krem : KC);
                 uint8_t* sbase = smem + size_t(st) * a.stage_bytes;
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             // drain copies still in flight (bounded) before the CTA exits
             for (uint32_t j = it > a.nstages ? it - a.nstages : 0; j < it; ++j) {
                 volatile int never = 0;
-                ptx::mbar_wait(&full_bar[j % a.nstages], (j / a.nstages) & 1u, a.wait_ns, &never);
+                ptx::mbar_wait(&full_bar[j % a.nstages], (j / a.nstages) & 1u, kDrainWaitNs, &never);
             }
         }
         return;
@@ -572,6 +577,7 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     a.slots = pl.slots;
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
+    a.drop_it = drop_stage();
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
     a.nstages = uint32_t(std::min<size_t>(kDecStages, (smem_cap - 1024 - kDecRedBytes) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;

@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
+        if ((it & 7) == 0) {
             if (*abort) return false;
             if (globaltimer() - t0 > limit_ns) return false;
         }

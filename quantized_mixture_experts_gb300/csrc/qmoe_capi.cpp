@@ -17,6 +17,7 @@ namespace qmoe {
 namespace {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int64_t> g_drop_stage{-1};
 
 struct ProfPair {
     cudaEvent_t a = nullptr, b = nullptr;
@@ -29,6 +30,7 @@ bool g_prof_open = false;
 }  // namespace
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+int64_t drop_stage() { return g_drop_stage.load(std::memory_order_relaxed); }
 
 void note_launch(int kernel_id, cudaStream_t stream, bool begin, int nkernels) {
     if (!begin) g_launches.fetch_add(uint64_t(nkernels), std::memory_order_relaxed);
@@ -500,6 +502,8 @@ qmoe_status qmoe_get_device_error(void* workspace, void* cuda_stream, int32_t* c
 }
 
 void qmoe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+void qmoe_debug_drop_stage(int64_t stage) { g_drop_stage.store(stage < 0 ? -1 : stage); }
 
 qmoe_status qmoe_profile_begin(int32_t kernel_id) {
     if (kernel_id < QMOE_KERNEL_ROUTE || kernel_id > QMOE_KERNEL_COMBINE)

@@ -85,6 +85,8 @@ void note_launch(int kernel_id, cudaStream_t stream, bool begin, int nkernels = 
 
 // Process-wide bound on a single in-kernel spin-wait, in nanoseconds.
 uint64_t wait_limit_ns();
+// Pipeline stage the producers skip (test hook), -1 when off.
+int64_t drop_stage();
 
 // ---- launchers (return cudaGetLastError()) ----
 cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,

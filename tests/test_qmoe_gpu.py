@@ -210,3 +210,34 @@ def test_full_size_parity(dev, name):
         y, sel, p = y[tokens], sel[tokens], p[tokens]
     check_routing(sel, p, sel_ref, p_ref, name)
     check_outputs(y, y_ref, name)
+
+
+@pytest.mark.parametrize("name,path", [("decode", 1), ("prefill_like_rank3", 2)])
+def test_wait_timeout_reports_error_and_recovers(dev, name, path):
+    """One pipeline stage is never filled (test hook), so a consumer waits on a
+    barrier nothing completes: with a 50 ms wait limit the kernels must record
+    QMOE_DEVERR_TIMEOUT, drain, free their resources and return, and the next
+    call with the normal limit must be correct."""
+    import quantized_mixture_experts_gb300 as q
+    from quantized_mixture_experts_gb300 import binding as b
+    wl = WORKLOADS[name] if name in WORKLOADS else [w for w in SMALL if w.name == name][0]
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(path=path, **wl.attrs())
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape, attrs))
+    q.set_wait_limit_ns(50_000_000)
+    b.debug_drop_stage(1)
+    try:
+        q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], t["fc1_scales"],
+                       t["fc2_experts_weights"], t["fc2_scales"], attrs=attrs, workspace=ws)
+        code = q.get_device_error(ws)
+    finally:
+        b.debug_drop_stage(-1)
+        q.set_wait_limit_ns(2_000_000_000)
+    assert code == q.DEVERR_TIMEOUT
+    y, sel, p = run_cuda(inp, wl.attrs(), path, dev, t=t, workspace=ws)
+    tokens = np.arange(min(wl.tokens, 64), dtype=np.int64)
+    y_ref, sel_ref, p_ref = _reference(wl, inp, tokens)
+    check_routing(sel[tokens], p[tokens], sel_ref, p_ref, name)
+    check_outputs(y[tokens], y_ref, name + " after timeout")
+    assert q.get_device_error(ws) == q.DEVERR_NONE
