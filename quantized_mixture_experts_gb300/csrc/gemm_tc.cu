@@ -37,34 +37,38 @@
 namespace qmoe {
 namespace {
 
-constexpr int kTcM = 128;            // weight rows per tile (MMA M)
+constexpr int kTcM = 128;            // weight rows per MMA (M)
+constexpr int kPair = 2;             // weight tiles per work item (share one token tile)
+constexpr int kItemRows = kPair * kTcM;
 constexpr int kTcMaxN = 256;         // tokens per tile (MMA N upper bound)
 constexpr int kTcK = 64;             // K per stage: one 128-byte row of fp16
-constexpr int kTcStages = 3;
-constexpr int kDeqWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kLoadStages = 3;       // TMA ring: packed weights, scales, token rows
+constexpr int kAStages = 2;          // ring of dequantised weight tiles
+constexpr int kDeqWarps = 8;         // one thread per weight row of the item
+constexpr int kEpiWarps = 8;         // two per TMEM lane quadrant (one per weight tile)
 constexpr int kTcWarps = 2 + kDeqWarps + kEpiWarps;
 constexpr int kTcThreads = 32 * kTcWarps;
-constexpr int kAccCols = 256;        // TMEM columns per accumulator buffer
-constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr int kAccCols = 256;        // TMEM columns per accumulator (one per weight tile)
+constexpr uint32_t kTmemCols = kPair * kAccCols;
 constexpr uint32_t kBBytes = kTcMaxN * 128;   // token tile, fp16, swizzled
-constexpr uint32_t kABytes = kTcM * 128;      // dequantised weight tile, fp16, swizzled
+constexpr uint32_t kABytes = kTcM * 128;      // one dequantised weight tile, fp16, swizzled
+constexpr uint32_t kAStageBytes = kPair * kABytes;
 constexpr unsigned kFull = 0xffffffffu;
 // Bound on the waits that drain a CTA's own copies / MMAs before it exits after
 // a timeout: independent of the (possibly tiny) configured wait limit.
 constexpr uint64_t kDrainWaitNs = 200000000ull;
 
 struct TcArgs {
-    CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
+    CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 256}
     CUtensorMap tm_b;           // expert-sorted fp16 token rows [slots, Kp], box {64, 16},
                                 // 128-byte swizzle
-    CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 128}
+    CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 256}
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, 0)
     const int32_t* perm;        // sorted position -> slot
     int64_t N, K;
     int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
-    int topk, n_mtiles, gm;
+    int topk, n_pairs, gm;
     __half* act_out;
     int64_t act_pitch;
     int act, has_limit;
@@ -74,7 +78,7 @@ struct TcArgs {
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
-    uint32_t raw_bytes, off_s, off_b, off_a, stage_bytes;
+    uint32_t off_s, off_b, load_bytes;
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -155,16 +159,16 @@ struct Item {
 
 __device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntiles) {
     const int64_t per_group = int64_t(ntiles) * a.gm;
-    const int mg = int(i / per_group);
+    const int pg = int(i / per_group);
     const int64_t rem = i % per_group;
     const int tau = int(rem / a.gm);
-    const int mm = int(rem % a.gm);
+    const int pm = int(rem % a.gm);
     const int32_t* t = a.tiles + kTileHeader + 4 * tau;
     Item it;
     it.e = t[0];
     it.row0 = t[1];
     it.rows = t[2];
-    it.m = mg * a.gm + mm;
+    it.m = (pg * a.gm + pm) * kPair;   // first weight tile of the pair
     it.nt = (it.rows + 15) & ~15;
     return it;
 }
@@ -197,27 +201,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t load_full[kTcStages];
-    __shared__ __align__(8) uint64_t deq_full[kTcStages];
-    __shared__ __align__(8) uint64_t stage_empty[kTcStages];
-    __shared__ __align__(8) uint64_t acc_full[2];
-    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t load_full[kLoadStages];   // TMA bytes landed
+    __shared__ __align__(8) uint64_t load_empty[kLoadStages];  // MMAs reading the stage done
+    __shared__ __align__(8) uint64_t a_full[kAStages];         // dequantised weights written
+    __shared__ __align__(8) uint64_t a_empty[kAStages];        // MMAs reading them done
+    __shared__ __align__(8) uint64_t acc_full;
+    __shared__ __align__(8) uint64_t acc_empty;
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
     constexpr int PACK = BITS == 4 ? 2 : 1;
+    constexpr uint32_t kRawRow = kTcK / PACK;                   // packed bytes per row per stage
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kLoadStages; ++s) {
             ptx::mbar_init(&load_full[s], 1);
-            ptx::mbar_init(&deq_full[s], kDeqWarps);
-            ptx::mbar_init(&stage_empty[s], 1);
+            ptx::mbar_init(&load_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], kEpiWarps);
+        for (int s = 0; s < kAStages; ++s) {
+            ptx::mbar_init(&a_full[s], kDeqWarps);
+            ptx::mbar_init(&a_empty[s], 1);
         }
+        ptx::mbar_init(&acc_full, 1);
+        ptx::mbar_init(&acc_empty, kEpiWarps);
         ptx::mbar_init(&drain_bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
@@ -234,15 +241,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     const uint32_t tmem_base = tmem_base_s;
 
     const int ntiles = a.tiles[0];
-    const int64_t items = int64_t(ntiles) * a.n_mtiles;
+    const int64_t items = int64_t(ntiles) * a.n_pairs;
     const int nkb = int(a.K / kTcK);
     const uint32_t sbase = ptx::smem_u32(smem);
+    const uint32_t abase = sbase + kLoadStages * a.load_bytes;   // dequantised-weight ring
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             ptx::prefetch_tmap(&a.tm_w);
             ptx::prefetch_tmap(&a.tm_b);
+            if (a.scale_tma) ptx::prefetch_tmap(&a.tm_s);
         }
         uint32_t it = 0;
         bool ok = true;
@@ -250,76 +259,80 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             const Item w = decode_item(a, i, ntiles);
             const int32_t wrow0 = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTcM);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int st = int(it % kTcStages);
-                const uint32_t ph = (it / kTcStages) & 1u;
-                if (!ptx::mbar_wait(&stage_empty[st], ph ^ 1u, a.wait_ns, &abort_flag)) {
+                const int sl = int(it % kLoadStages);
+                const uint32_t ph = (it / kLoadStages) & 1u;
+                if (!ptx::mbar_wait(&load_empty[sl], ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 if (int64_t(it) == a.drop_it) continue;   // test hook: this stage never fills
-                uint8_t* sp = smem + size_t(st) * a.stage_bytes;
+                uint8_t* sp = smem + size_t(sl) * a.load_bytes;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&load_full[st], a.raw_bytes +
-                                               (a.scale_tma ? 2048u : 0u) +
+                    ptx::mbar_arrive_expect_tx(&load_full[sl], kItemRows * kRawRow +
+                                               (a.scale_tma ? kItemRows * 16u : 0u) +
                                                uint32_t(w.nt) * 128u);
-                    ptx::tma_load_2d(sp, &a.tm_w, kb * (kTcK / PACK), wrow0, &load_full[st]);
+                    ptx::tma_load_2d(sp, &a.tm_w, kb * int(kRawRow), wrow0, &load_full[sl]);
                     if (a.scale_tma)
                         ptx::tma_load_2d(sp + a.off_s, &a.tm_s, ((kb * kTcK) >> a.lbs) & ~3,
-                                         wrow0, &load_full[st]);
+                                         wrow0, &load_full[sl]);
                 }
                 __syncwarp();
                 // expert-sorted token rows are contiguous: one 16-row box per lane
                 if (lane < w.nt / 16)
                     ptx::tma_load_2d(sp + a.off_b + lane * 2048, &a.tm_b, kb * kTcK,
-                                     w.row0 + lane * 16, &load_full[st]);
+                                     w.row0 + lane * 16, &load_full[sl]);
             }
         }
         if (!ok && lane == 0) {
             record_error(a.err, QMOE_DEVERR_TIMEOUT);
             abort_flag = 1;
-            for (uint32_t j = it > kTcStages ? it - kTcStages : 0; j < it; ++j) {
+            for (uint32_t j = it > kLoadStages ? it - kLoadStages : 0; j < it; ++j) {
                 volatile int never = 0;
-                ptx::mbar_wait(&load_full[j % kTcStages], (j / kTcStages) & 1u, kDrainWaitNs, &never);
+                ptx::mbar_wait(&load_full[j % kLoadStages], (j / kLoadStages) & 1u, kDrainWaitNs,
+                               &never);
             }
         }
     } else if (warp == 1) {
         // ------------------------------- MMA issuer -------------------------------
-        uint32_t it = 0, acc_it = 0;
+        uint32_t it = 0, item_it = 0;
         bool ok = true;
         bool issued = false;
-        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x, ++acc_it) {
+        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x, ++item_it) {
             const Item w = decode_item(a, i, ntiles);
-            const int buf = int(acc_it & 1u);
-            const uint32_t aph = (acc_it >> 1) & 1u;
-            if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, a.wait_ns, &abort_flag)) {
+            if (!ptx::mbar_wait(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t idesc = f16_idesc(kTcM, w.nt);
-            const uint32_t d_tmem = tmem_base + uint32_t(buf * kAccCols);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int st = int(it % kTcStages);
-                const uint32_t ph = (it / kTcStages) & 1u;
-                if (!ptx::mbar_wait(&deq_full[st], ph, a.wait_ns, &abort_flag)) {
+                const int sl = int(it % kLoadStages);
+                const int sa = int(it % kAStages);
+                if (!ptx::mbar_wait(&a_full[sa], (it / kAStages) & 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sa = sbase + uint32_t(st) * a.stage_bytes + a.off_a;
-                    const uint32_t sb = sbase + uint32_t(st) * a.stage_bytes + a.off_b;
+                    const uint32_t sb = sbase + uint32_t(sl) * a.load_bytes + a.off_b;
+                    const uint32_t sa0 = abase + uint32_t(sa) * kAStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kTcK / 16; ++kk)
-                        mma_f16(d_tmem, sw128_desc(sa + 32u * kk), sw128_desc(sb + 32u * kk), idesc,
-                                (kb | kk) != 0 ? 1u : 0u);
-                    mma_commit(&stage_empty[st]);
+                    for (int kk = 0; kk < kTcK / 16; ++kk) {
+                        const uint64_t bd = sw128_desc(sb + 32u * kk);
+#pragma unroll
+                        for (int t = 0; t < kPair; ++t)
+                            mma_f16(tmem_base + uint32_t(t * kAccCols),
+                                    sw128_desc(sa0 + uint32_t(t) * kABytes + 32u * kk), bd, idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&load_empty[sl]);
+                    mma_commit(&a_empty[sa]);
                     issued = true;
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&acc_full[buf]);
+            if (lane == 0) mma_commit(&acc_full);
             __syncwarp();
         }
         if (!ok && lane == 0) {
@@ -327,7 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             abort_flag = 1;
         }
         if (lane == 0 && issued) {
-            // all MMAs this thread issued complete before TMEM is released
+            // every MMA this thread issued completes before TMEM is released
             mma_commit(&drain_bar);
             volatile int never = 0;
             ptx::mbar_wait(&drain_bar, 0, kDrainWaitNs, &never);
@@ -335,9 +348,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         __syncwarp();
     } else if (warp < 2 + kDeqWarps) {
         // ------------------------------ dequantisers ------------------------------
-        const int dt = threadIdx.x - 64;           // 0..255
-        const int r = dt % kTcM;                   // weight row in the tile
-        const int kh = dt / kTcM;                  // K half (32 values) of the stage
+        const int r = threadIdx.x - 64;            // row of the 256-row item (two weight tiles)
+        const int tile = r >> 7, rr = r & (kTcM - 1);
         uint32_t it = 0;
         bool ok = true;
         for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
@@ -346,26 +358,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             const bool valid = row < a.N;
             const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
             __half2 sc = __float2half2_rn(valid && a.lbs < 0 ? __ldg(srow) : 0.f);
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int st = int(it % kTcStages);
-                const uint32_t ph = (it / kTcStages) & 1u;
-                if (!ptx::mbar_wait(&load_full[st], ph, a.wait_ns, &abort_flag)) {
+                const int sl = int(it % kLoadStages);
+                const int sa = int(it % kAStages);
+                if (!ptx::mbar_wait(&load_full[sl], (it / kLoadStages) & 1u, a.wait_ns, &abort_flag) ||
+                    !ptx::mbar_wait(&a_empty[sa], ((it / kAStages) & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t sp = ptx::launder(sbase + uint32_t(st) * a.stage_bytes);
-                const uint32_t arow = sp + a.off_a + uint32_t(r) * 128u;
+                const uint32_t sp = ptx::launder(sbase + uint32_t(sl) * a.load_bytes);
+                const uint32_t arow = abase + uint32_t(sa) * kAStageBytes + uint32_t(tile) * kABytes +
+                                      uint32_t(rr) * 128u;
                 const int sx0 = ((kb * kTcK) >> (a.lbs < 0 ? 0 : a.lbs)) & ~3;   // first staged block
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (a.scale_tma) s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
-                uint32_t outv[16];
+                uint32_t outv[32];
                 if (BITS == 4) {
-                    const uint4 raw = ptx::lds128(sp + uint32_t(r) * 32u + uint32_t(kh) * 16u);
-                    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+                    // 32 packed bytes; the two 16-byte halves are read in an order that
+                    // keeps each quarter warp on distinct banks
+                    const bool swp = ((r >> 2) & 1) != 0;
+                    const uint4 p0 = ptx::lds128(sp + uint32_t(r) * 32u + (swp ? 16u : 0u));
+                    const uint4 p1 = ptx::lds128(sp + uint32_t(r) * 32u + (swp ? 0u : 16u));
+                    const uint4 lo = swp ? p1 : p0, hi = swp ? p0 : p1;
+                    const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 8; ++q) {
                         if (a.lbs >= 0) {
-                            const int k0 = kb * kTcK + kh * 32 + q * 8;
+                            const int k0 = kb * kTcK + q * 8;
                             const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
                                                          : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
                             sc = __float2half2_rn(sv);
@@ -373,13 +392,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         deq4_natural(wv[q], sc, outv + 4 * q);
                     }
                 } else {
-                    const uint4 raw0 = ptx::lds128(sp + uint32_t(r) * 64u + uint32_t(kh) * 32u);
-                    const uint4 raw1 = ptx::lds128(sp + uint32_t(r) * 64u + uint32_t(kh) * 32u + 16u);
-                    const uint32_t wv[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+                    uint32_t wv[16];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 pj = ptx::lds128(sp + uint32_t(r) * 64u + uint32_t(j) * 16u);
+                        wv[4 * j] = pj.x; wv[4 * j + 1] = pj.y; wv[4 * j + 2] = pj.z; wv[4 * j + 3] = pj.w;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
                         if (a.lbs >= 0) {
-                            const int k0 = kb * kTcK + kh * 32 + q * 4;
+                            const int k0 = kb * kTcK + q * 4;
                             const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
                                                          : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
                             sc = __float2half2_rn(sv);
@@ -387,11 +409,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         deq8_natural(wv[q], sc, outv + 2 * q);
                     }
                 }
-                // 32 fp16 = four 16-byte chunks (kh*4 .. kh*4+3) of the 128-byte row, swizzled
+                // 64 fp16 = eight 16-byte chunks of the 128-byte row, swizzled
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = kh * 4 + c;
-                    const uint32_t addr = arow + uint32_t((chunk ^ (r & 7)) << 4);
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t addr = arow + uint32_t((c ^ (rr & 7)) << 4);
                     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr),
                                  "r"(outv[4 * c]), "r"(outv[4 * c + 1]), "r"(outv[4 * c + 2]),
                                  "r"(outv[4 * c + 3])
@@ -399,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 }
                 ptx::fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&deq_full[st]);
+                if (lane == 0) ptx::mbar_arrive(&a_full[sa]);
             }
         }
         if (!ok && lane == 0) {
@@ -408,14 +429,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         }
     } else {
         // -------------------------------- epilogue --------------------------------
+        const int ew = warp - 2 - kDeqWarps;       // 0..7
+        const int tile = ew / 4;                   // weight tile of the item
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int r = quad * 32 + lane;            // weight row in the tile
-        uint32_t acc_it = 0;
-        for (int64_t i = blockIdx.x; i < items; i += gridDim.x, ++acc_it) {
+        const int r = quad * 32 + lane;            // row in the weight tile
+        uint32_t item_it = 0;
+        for (int64_t i = blockIdx.x; i < items; i += gridDim.x, ++item_it) {
             const Item w = decode_item(a, i, ntiles);
-            const int buf = int(acc_it & 1u);
-            const uint32_t aph = (acc_it >> 1) & 1u;
-            if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
+            if (!ptx::mbar_wait(&acc_full, item_it & 1u, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
@@ -423,8 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 break;
             }
             tc_fence_after();
-            const int64_t row = int64_t(w.m) * kTcM + r;
-            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(buf * kAccCols);
+            const int64_t row = int64_t(w.m + tile) * kTcM + r;
+            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(tile * kAccCols);
             for (int c0 = 0; c0 < w.nt; c0 += 32) {
                 float v[32];
                 tmem_ld32(tbase + uint32_t(c0), v);
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) ptx::mbar_arrive(&acc_empty);
         }
     }
 
@@ -551,7 +572,7 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.scales = fc1 ? p.s1 : p.s2;
     const int pack = p.pack;
     if (!encode_tmap_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, uint64_t(a.K / pack),
-                        uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kTcK / pack), kTcM,
+                        uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kTcK / pack), kItemRows,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const __half* bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
@@ -564,14 +585,15 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.scale_tma = (p.bs != 0 && a.nb % 4 == 0) ? 1 : 0;
     if (a.scale_tma &&
         !encode_tmap_2d(&a.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, uint64_t(a.nb),
-                        uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kTcM,
+                        uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kItemRows,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     a.tiles = w.tiles;
     a.perm = w.perm;
     a.topk = int(p.k);
-    a.n_mtiles = int((a.N + kTcM - 1) / kTcM);
-    a.gm = pick_group(a.n_mtiles);
+    const int n_mtiles = int((a.N + kTcM - 1) / kTcM);
+    a.n_pairs = (n_mtiles + kPair - 1) / kPair;
+    a.gm = pick_group(a.n_pairs);
     a.act_out = static_cast<__half*>(w.act);
     a.act_pitch = pl.Ip;
     a.act = p.act;
@@ -583,14 +605,12 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
     a.drop_it = drop_stage();
-    a.raw_bytes = uint32_t(kTcM * (kTcK / pack));
-    a.off_s = a.raw_bytes;                       // 128 rows x 4 scales
-    const uint32_t raw_pad = (a.raw_bytes + 2048u + 1023u) & ~1023u;
-    a.off_b = raw_pad;
-    a.off_a = raw_pad + kBBytes;
-    a.stage_bytes = a.off_a + kABytes;
-    const size_t smem = 1024 + size_t(kTcStages) * a.stage_bytes;
-    const int64_t items_max = pl.max_tiles * a.n_mtiles;
+    const uint32_t raw_bytes = uint32_t(kItemRows * (kTcK / pack));
+    a.off_s = raw_bytes;                          // 256 rows x 4 scales
+    a.off_b = (raw_bytes + kItemRows * 16u + 1023u) & ~1023u;
+    a.load_bytes = a.off_b + kBBytes;
+    const size_t smem = 1024 + size_t(kLoadStages) * a.load_bytes + size_t(kAStages) * kAStageBytes;
+    const int64_t items_max = pl.max_tiles * a.n_pairs;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
     const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
     note_launch(kid, s, true);
