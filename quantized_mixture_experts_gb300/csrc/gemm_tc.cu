@@ -42,7 +42,7 @@ constexpr int kPair = 2;             // weight tiles per work item (share one to
 constexpr int kItemRows = kPair * kTcM;
 constexpr int kTcMaxN = 256;         // tokens per tile (MMA N upper bound)
 constexpr int kTcK = 64;             // K per stage: one 128-byte row of fp16
-constexpr int kLoadStages = 3;       // TMA ring: packed weights, scales, token rows
+constexpr int kLoadStages = 4;       // TMA ring depth upper bound (the launch picks what fits)
 constexpr int kAStages = 2;          // ring of dequantised weight tiles
 constexpr int kDeqWarps = 8;         // one thread per weight row of the item
 constexpr int kEpiWarps = 8;         // two per TMEM lane quadrant (one per weight tile)
@@ -69,6 +69,8 @@ struct TcArgs {
     int64_t N, K;
     int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
     int topk, n_pairs, gm;
+    int split_n;                // 2: items take half a token tile (N <= 128), double-buffered
+                                // accumulators; 1: whole tile (N <= 256), single buffer
     __half* act_out;
     int64_t act_pitch;
     int act, has_limit;
@@ -78,7 +80,7 @@ struct TcArgs {
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
-    uint32_t off_s, off_b, load_bytes;
+    uint32_t off_s, off_b, load_bytes, nload;
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -158,45 +160,57 @@ struct Item {
 };
 
 __device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntiles) {
-    const int64_t per_group = int64_t(ntiles) * a.gm;
+    const int64_t per_group = int64_t(ntiles) * a.split_n * a.gm;
     const int pg = int(i / per_group);
     const int64_t rem = i % per_group;
-    const int tau = int(rem / a.gm);
+    const int th = int(rem / a.gm);            // token tile and half
     const int pm = int(rem % a.gm);
+    const int tau = th / a.split_n, half = th % a.split_n;
     const int32_t* t = a.tiles + kTileHeader + 4 * tau;
+    const int span = kTcMaxN / a.split_n;      // token rows per item
     Item it;
     it.e = t[0];
-    it.row0 = t[1];
-    it.rows = t[2];
-    it.m = (pg * a.gm + pm) * kPair;   // first weight tile of the pair
+    it.row0 = t[1] + half * span;
+    it.rows = min(t[2] - half * span, span);   // <= 0: nothing to do for this half
+    it.m = (pg * a.gm + pm) * kPair;           // first weight tile of the pair
     it.nt = (it.rows + 15) & ~15;
     return it;
 }
 
-// Four packed 4-bit codes pairs -> natural-order fp16 pairs of (q - 8) * s:
-// out[0] = (q0,q1), out[1] = (q2,q3), out[2] = (q4,q5), out[3] = (q6,q7).
-__device__ __forceinline__ void deq4_natural(uint32_t w, __half2 s, uint32_t* out) {
+// Eight packed 4-bit codes (low nibble first) -> four fp16 pairs
+// ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) of (q - 8) [* s].  The activations of the
+// 4-bit path are stored with the same order inside every group of eight, so
+// A and B agree on the K order without a shuffle.  1024 + q is built exactly
+// by OR-ing the nibble into the mantissa of fp16 1024.
+template <bool SCALE>
+__device__ __forceinline__ void deq4(uint32_t w, __half2 s, uint32_t* out) {
     const __half2 bias = ptx::u32_as_h2(0x64086408u);
-    uint32_t h[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
-        h[q] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(v), bias), s));
+        const __half2 d = __hsub2(ptx::u32_as_h2(v), bias);
+        out[q] = ptx::h2_as_u32(SCALE ? __hmul2(d, s) : d);
     }
-    out[0] = ptx::prmt(h[0], h[1], 0x5410u);
-    out[1] = ptx::prmt(h[2], h[3], 0x5410u);
-    out[2] = ptx::prmt(h[0], h[1], 0x7632u);
-    out[3] = ptx::prmt(h[2], h[3], 0x7632u);
 }
 
-// Four 8-bit codes -> natural-order fp16 pairs of (q - 128) * s.
-__device__ __forceinline__ void deq8_natural(uint32_t w, __half2 s, uint32_t* out) {
+// Four 8-bit codes -> natural-order fp16 pairs ((q0,q1),(q2,q3)) of (q - 128) [* s].
+template <bool SCALE>
+__device__ __forceinline__ void deq8(uint32_t w, __half2 s, uint32_t* out) {
     const __half2 bias = ptx::u32_as_h2(0x64806480u);
-    out[0] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4140u)), bias), s));
-    out[1] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4342u)), bias), s));
+    const __half2 d0 = __hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4140u)), bias);
+    const __half2 d1 = __hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4342u)), bias);
+    out[0] = ptx::h2_as_u32(SCALE ? __hmul2(d0, s) : d0);
+    out[1] = ptx::h2_as_u32(SCALE ? __hmul2(d1, s) : d1);
 }
 
-template <int BITS, bool FC1>
+// Position of column j in a row stored with groups of eight in the order
+// 0,4,1,5,2,6,3,7 (the 4-bit operand order).
+__device__ __forceinline__ int64_t perm8(int64_t j) {
+    const int q = int(j & 7);
+    return (j & ~int64_t(7)) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
+}
+
+template <int BITS, bool FC1, bool SCOL>
 __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -205,8 +219,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     __shared__ __align__(8) uint64_t load_empty[kLoadStages];  // MMAs reading the stage done
     __shared__ __align__(8) uint64_t a_full[kAStages];         // dequantised weights written
     __shared__ __align__(8) uint64_t a_empty[kAStages];        // MMAs reading them done
-    __shared__ __align__(8) uint64_t acc_full;
-    __shared__ __align__(8) uint64_t acc_empty;
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kLoadStages; ++s) {
+        for (uint32_t s = 0; s < a.nload; ++s) {
             ptx::mbar_init(&load_full[s], 1);
             ptx::mbar_init(&load_empty[s], 1);
         }
@@ -223,8 +237,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             ptx::mbar_init(&a_full[s], kDeqWarps);
             ptx::mbar_init(&a_empty[s], 1);
         }
-        ptx::mbar_init(&acc_full, 1);
-        ptx::mbar_init(&acc_empty, kEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], kEpiWarps);
+        }
         ptx::mbar_init(&drain_bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
@@ -241,10 +257,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     const uint32_t tmem_base = tmem_base_s;
 
     const int ntiles = a.tiles[0];
-    const int64_t items = int64_t(ntiles) * a.n_pairs;
+    const int64_t items = int64_t(ntiles) * a.split_n * a.n_pairs;
+    const int acc_cols = kAccCols / a.split_n;     // TMEM columns per weight tile and buffer
     const int nkb = int(a.K / kTcK);
     const uint32_t sbase = ptx::smem_u32(smem);
-    const uint32_t abase = sbase + kLoadStages * a.load_bytes;   // dequantised-weight ring
+    const uint32_t abase = sbase + a.nload * a.load_bytes;   // dequantised-weight ring
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
@@ -257,10 +274,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         bool ok = true;
         for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
+            if (w.rows <= 0) continue;
             const int32_t wrow0 = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTcM);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int sl = int(it % kLoadStages);
-                const uint32_t ph = (it / kLoadStages) & 1u;
+                const int sl = int(it % a.nload);
+                const uint32_t ph = (it / a.nload) & 1u;
                 if (!ptx::mbar_wait(&load_empty[sl], ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
@@ -286,9 +304,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         if (!ok && lane == 0) {
             record_error(a.err, QMOE_DEVERR_TIMEOUT);
             abort_flag = 1;
-            for (uint32_t j = it > kLoadStages ? it - kLoadStages : 0; j < it; ++j) {
+            for (uint32_t j = it > a.nload ? it - a.nload : 0; j < it; ++j) {
                 volatile int never = 0;
-                ptx::mbar_wait(&load_full[j % kLoadStages], (j / kLoadStages) & 1u, kDrainWaitNs,
+                ptx::mbar_wait(&load_full[j % a.nload], (j / a.nload) & 1u, kDrainWaitNs,
                                &never);
             }
         }
@@ -297,16 +315,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         uint32_t it = 0, item_it = 0;
         bool ok = true;
         bool issued = false;
-        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x, ++item_it) {
+        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
-            if (!ptx::mbar_wait(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
+            if (w.rows <= 0) continue;
+            const int buf = a.split_n == 2 ? int(item_it & 1u) : 0;
+            const uint32_t aph = (a.split_n == 2 ? (item_it >> 1) : item_it) & 1u;
+            ++item_it;
+            if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, a.wait_ns, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t dbase = tmem_base + uint32_t(buf * kAccCols);
             const uint32_t idesc = f16_idesc(kTcM, w.nt);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int sl = int(it % kLoadStages);
+                const int sl = int(it % a.nload);
                 const int sa = int(it % kAStages);
                 if (!ptx::mbar_wait(&a_full[sa], (it / kAStages) & 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         const uint64_t bd = sw128_desc(sb + 32u * kk);
 #pragma unroll
                         for (int t = 0; t < kPair; ++t)
-                            mma_f16(tmem_base + uint32_t(t * kAccCols),
+                            mma_f16(dbase + uint32_t(t * acc_cols),
                                     sw128_desc(sa0 + uint32_t(t) * kABytes + 32u * kk), bd, idesc,
                                     (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&acc_full);
+            if (lane == 0) mma_commit(&acc_full[buf]);
             __syncwarp();
         }
         if (!ok && lane == 0) {
@@ -354,14 +377,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         bool ok = true;
         for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
+            if (w.rows <= 0) continue;
             const int64_t row = int64_t(w.m) * kTcM + r;   // weight row within the expert
             const bool valid = row < a.N;
             const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
-            __half2 sc = __float2half2_rn(valid && a.lbs < 0 ? __ldg(srow) : 0.f);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const int sl = int(it % kLoadStages);
+                const int sl = int(it % a.nload);
                 const int sa = int(it % kAStages);
-                if (!ptx::mbar_wait(&load_full[sl], (it / kLoadStages) & 1u, a.wait_ns, &abort_flag) ||
+                if (!ptx::mbar_wait(&load_full[sl], (it / a.nload) & 1u, a.wait_ns, &abort_flag) ||
                     !ptx::mbar_wait(&a_empty[sa], ((it / kAStages) & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
@@ -369,9 +392,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 const uint32_t sp = ptx::launder(sbase + uint32_t(sl) * a.load_bytes);
                 const uint32_t arow = abase + uint32_t(sa) * kAStageBytes + uint32_t(tile) * kABytes +
                                       uint32_t(rr) * 128u;
-                const int sx0 = ((kb * kTcK) >> (a.lbs < 0 ? 0 : a.lbs)) & ~3;   // first staged block
-                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (a.scale_tma) s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
+                // Block scales of this K block: the staged group of four covers it.
+                // Column-wise scales are applied to the accumulator instead.
+                __half2 sc[4];
+                if (!SCOL) {
+                    // the four staged blocks start at ((kb * 64) >> lbs) & ~3; rows whose scale
+                    // row is not 16-byte aligned (nb % 4 != 0) read them from global memory
+                    float4 s4;
+                    if (a.scale_tma) {
+                        s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
+                    } else {
+                        const int g0 = ((kb * kTcK) >> a.lbs) & ~3;
+                        s4.x = valid && g0 < a.nb ? __ldg(srow + g0) : 0.f;
+                        s4.y = valid && g0 + 1 < a.nb ? __ldg(srow + g0 + 1) : 0.f;
+                        s4.z = valid && g0 + 2 < a.nb ? __ldg(srow + g0 + 2) : 0.f;
+                        s4.w = valid && g0 + 3 < a.nb ? __ldg(srow + g0 + 3) : 0.f;
+                    }
+                    if (a.lbs >= 6) {            // one block per K block
+                        const int sx0 = ((kb * kTcK) >> a.lbs) & ~3;
+                        sc[0] = sc[1] = sc[2] = sc[3] =
+                            __float2half2_rn(pick4(s4, ((kb * kTcK) >> a.lbs) - sx0));
+                    } else if (a.lbs == 5) {     // two blocks of 32
+                        const int o = (2 * kb) & 3;
+                        sc[0] = sc[1] = __float2half2_rn(pick4(s4, o));
+                        sc[2] = sc[3] = __float2half2_rn(pick4(s4, o + 1));
+                    } else {                     // four blocks of 16
+                        sc[0] = __float2half2_rn(s4.x);
+                        sc[1] = __float2half2_rn(s4.y);
+                        sc[2] = __float2half2_rn(s4.z);
+                        sc[3] = __float2half2_rn(s4.w);
+                    }
+                }
                 uint32_t outv[32];
                 if (BITS == 4) {
                     // 32 packed bytes; the two 16-byte halves are read in an order that
@@ -383,13 +434,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        if (a.lbs >= 0) {
-                            const int k0 = kb * kTcK + q * 8;
-                            const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
-                                                         : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
-                            sc = __float2half2_rn(sv);
-                        }
-                        deq4_natural(wv[q], sc, outv + 4 * q);
+                        if (SCOL) deq4<false>(wv[q], sc[0], outv + 4 * q);
+                        else deq4<true>(wv[q], sc[q >> 1], outv + 4 * q);   // word q: K 8q..8q+7
                     }
                 } else {
                     uint32_t wv[16];
@@ -400,13 +446,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     }
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        if (a.lbs >= 0) {
-                            const int k0 = kb * kTcK + q * 4;
-                            const float sv = a.scale_tma ? pick4(s4, (k0 >> a.lbs) - sx0)
-                                                         : (valid ? __ldg(srow + (k0 >> a.lbs)) : 0.f);
-                            sc = __float2half2_rn(sv);
-                        }
-                        deq8_natural(wv[q], sc, outv + 2 * q);
+                        if (SCOL) deq8<false>(wv[q], sc[0], outv + 2 * q);
+                        else deq8<true>(wv[q], sc[q >> 2], outv + 2 * q);   // word q: K 4q..4q+3
                     }
                 }
                 // 64 fp16 = eight 16-byte chunks of the 128-byte row, swizzled
@@ -434,9 +475,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row in the weight tile
         uint32_t item_it = 0;
-        for (int64_t i = blockIdx.x; i < items; i += gridDim.x, ++item_it) {
+        for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
-            if (!ptx::mbar_wait(&acc_full, item_it & 1u, a.wait_ns, &abort_flag)) {
+            if (w.rows <= 0) continue;
+            const int buf = a.split_n == 2 ? int(item_it & 1u) : 0;
+            const uint32_t aph = (a.split_n == 2 ? (item_it >> 1) : item_it) & 1u;
+            ++item_it;
+            if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
@@ -445,15 +490,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             }
             tc_fence_after();
             const int64_t row = int64_t(w.m + tile) * kTcM + r;
-            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(tile * kAccCols);
+            // column-wise scale of this output row (applied here, not in the operand)
+            const float srow = SCOL && row < a.N ? __ldg(a.scales + int64_t(w.e) * a.N + row) : 1.f;
+            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) +
+                                   uint32_t(buf * kAccCols + tile * acc_cols);
             for (int c0 = 0; c0 < w.nt; c0 += 32) {
                 float v[32];
                 tmem_ld32(tbase + uint32_t(c0), v);
+                if (SCOL) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) v[q] *= srow;
+                }
                 if (FC1) {
                     if (a.act == QMOE_ACT_SWIGLU) {
                         // even lane: gate row, tokens c0..c0+15; odd lane: tokens c0+16..c0+31
                         const bool even = (lane & 1) == 0;
-                        const int64_t j = row >> 1;
+                        const int64_t j = BITS == 4 ? perm8(row >> 1) : (row >> 1);
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
                             const float send = even ? v[16 + q] : v[q];
@@ -474,7 +526,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                             if (col < w.rows && row < a.N) {
                                 const float o = fmaxf(v[q], 0.f);
                                 if (!(o <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + row] = __float2half_rn(o);
+                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + (BITS == 4 ? perm8(row) : row)] =
+                                    __float2half_rn(o);
                             }
                         }
                     }
@@ -491,7 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty);
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
         }
     }
 
@@ -518,9 +571,9 @@ __global__ void sort_rows_kernel(const uint4* __restrict__ x16, int64_t row_vec,
     }
 }
 
-template <int BITS, bool FC1>
+template <int BITS, bool FC1, bool SCOL>
 cudaError_t launch_tc(const TcArgs& args, int grid, size_t smem, cudaStream_t s) {
-    auto kern = grouped_gemm_kernel<BITS, FC1>;
+    auto kern = grouped_gemm_kernel<BITS, FC1, SCOL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, kTcThreads, smem, s>>>(args);
@@ -594,6 +647,9 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     const int n_mtiles = int((a.N + kTcM - 1) / kTcM);
     a.n_pairs = (n_mtiles + kPair - 1) / kPair;
     a.gm = pick_group(a.n_pairs);
+    // FC2 with a short reduction: half-tile items so the fp32 epilogue overlaps the
+    // next item's MMAs (FC1 keeps whole tiles: halves would double the dequantisation)
+    a.split_n = 1;
     a.act_out = static_cast<__half*>(w.act);
     a.act_pitch = pl.Ip;
     a.act = p.act;
@@ -609,14 +665,22 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.off_s = raw_bytes;                          // 256 rows x 4 scales
     a.off_b = (raw_bytes + kItemRows * 16u + 1023u) & ~1023u;
     a.load_bytes = a.off_b + kBBytes;
-    const size_t smem = 1024 + size_t(kLoadStages) * a.load_bytes + size_t(kAStages) * kAStageBytes;
-    const int64_t items_max = pl.max_tiles * a.n_pairs;
+    const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
+    a.nload = uint32_t(std::min<size_t>(kLoadStages, (smem_cap - 1024 - size_t(kAStages) * kAStageBytes) /
+                                                         a.load_bytes));
+    if (a.nload < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + size_t(a.nload) * a.load_bytes + size_t(kAStages) * kAStageBytes;
+    const int64_t items_max = pl.max_tiles * a.split_n * a.n_pairs;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
     const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
     note_launch(kid, s, true);
     cudaError_t e;
-    if (p.bits == 4) e = fc1 ? launch_tc<4, true>(a, grid, smem, s) : launch_tc<4, false>(a, grid, smem, s);
-    else e = fc1 ? launch_tc<8, true>(a, grid, smem, s) : launch_tc<8, false>(a, grid, smem, s);
+    const bool scol = p.bs == 0;
+#define QMOE_TC_LAUNCH(B, C) \
+    (fc1 ? launch_tc<B, true, C>(a, grid, smem, s) : launch_tc<B, false, C>(a, grid, smem, s))
+    if (p.bits == 4) e = scol ? QMOE_TC_LAUNCH(4, true) : QMOE_TC_LAUNCH(4, false);
+    else e = scol ? QMOE_TC_LAUNCH(8, true) : QMOE_TC_LAUNCH(8, false);
+#undef QMOE_TC_LAUNCH
     note_launch(kid, s, false);
     return e;
 }

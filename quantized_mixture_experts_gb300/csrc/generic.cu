@@ -114,30 +114,43 @@ __global__ void combine_kernel(const float* __restrict__ slot_out, const float* 
         const int64_t H4 = H / 4;
         if (idx >= T * H4) return;
         const int64_t t = idx / H4, d4 = idx % H4;
+        const float4* base = reinterpret_cast<const float4*>(slot_out + t * k * H) + d4;
+        const int64_t sstride = slots * H / 4;   // between K splits
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < k; ++i) {
-            const float w = pw[t * k + i];
-            const float4* src = reinterpret_cast<const float4*>(slot_out + (t * k + i) * H) + d4;
-            const int64_t sstride = slots * H / 4;
-            float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (splits <= 8) {
-                // issue every split's load first; the sum stays in split order
-                float4 v[8];
+        if (splits == 1 && k <= 16) {
+            // issue every slot's load first; the sum keeps ascending slot order
+            float4 v[16];
 #pragma unroll
-                for (int sp = 0; sp < 8; ++sp)
-                    if (sp < splits) v[sp] = __ldg(src + sp * sstride);
+            for (int i = 0; i < 16; ++i)
+                if (i < k) v[i] = __ldg(base + int64_t(i) * (H / 4));
 #pragma unroll
-                for (int sp = 0; sp < 8; ++sp)
-                    if (sp < splits) {
-                        part.x += v[sp].x; part.y += v[sp].y; part.z += v[sp].z; part.w += v[sp].w;
-                    }
-            } else {
-                for (int sp = 0; sp < splits; ++sp) {
-                    const float4 v = __ldg(src + sp * sstride);
-                    part.x += v.x; part.y += v.y; part.z += v.z; part.w += v.w;
+            for (int i = 0; i < 16; ++i)
+                if (i < k) {
+                    const float w = pw[t * k + i];
+                    acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
                 }
+        } else {
+            for (int i = 0; i < k; ++i) {
+                float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (splits <= 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int sp = 0; sp < 8; ++sp)
+                        if (sp < splits) v[sp] = __ldg(base + int64_t(i) * (H / 4) + sp * sstride);
+#pragma unroll
+                    for (int sp = 0; sp < 8; ++sp)
+                        if (sp < splits) {
+                            part.x += v[sp].x; part.y += v[sp].y; part.z += v[sp].z; part.w += v[sp].w;
+                        }
+                } else {
+                    for (int sp = 0; sp < splits; ++sp) {
+                        const float4 v = __ldg(base + int64_t(i) * (H / 4) + sp * sstride);
+                        part.x += v.x; part.y += v.y; part.z += v.z; part.w += v.w;
+                    }
+                }
+                const float w = pw[t * k + i];
+                acc.x += w * part.x; acc.y += w * part.y; acc.z += w * part.z; acc.w += w * part.w;
             }
-            acc.x += w * part.x; acc.y += w * part.y; acc.z += w * part.z; acc.w += w * part.w;
         }
         reinterpret_cast<float4*>(y + t * H)[d4] = acc;
     } else {

@@ -278,11 +278,13 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             return QMOE_OK;
         }
         case QMOE_PATH_GROUPED: {
+            // 4-bit: activations in the interleaved operand order of the nibble conversion
+            const bool il = p.bits == 4;
             if (small_route_ok(p, pl)) {
-                if ((e = launch_route_group_small(p, pl, w, false, s)) != cudaSuccess)
+                if ((e = launch_route_group_small(p, pl, w, il, s)) != cudaSuccess)
                     return QMOE_ERR_CUDA;
             } else {
-                if ((e = launch_route(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_route(p, pl, w, il, s)) != cudaSuccess) return QMOE_ERR_CUDA;
                 if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
             if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;

@@ -11,6 +11,7 @@
 #include <algorithm>
 
 #include "qmoe_internal.h"
+#include "tma_host.h"
 
 namespace qmoe {
 namespace {
@@ -398,9 +399,13 @@ cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
-    // split the fp16 conversion of each chunk over several CTAs (~256 groups of 8 each)
+    // split the fp16 conversion of each chunk over enough CTAs to cover the GPU
+    // (at least 32 groups of eight columns per CTA)
     int ysplit = 1;
-    if (w.x16) ysplit = int(std::min<int64_t>(32, std::max<int64_t>(1, (pl.Hp / 8) / 256)));
+    if (w.x16) {
+        const int64_t want = (int64_t(4) * device_sm_count() + pl.route_chunks - 1) / pl.route_chunks;
+        ysplit = int(std::max<int64_t>(1, std::min<int64_t>(want, pl.Hp / 256)));
+    }
     note_launch(QMOE_KERNEL_ROUTE, s, true);
     route_kernel<<<dim3(unsigned(pl.route_chunks), unsigned(ysplit)), kRouteThreads, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
