@@ -148,7 +148,7 @@ __device__ __forceinline__ float swiglu(float g, float u, float alpha, float bet
         g = fminf(g, limit);
         u = fminf(fmaxf(u, -limit), limit);
     }
-    return g * (1.f / (1.f + expf(-alpha * g))) * (u + beta);
+    return __fdividef(g, 1.f + __expf(-alpha * g)) * (u + beta);
 }
 
 __device__ __forceinline__ float pick4(float4 v, int i) {
@@ -180,17 +180,23 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntil
 // Eight packed 4-bit codes (low nibble first) -> four fp16 pairs
 // ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) of (q - 8) [* s].  The activations of the
 // 4-bit path are stored with the same order inside every group of eight, so
-// A and B agree on the K order without a shuffle.  1024 + q is built exactly
-// by OR-ing the nibble into the mantissa of fp16 1024.
+// A and B agree on the K order without a shuffle.  A low nibble OR-ed into the
+// mantissa of fp16 1024 gives 1024 + q; a high nibble left in place gives
+// 1024 + 16 q, whose pairs are scaled by s / 16 (1/16 when unscaled), which is
+// exact.
 template <bool SCALE>
-__device__ __forceinline__ void deq4(uint32_t w, __half2 s, uint32_t* out) {
-    const __half2 bias = ptx::u32_as_h2(0x64086408u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
-        const __half2 d = __hsub2(ptx::u32_as_h2(v), bias);
-        out[q] = ptx::h2_as_u32(SCALE ? __hmul2(d, s) : d);
-    }
+__device__ __forceinline__ void deq4(uint32_t w, __half2 s, __half2 s16, uint32_t* out) {
+    const __half2 lo_bias = ptx::u32_as_h2(0x64086408u);   // 1032
+    const __half2 hi_bias = ptx::u32_as_h2(0x64806480u);   // 1152 = 1024 + 16 * 8
+    const uint32_t w8 = w >> 8;
+    const __half2 d0 = __hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x000F000Fu, 0x64006400u)), lo_bias);
+    const __half2 d1 = __hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x00F000F0u, 0x64006400u)), hi_bias);
+    const __half2 d2 = __hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x000F000Fu, 0x64006400u)), lo_bias);
+    const __half2 d3 = __hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x00F000F0u, 0x64006400u)), hi_bias);
+    out[0] = ptx::h2_as_u32(SCALE ? __hmul2(d0, s) : d0);
+    out[1] = ptx::h2_as_u32(__hmul2(d1, s16));
+    out[2] = ptx::h2_as_u32(SCALE ? __hmul2(d2, s) : d2);
+    out[3] = ptx::h2_as_u32(__hmul2(d3, s16));
 }
 
 // Four 8-bit codes -> natural-order fp16 pairs ((q0,q1),(q2,q3)) of (q - 128) [* s].
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                                       uint32_t(rr) * 128u;
                 // Block scales of this K block: the staged group of four covers it.
                 // Column-wise scales are applied to the accumulator instead.
-                __half2 sc[4];
+                __half2 sc[4] = {};
                 if (!SCOL) {
                     // the four staged blocks start at ((kb * 64) >> lbs) & ~3; rows whose scale
                     // row is not 16-byte aligned (nb % 4 != 0) read them from global memory
@@ -432,10 +438,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     const uint4 p1 = ptx::lds128(sp + uint32_t(r) * 32u + (swp ? 0u : 16u));
                     const uint4 lo = swp ? p1 : p0, hi = swp ? p0 : p1;
                     const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    const __half2 inv16 = __float2half2_rn(0.0625f);
+                    __half2 sc16[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) sc16[b] = SCOL ? inv16 : __hmul2(sc[b], inv16);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        if (SCOL) deq4<false>(wv[q], sc[0], outv + 4 * q);
-                        else deq4<true>(wv[q], sc[q >> 1], outv + 4 * q);   // word q: K 8q..8q+7
+                        if (SCOL) deq4<false>(wv[q], sc[0], inv16, outv + 4 * q);
+                        else deq4<true>(wv[q], sc[q >> 1], sc16[q >> 1], outv + 4 * q);   // word q: K 8q..8q+7
                     }
                 } else {
                     uint32_t wv[16];

@@ -67,7 +67,7 @@ struct DecodeArgs {
     uint32_t stage_bytes, off_s, off_b, pitch_b, nstages;
     __half* act_out;
     int64_t act_pitch;
-    int act, interleave8, has_limit;
+    int act, act_mode, has_limit;   // act_mode: 2 = 4-bit operand layout, 0 = natural
     float alpha, beta, limit;
     float* slot_out;
     int64_t slots;
@@ -80,26 +80,28 @@ __device__ __forceinline__ void record_error(int32_t* err, int code) {
     atomicCAS(err, 0, code);
 }
 
-// Eight 4-bit codes of `w` (low nibble first) -> four fp16 pairs
-// ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) holding q - 8 exactly: 1024 + q is built
-// by OR-ing the nibble into the mantissa of fp16 1024, then 1032 is subtracted.
+// Eight 4-bit codes of `w` (low nibble first, element e in bits 4e..4e+3) ->
+// four fp16 pairs, each exact:
+//   h[0] = (q0, q4) - 8          h[2] = (q2, q6) - 8         (low nibbles of each byte)
+//   h[1] = 16 * ((q1, q5) - 8)   h[3] = 16 * ((q3, q7) - 8)  (high nibbles, kept in place)
+// A nibble OR-ed into the mantissa of fp16 1024 gives 1024 + q; a high nibble
+// left at bits 4..7 gives 1024 + 16 q.  The activations feeding the high
+// pairs are stored divided by 16, so each product is unchanged.
 __device__ __forceinline__ void dequant4(uint32_t w, uint32_t* h) {
-    const __half2 bias = ptx::u32_as_h2(0x64086408u);   // (1032, 1032)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
-        h[q] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(v), bias));
-    }
+    const __half2 lo_bias = ptx::u32_as_h2(0x64086408u);   // (1032, 1032)
+    const __half2 hi_bias = ptx::u32_as_h2(0x64806480u);   // (1152, 1152)
+    const uint32_t w8 = w >> 8;
+    h[0] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x000F000Fu, 0x64006400u)), lo_bias));
+    h[1] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x00F000F0u, 0x64006400u)), hi_bias));
+    h[2] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x000F000Fu, 0x64006400u)), lo_bias));
+    h[3] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x00F000F0u, 0x64006400u)), hi_bias));
 }
 
-// As dequant4, multiplied by the fp16 scale (for block sizes below 32).
+// As dequant4, every pair multiplied by the fp16 scale (block size 16).
 __device__ __forceinline__ void dequant4_scaled(uint32_t w, __half2 s, uint32_t* h) {
-    const __half2 bias = ptx::u32_as_h2(0x64086408u);
+    dequant4(w, h);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t v = ptx::and_or(w >> (4 * q), 0x000F000Fu, 0x64006400u);
-        h[q] = ptx::h2_as_u32(__hmul2(__hsub2(ptx::u32_as_h2(v), bias), s));
-    }
+    for (int q = 0; q < 4; ++q) h[q] = ptx::h2_as_u32(__hmul2(ptx::u32_as_h2(h[q]), s));
 }
 
 // Four 8-bit codes -> two fp16 pairs ((q0,q1),(q2,q3)) holding q - 128 exactly.
@@ -117,7 +119,7 @@ __device__ __forceinline__ float swiglu(float g, float u, float alpha, float bet
         g = fminf(g, limit);
         u = fminf(fmaxf(u, -limit), limit);
     }
-    return g * (1.f / (1.f + expf(-alpha * g))) * (u + beta);
+    return __fdividef(g, 1.f + __expf(-alpha * g)) * (u + beta);
 }
 
 // Position of activation column j in a row stored with 8-groups in the
@@ -125,6 +127,13 @@ __device__ __forceinline__ float swiglu(float g, float u, float alpha, float bet
 __device__ __forceinline__ int64_t perm8(int64_t j) {
     const int q = int(j & 7);
     return (j & ~int64_t(7)) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
+}
+
+// Stores activation v of column j in the layout the 4-bit FC2 reads (mode 2:
+// pair order, odd columns divided by 16) or in natural order (mode 0).
+__device__ __forceinline__ void store_act(__half* row, int64_t j, float v, int mode) {
+    if (mode == 2) row[perm8(j)] = __float2half_rn((j & 1) ? v * 0.0625f : v);
+    else row[j] = __float2half_rn(v);
 }
 
 template <int BITS, int SMODE, bool FC1>
@@ -323,17 +332,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                             if (nt == 1 && !two) break;
                             ptx::ld128_pred(bq[nt], sB + uint32_t(g + 8 * nt) * a.pitch_b + boff,
                                             nt == 0 ? ld0 : ld1);
+                            // low pairs (K 0,4 | 2,6) with b.x|b.z; high pairs (K 1,5 | 3,7),
+                            // 16x larger, with b.y|b.w stored divided by 16
                             if (SMODE == kScalePost) {
                                 float tmp[4];
-                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
-                                ptx::mma_16816(tmp, hg[2], hg8[2], hg[3], hg8[3], bq[nt].z, bq[nt].w);
+                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[2], hg8[2], bq[nt].x, bq[nt].z);
+                                ptx::mma_16816(tmp, hg[1], hg8[1], hg[3], hg8[3], bq[nt].y, bq[nt].w);
                                 acc[nt][0] = fmaf(sgv[i], tmp[0], acc[nt][0]);
                                 acc[nt][1] = fmaf(sgv[i], tmp[1], acc[nt][1]);
                                 acc[nt][2] = fmaf(sg8v[i], tmp[2], acc[nt][2]);
                                 acc[nt][3] = fmaf(sg8v[i], tmp[3], acc[nt][3]);
                             } else {
-                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
-                                ptx::mma_16816(accB[nt], hg[2], hg8[2], hg[3], hg8[3], bq[nt].z, bq[nt].w);
+                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[2], hg8[2], bq[nt].x, bq[nt].z);
+                                ptx::mma_16816(accB[nt], hg[1], hg8[1], hg[3], hg8[3], bq[nt].y, bq[nt].w);
                             }
                         }
                     } else {
@@ -429,15 +440,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                                 const float v = swiglu(acc[nt][q], pv[q], a.alpha, a.beta,
                                                        a.has_limit, a.limit);
                                 if (!(fabsf(v) <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                                const int64_t j = rg >> 1;
-                                dst[a.interleave8 ? perm8(j) : j] = __float2half_rn(v);
+                                store_act(dst, rg >> 1, v, a.act_mode);
                             }
                             if (rg8 < a.N) {
                                 const float v = swiglu(acc[nt][2 + q], pv[2 + q], a.alpha, a.beta,
                                                        a.has_limit, a.limit);
                                 if (!(fabsf(v) <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                                const int64_t j = rg8 >> 1;
-                                dst[a.interleave8 ? perm8(j) : j] = __float2half_rn(v);
+                                store_act(dst, rg8 >> 1, v, a.act_mode);
                             }
                         }
                     }
@@ -453,12 +462,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                         if (rg < a.N) {
                             const float v = fmaxf(acc[nt][q], 0.f);
                             if (!(v <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                            dst[a.interleave8 ? perm8(rg) : rg] = __float2half_rn(v);
+                            store_act(dst, rg, v, a.act_mode);
                         }
                         if (rg8 < a.N) {
                             const float v = fmaxf(acc[nt][2 + q], 0.f);
                             if (!(v <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                            dst[a.interleave8 ? perm8(rg8) : rg8] = __float2half_rn(v);
+                            store_act(dst, rg8, v, a.act_mode);
                         }
                     }
                 }
@@ -568,7 +577,7 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     a.act_out = static_cast<__half*>(w.act);
     a.act_pitch = pl.Ip;
     a.act = p.act;
-    a.interleave8 = p.bits == 4 ? 1 : 0;
+    a.act_mode = p.bits == 4 ? 2 : 0;
     a.has_limit = p.has_limit;
     a.alpha = p.alpha;
     a.beta = p.beta;

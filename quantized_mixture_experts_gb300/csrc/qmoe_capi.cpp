@@ -246,7 +246,7 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
         if (topk_idx_out || topk_w_out) {
             Work wr = w;
             wr.x16 = nullptr;
-            e = launch_route(p, pl, wr, false, s);
+            e = launch_route(p, pl, wr, 0, s);
         } else {
             e = cudaMemsetAsync(w.ctrl, 0, sizeof(int32_t), s);
             note_launch(-1, s, false, 1);
@@ -257,7 +257,7 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
         case QMOE_PATH_GENERIC: {
             Work wr = w;
             wr.x16 = nullptr;
-            if ((e = launch_route(p, pl, wr, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_route(p, pl, wr, 0, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_generic_fc1(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_generic_fc2(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
@@ -265,11 +265,12 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             return QMOE_OK;
         }
         case QMOE_PATH_DECODE: {
+            const int mode = p.bits == 4 ? 2 : 0;   // layout the decode kernel reads
             if (small_route_ok(p, pl)) {
-                if ((e = launch_route_group_small(p, pl, w, p.bits == 4, s)) != cudaSuccess)
+                if ((e = launch_route_group_small(p, pl, w, mode, s)) != cudaSuccess)
                     return QMOE_ERR_CUDA;
             } else {
-                if ((e = launch_route(p, pl, w, p.bits == 4, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_route(p, pl, w, mode, s)) != cudaSuccess) return QMOE_ERR_CUDA;
                 if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
             if ((e = launch_decode_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
@@ -279,12 +280,12 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
         }
         case QMOE_PATH_GROUPED: {
             // 4-bit: activations in the interleaved operand order of the nibble conversion
-            const bool il = p.bits == 4;
+            const int mode = p.bits == 4 ? 1 : 0;
             if (small_route_ok(p, pl)) {
-                if ((e = launch_route_group_small(p, pl, w, il, s)) != cudaSuccess)
+                if ((e = launch_route_group_small(p, pl, w, mode, s)) != cudaSuccess)
                     return QMOE_ERR_CUDA;
             } else {
-                if ((e = launch_route(p, pl, w, il, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_route(p, pl, w, mode, s)) != cudaSuccess) return QMOE_ERR_CUDA;
                 if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
             if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;

@@ -89,14 +89,16 @@ uint64_t wait_limit_ns();
 int64_t drop_stage();
 
 // ---- launchers (return cudaGetLastError()) ----
-cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,
+// x16_mode: fp16 activation layout (0 natural, 1 4-bit pair order, 2 as 1 with the odd
+// elements divided by 16 for the 4-bit decode kernel).
+cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, int x16_mode,
                          cudaStream_t s);
 cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 // Routing and grouping in a single launch for small batches.
 constexpr int kSmallRouteSlots = 4096;
 bool small_route_ok(const Problem& p, const Plan& pl);
 cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Work& w,
-                                     bool x16_interleaved, cudaStream_t s);
+                                     int x16_mode, cudaStream_t s);
 cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,

@@ -71,11 +71,15 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
 }
 
 // fp16 copy of rows [t0, t0+ntok) of the activations, columns [g_lo, g_hi)
-// in groups of eight, zero padded to Hp.  With interleave8 the eight values of
-// each aligned group are stored in the order 0,4,1,5,2,6,3,7 (the operand
-// order of the decode GEMV).  Threads stride over the (row, group) pairs.
+// in groups of eight, zero padded to Hp.  Layout mode:
+//   0  natural order;
+//   1  each group of eight stored in the order 0,4,1,5,2,6,3,7 (the pair order
+//      of the 4-bit conversion);
+//   2  as 1, with the odd elements (1,3,5,7) divided by 16 (exact): the 4-bit
+//      decode kernel feeds those K positions with 16 * (q - 8).
+// Threads stride over the (row, group) pairs.
 __device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, int64_t H,
-                             __half* __restrict__ x16, int64_t Hp, int interleave8, int64_t g_lo,
+                             __half* __restrict__ x16, int64_t Hp, int mode, int64_t g_lo,
                              int64_t g_hi, int tid, int nthr) {
     const int64_t width = g_hi - g_lo;
     if (width <= 0) return;
@@ -102,9 +106,12 @@ __device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, 
             for (int q = 0; q < 8; ++q) v[q] = (g * 8 + q < H) ? xr[g * 8 + q] : 0.f;
         }
         __half2 h[4];
-        if (interleave8) {
+        if (mode != 0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+            for (int q = 0; q < 4; ++q) {
+                const float f = (mode == 2 && (q & 1)) ? 0.0625f : 1.f;
+                h[q] = __floats2half2_rn(v[q] * f, v[q + 4] * f);
+            }
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
     float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
     const float* __restrict__ x, int64_t H, __half* __restrict__ x16, int64_t Hp,
-    int interleave8, int32_t* __restrict__ ctrl) {
+    int x16_mode, int32_t* __restrict__ ctrl) {
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;        // [E]
     int32_t* s_exp = smem + E;    // [chunk tokens * k]
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
         const int64_t per = (G8 + gridDim.y - 1) / gridDim.y;
         const int64_t g_lo = int64_t(blockIdx.y) * per;
         const int64_t g_hi = g_lo + per < G8 ? g_lo + per : G8;
-        convert_rows(x, t0, ntok, H, x16, Hp, interleave8, g_lo, g_hi, threadIdx.x, blockDim.x);
+        convert_rows(x, t0, ntok, H, x16, Hp, x16_mode, g_lo, g_hi, threadIdx.x, blockDim.x);
     }
     if (blockIdx.y != 0) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && ctrl) ctrl[0] = 0;
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
 __global__ void __launch_bounds__(1024) route_group_small_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
     float* __restrict__ pw, const float* __restrict__ x, int64_t H, __half* __restrict__ x16,
-    int64_t Hp, int interleave8, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int64_t Hp, int x16_mode, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ tiles, int32_t* __restrict__ active, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, int tile_tokens, int32_t* __restrict__ ctrl) {
     extern __shared__ int32_t smem[];
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(1024) route_group_small_kernel(
             const int64_t hi = lo + per < total ? lo + per : total;
             // rows are whole groups; walk the flat (token, group) range
             for (int64_t idx = lo + threadIdx.x; idx < hi; idx += blockDim.x)
-                convert_rows(x, idx / G8, 1, H, x16, Hp, interleave8, idx % G8, idx % G8 + 1, 0, 1);
+                convert_rows(x, idx / G8, 1, H, x16, Hp, x16_mode, idx % G8, idx % G8 + 1, 0, 1);
         }
         return;
     }
@@ -390,7 +397,7 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ sel,
 
 }  // namespace
 
-cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x16_interleaved,
+cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, int x16_mode,
                          cudaStream_t s) {
     const size_t smem = sizeof(int32_t) * (size_t(p.E) + size_t(kRouteTokensPerChunk) * p.k);
     if (smem > 48 * 1024) {
@@ -409,7 +416,7 @@ cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, bool x
     note_launch(QMOE_KERNEL_ROUTE, s, true);
     route_kernel<<<dim3(unsigned(pl.route_chunks), unsigned(ysplit)), kRouteThreads, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
-        x16_interleaved ? 1 : 0, w.ctrl);
+        x16_mode, w.ctrl);
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
 }
@@ -419,7 +426,7 @@ bool small_route_ok(const Problem& p, const Plan& pl) {
 }
 
 cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Work& w,
-                                     bool x16_interleaved, cudaStream_t s) {
+                                     int x16_mode, cudaStream_t s) {
     const size_t smem = sizeof(int32_t) * (3 * size_t(p.E) + 1 + 2 * size_t(pl.slots));
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(route_group_small_kernel,
@@ -432,7 +439,7 @@ cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Wor
     note_launch(QMOE_KERNEL_ROUTE, s, true);
     route_group_small_kernel<<<unsigned(1 + conv), 1024, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, p.x, p.H, w.x16, pl.Hp,
-        x16_interleaved ? 1 : 0, w.counts, w.offsets, w.tiles, w.active, w.perm, w.inv,
+        x16_mode, w.counts, w.offsets, w.tiles, w.active, w.perm, w.inv,
         pl.tile_tokens, w.ctrl);
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
