@@ -76,25 +76,44 @@ struct DecodeArgs {
     int64_t drop_it;            // test hook: stage whose copies the producer skips
 };
 
+// Position in the stage ring: slot and the parity of its current phase.
+struct Ring {
+    uint32_t st = 0, ph = 0;
+    __device__ __forceinline__ void advance(uint32_t n) {
+        if (++st == n) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ void record_error(int32_t* err, int code) {
     atomicCAS(err, 0, code);
 }
 
 // Eight 4-bit codes of `w` (low nibble first, element e in bits 4e..4e+3) ->
-// four fp16 pairs, each exact:
-//   h[0] = (q0, q4) - 8          h[2] = (q2, q6) - 8         (low nibbles of each byte)
-//   h[1] = 16 * ((q1, q5) - 8)   h[3] = 16 * ((q3, q7) - 8)  (high nibbles, kept in place)
-// A nibble OR-ed into the mantissa of fp16 1024 gives 1024 + q; a high nibble
-// left at bits 4..7 gives 1024 + 16 q.  The activations feeding the high
-// pairs are stored divided by 16, so each product is unchanged.
-__device__ __forceinline__ void dequant4(uint32_t w, uint32_t* h) {
-    const __half2 lo_bias = ptx::u32_as_h2(0x64086408u);   // (1032, 1032)
-    const __half2 hi_bias = ptx::u32_as_h2(0x64806480u);   // (1152, 1152)
+// four fp16 pairs, each exact and each 1160 above its weight:
+//   h[0] = 1152 + (q0, q4)         h[1] = 1152 + (q2, q6)        (low nibbles of each byte)
+//   h[2] = 1032 + 16 * (q1, q5)    h[3] = 1032 + 16 * (q3, q7)   (high nibbles, kept in place)
+// A nibble OR-ed into the mantissa of fp16 1152 gives 1152 + q; a high nibble
+// left at bits 4..7 of fp16 1032 gives 1032 + 16 q.  The activations feeding
+// the high pairs are stored divided by 16, so every pair is (q - 8) + 1160 in
+// units of its activation: (1152 + q) - 1160 = q - 8 and
+// (1032 + 16 q) - 1160 = 16 (q - 8).
+__device__ __forceinline__ void biased4(uint32_t w, uint32_t* h) {
     const uint32_t w8 = w >> 8;
-    h[0] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x000F000Fu, 0x64006400u)), lo_bias));
-    h[1] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x00F000F0u, 0x64006400u)), hi_bias));
-    h[2] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x000F000Fu, 0x64006400u)), lo_bias));
-    h[3] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x00F000F0u, 0x64006400u)), hi_bias));
+    h[0] = ptx::and_or(w, 0x000F000Fu, 0x64806480u);
+    h[1] = ptx::and_or(w8, 0x000F000Fu, 0x64806480u);
+    h[2] = ptx::and_or(w, 0x00F000F0u, 0x64086408u);
+    h[3] = ptx::and_or(w8, 0x00F000F0u, 0x64086408u);
+}
+
+// As biased4 with the offset removed: h[0], h[1] = q - 8; h[2], h[3] = 16 (q - 8).
+__device__ __forceinline__ void dequant4(uint32_t w, uint32_t* h) {
+    const __half2 bias = ptx::u32_as_h2(0x64886488u);   // (1160, 1160)
+    biased4(w, h);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = ptx::h2_as_u32(__hsub2(ptx::u32_as_h2(h[q]), bias));
 }
 
 // As dequant4, every pair multiplied by the fp16 scale (block size 16).
@@ -123,20 +142,207 @@ __device__ __forceinline__ float swiglu(float g, float u, float alpha, float bet
 }
 
 // Position of activation column j in a row stored with 8-groups in the
-// order 0,4,1,5,2,6,3,7.
+// order 0,4,2,6,1,5,3,7 (pairs (0,4),(2,6) meet low nibbles, (1,5),(3,7) high).
 __device__ __forceinline__ int64_t perm8(int64_t j) {
-    const int q = int(j & 7);
-    return (j & ~int64_t(7)) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
+    const int q = int(j & 3);
+    const int slot = (q & 1) ? 2 + (q >> 1) : (q >> 1);
+    return (j & ~int64_t(7)) + 2 * slot + ((j >> 2) & 1);
 }
 
 // Stores activation v of column j in the layout the 4-bit FC2 reads (mode 2:
-// pair order, odd columns divided by 16) or in natural order (mode 0).
+// pair order above, odd columns divided by 16) or in natural order (mode 0).
 __device__ __forceinline__ void store_act(__half* row, int64_t j, float v, int mode) {
     if (mode == 2) row[perm8(j)] = __float2half_rn((j & 1) ? v * 0.0625f : v);
     else row[j] = __float2half_rn(v);
 }
 
-template <int BITS, int SMODE, bool FC1>
+// Shared-memory byte offsets of one consumer thread relative to a stage's base.
+// Consumer warp (row group rgi, K half kh) owns rows r_g = 16 rgi + g and
+// r_g + 8 of the unit and the 64-byte segments s = kh and s = kh + 2 of each
+// row's 256 packed bytes; lane (g, c) reads word c of every 16-byte chunk.
+struct ThreadOffsets {
+    uint32_t a[4];   // A word of row r_g in step i of segment s = kh (128-byte swizzle applied)
+    uint32_t b;      // B fragment of token row g at step 0 of segment s = kh
+    uint32_t b8;     // the same for token row g + 8
+    uint32_t s[2];   // block-scaled: scales of row r_g for segments kh and kh + 2
+                     // (post-scaled) or the scale of step 0 (pre-scaled)
+    uint32_t s8;     // distance from row r_g's scales to row r_g + 8's
+};
+
+// The NBS block scales of one row that one 64-byte segment spans.
+template <int NBS>
+__device__ __forceinline__ void load_seg_scales(uint32_t addr, float* v) {
+    if (NBS == 4) {
+        const float4 t = ptx::ld_f32x4(addr);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else if (NBS == 2) {
+        const float2 t = ptx::ld_f32x2(addr);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+        v[0] = ptx::ld_f32(addr);
+    }
+}
+
+// All MMAs of one pipeline stage for one consumer warp.  nsp = how many of the
+// warp's two segments the stage holds (fewer on a ragged last chunk).  NT =
+// token tiles of 8 (2 when more than 8 tokens are routed to the expert).
+// Block-scaled codes accumulate one scale block in a scratch accumulator
+// (exact integer weights times fp16 activations) and fold it into acc with
+// the block's fp32 scale; column-wise codes accumulate directly and are scaled
+// after the K loop; 4-bit codes with 16-element blocks are pre-scaled in fp16.
+template <int BITS, int SMODE, int NBS, int NT>
+__device__ __forceinline__ void consume_stage(uint32_t sA, const ThreadOffsets& o, int nsp, bool ld0,
+                                              bool ld1, uint4 (&bq)[NT], float (&acc)[NT][4],
+                                              float (&accB)[NT][4]) {
+    constexpr uint32_t kSegB = BITS == 4 ? 512u : 256u;   // B bytes between a warp's segments
+    constexpr uint32_t kStepB = BITS == 4 ? 64u : 32u;    // B bytes per step
+    constexpr int IPB = NBS > 0 ? 4 / NBS : 1;            // steps per scale block
+#pragma unroll
+    for (int sp = 0; sp < 2; ++sp) {
+        if (sp >= nsp) break;
+        float sg[4], s8[4];
+        if constexpr (SMODE == kScalePost) {
+            load_seg_scales<NBS>(sA + o.s[sp], sg);
+            load_seg_scales<NBS>(sA + o.s[sp] + o.s8, s8);
+        }
+        float tmp[NT][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t aw = sA + o.a[i] + uint32_t(sp) * kBoxTile;
+            const uint32_t wa = ptx::ld_u32(aw);
+            const uint32_t wb = ptx::ld_u32(aw + 8u * kBoxBytes);
+            // B fragment: 8 fp16 (16 bytes) per step for 4-bit codes, 4 (8 bytes) for
+            // 8-bit.  Lanes of token rows >= ne skip the load (no shared-memory
+            // traffic) and keep stale registers, which only reach output columns
+            // that are never stored.
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t ba = sA + (nt ? o.b8 : o.b) + uint32_t(sp) * kSegB + uint32_t(i) * kStepB;
+                if constexpr (BITS == 4)
+                    ptx::ld128_pred(bq[nt], ba, nt ? ld1 : ld0);
+                else
+                    ptx::ld64_pred(bq[nt].x, bq[nt].y, ba, nt ? ld1 : ld0);
+            }
+            const bool first = i % IPB == 0, last = i % IPB == IPB - 1;
+            if constexpr (BITS == 4 && SMODE == kScalePost) {
+                uint32_t ha[4], hb[4];
+                dequant4(wa, ha);
+                dequant4(wb, hb);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    // low pairs (K 0,4 | 2,6) with b.x|b.y; high pairs (K 1,5 | 3,7) with b.z|b.w
+                    if (first)
+                        ptx::mma_16816_z(tmp[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                    else
+                        ptx::mma_16816(tmp[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                    ptx::mma_16816(tmp[nt], ha[2], hb[2], ha[3], hb[3], bq[nt].z, bq[nt].w);
+                    if (last) {
+                        acc[nt][0] = fmaf(sg[i / IPB], tmp[nt][0], acc[nt][0]);
+                        acc[nt][1] = fmaf(sg[i / IPB], tmp[nt][1], acc[nt][1]);
+                        acc[nt][2] = fmaf(s8[i / IPB], tmp[nt][2], acc[nt][2]);
+                        acc[nt][3] = fmaf(s8[i / IPB], tmp[nt][3], acc[nt][3]);
+                    }
+                }
+            } else if constexpr (BITS == 4) {
+                uint32_t ha[4], hb[4];
+                if constexpr (SMODE == kScalePre) {
+                    const uint32_t sa = sA + o.s[0] + uint32_t(sp) * 64u + uint32_t(i) * 8u;
+                    dequant4_scaled(wa, __float2half2_rn(ptx::ld_f32(sa)), ha);
+                    dequant4_scaled(wb, __float2half2_rn(ptx::ld_f32(sa + o.s8)), hb);
+                } else {
+                    dequant4(wa, ha);
+                    dequant4(wb, hb);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    ptx::mma_16816(acc[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                    ptx::mma_16816(accB[nt], ha[2], hb[2], ha[3], hb[3], bq[nt].z, bq[nt].w);
+                }
+            } else {
+                uint32_t ha[2], hb[2];
+                dequant8(wa, ha);
+                dequant8(wb, hb);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if constexpr (SMODE == kScalePost) {
+                        if (first)
+                            ptx::mma_16816_z(tmp[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                        else
+                            ptx::mma_16816(tmp[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                        if (last) {
+                            acc[nt][0] = fmaf(sg[i / IPB], tmp[nt][0], acc[nt][0]);
+                            acc[nt][1] = fmaf(sg[i / IPB], tmp[nt][1], acc[nt][1]);
+                            acc[nt][2] = fmaf(s8[i / IPB], tmp[nt][2], acc[nt][2]);
+                            acc[nt][3] = fmaf(s8[i / IPB], tmp[nt][3], acc[nt][3]);
+                        }
+                    } else if (i & 1) {
+                        ptx::mma_16816(accB[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                    } else {
+                        ptx::mma_16816(acc[nt], ha[0], hb[0], ha[1], hb[1], bq[nt].x, bq[nt].y);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The K loop of one unit for one consumer warp: waits for each stage, runs its
+// MMAs and releases it.  Returns false when a wait gave up.  On return, out
+// holds the warp's partial sums (column-wise scales applied).
+template <int BITS, int SMODE, int NBS, int NT>
+__device__ __forceinline__ bool consume_unit(const DecodeArgs& a, uint64_t* full_bar,
+                                             uint64_t* empty_bar, volatile int* abort_flag,
+                                             uint32_t sbase0, const ThreadOffsets& o, Ring& ring,
+                                             int c0, int c1, int tail_nsp, int ne, int g, int lane,
+                                             float scol_g, float scol_g8, float (&out)[2][4]) {
+    constexpr bool POST = SMODE == kScalePost;
+    float acc[NT][4], accB[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[nt][q] = accB[nt][q] = 0.f;
+    uint4 bq[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) bq[nt] = make_uint4(0u, 0u, 0u, 0u);
+    const bool ld0 = g < ne, ld1 = g + 8 < ne;
+    for (int kc = c0; kc < c1; ++kc, ring.advance(a.nstages)) {
+        if (!ptx::mbar_wait(&full_bar[ring.st], ring.ph, a.wait_ns, abort_flag)) {
+            if (lane == 0) {
+                record_error(a.err, QMOE_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return false;
+        }
+        const uint32_t sA = ptx::launder(sbase0 + ring.st * a.stage_bytes);
+        // the warp's segments in this chunk: both, except on a ragged last chunk
+        const int nsp = kc == a.nkc - 1 ? tail_nsp : 2;
+        consume_stage<BITS, SMODE, NBS, NT>(sA, o, nsp, ld0, ld1, bq, acc, accB);
+        // every shared load of this stage feeds the accumulators: finish them first
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                ptx::depend(acc[nt][q]);
+                if (!POST) ptx::depend(accB[nt][q]);
+            }
+        __syncwarp();
+        ptx::mbar_arrive_if(&empty_bar[ring.st], lane == 0);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int src = nt < NT ? nt : 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float v = 0.f;
+            if (nt < NT) v = POST ? acc[src][q] : acc[src][q] + accB[src][q];
+            if (SMODE == kScaleCol) v *= q < 2 ? scol_g : scol_g8;
+            out[nt][q] = v;
+        }
+    }
+    return true;
+}
+
+template <int BITS, int SMODE, int NBS, bool FC1>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -174,7 +380,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             ptx::prefetch_tmap(&a.tm_w);
             if (!SCOL) ptx::prefetch_tmap(&a.tm_s);
         }
-        uint32_t it = 0;
+        uint32_t it = 0;   // stages issued (for the drain after a timeout)
+        Ring ring;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int ks = int(u % a.splits);
@@ -187,10 +394,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             const int32_t row0 = int32_t(int64_t(e) * a.N + int64_t(rb) * kDecRows);
             int64_t brow = 0;
             if (lane < ne) brow = FC1 ? int64_t(a.perm[off + lane] / a.topk) : int64_t(off + lane);
-            for (int kc = c0; kc < c1; ++kc, ++it) {
-                const int st = int(it % a.nstages);
-                const uint32_t ph = (it / a.nstages) & 1u;
-                if (!ptx::mbar_wait(&empty_bar[st], ph ^ 1u, a.wait_ns, &abort_flag)) {
+            for (int kc = c0; kc < c1; ++kc, ++it, ring.advance(a.nstages)) {
+                const uint32_t st = ring.st;
+                if (!ptx::mbar_wait_sleep(&empty_bar[st], ring.ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -236,11 +442,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     const int r_g = 16 * rgi + g;   // row of this thread inside the 128-row box (and r_g + 8)
     float* red = reinterpret_cast<float*>(smem + size_t(a.nstages) * a.stage_bytes);
     const uint32_t sbase0 = ptx::smem_u32(smem);
-    uint32_t it = 0;
+    ThreadOffsets o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o.a[i] = uint32_t(r_g) * kBoxBytes + (uint32_t(((kh << 2) + i) ^ g) << 4) + uint32_t(c) * 4u;
+    o.b = a.off_b + uint32_t(g) * a.pitch_b +
+          (BITS == 4 ? uint32_t(256 * kh + 16 * c) : uint32_t(128 * kh + 8 * c));
+    o.b8 = o.b + 8u * a.pitch_b;
+    o.s8 = 8u * uint32_t(a.nsc) * 4u;
+    if (SMODE == kScalePost) {
+#pragma unroll
+        for (int sp = 0; sp < 2; ++sp)
+            o.s[sp] = a.off_s + uint32_t(r_g * a.nsc + ((SEGK * (kh + 2 * sp)) >> a.lbs)) * 4u;
+    } else {
+        // pre-scaled (block size 16): the scale of K index 128 s + 32 i + 8 c
+        o.s[0] = a.off_s + uint32_t(r_g * a.nsc) * 4u + uint32_t(32 * kh + 4 * (c >> 1));
+        o.s[1] = 0;
+    }
+    // segments of this warp in the last K chunk (ragged when K is not a multiple of KC)
+    const int tail_seg = int((a.K - int64_t(a.nkc - 1) * KC) / SEGK);
+    const int tail_nsp = int(tail_seg > kh) + int(tail_seg > kh + 2);
+    Ring ring;
     uint32_t un = 0;   // units processed by this CTA (reduction buffer parity)
-    // B fragments keep stale values for token columns >= ne; those columns of
-    // the MMA result are never stored.
-    uint4 bq[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++un) {
         const int ks = int(u % a.splits);
         const int rb = int((u / a.splits) % a.n_rb);
@@ -257,142 +480,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             scol_g = rg < a.N ? sc[rg] : 0.f;
             scol_g8 = rg8 < a.N ? sc[rg8] : 0.f;
         }
-        float acc[2][4], accB[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] = accB[nt][q] = 0.f;
-        const bool two = ne > 8;
-        const bool ld0 = g < ne, ld1 = g + 8 < ne;
-
-        for (int kc = c0; kc < c1; ++kc, ++it) {
-            const int st = int(it % a.nstages);
-            const uint32_t ph = (it / a.nstages) & 1u;
-            if (!ptx::mbar_wait(&full_bar[st], ph, a.wait_ns, &abort_flag)) {
-                if (lane == 0) {
-                    record_error(a.err, QMOE_DEVERR_TIMEOUT);
-                    abort_flag = 1;
-                }
-                return;
-            }
-            const uint32_t sA = ptx::launder(sbase0 + uint32_t(st) * a.stage_bytes);
-            const uint32_t sS = sA + a.off_s;
-            const uint32_t sB = sA + a.off_b;
-            const uint32_t rowA = sA + uint32_t(r_g) * kBoxBytes;
-            const uint32_t rowA8 = rowA + 8u * kBoxBytes;
-            const int64_t krem = a.K - int64_t(kc) * KC;
-            const int nseg = int(krem < KC ? krem : KC) / SEGK;
-            for (int s = kh; s < nseg; s += 2) {
-                const uint32_t half = uint32_t(s >> 1) * kBoxTile;
-                float sgv[4], sg8v[4];
-                if (SMODE == kScalePost) {
-                    // word i of every lane lies in scale block (SEGK*s + SEGK/4*i) >> lbs;
-                    // the seg spans 4, 2 or 1 blocks (block sizes SEGK/4, SEGK/2, >= SEGK)
-                    const int nbs = SEGK >> a.lbs;   // blocks per segment (0 when bs > SEGK)
-                    const int si0 = (SEGK * s) >> a.lbs;
-                    const uint32_t a0 = sS + uint32_t(r_g * a.nsc + si0) * 4u;
-                    const uint32_t a8 = a0 + uint32_t(8 * a.nsc) * 4u;
-                    if (nbs >= 4) {
-                        const float4 v0 = ptx::ld_f32x4(a0), v8 = ptx::ld_f32x4(a8);
-                        sgv[0] = v0.x; sgv[1] = v0.y; sgv[2] = v0.z; sgv[3] = v0.w;
-                        sg8v[0] = v8.x; sg8v[1] = v8.y; sg8v[2] = v8.z; sg8v[3] = v8.w;
-                    } else if (nbs == 2) {
-                        const float2 v0 = ptx::ld_f32x2(a0), v8 = ptx::ld_f32x2(a8);
-                        sgv[0] = sgv[1] = v0.x; sgv[2] = sgv[3] = v0.y;
-                        sg8v[0] = sg8v[1] = v8.x; sg8v[2] = sg8v[3] = v8.y;
-                    } else {
-                        const float v0 = ptx::ld_f32(a0), v8 = ptx::ld_f32(a8);
-                        sgv[0] = sgv[1] = sgv[2] = sgv[3] = v0;
-                        sg8v[0] = sg8v[1] = sg8v[2] = sg8v[3] = v8;
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // word i of lane c: packed bytes 16i + 4c of this 64-byte segment
-                    const int jchunk = ((s & 1) << 2) + i;
-                    const uint32_t offw = half + uint32_t((jchunk ^ g) << 4) + uint32_t(c) * 4u;
-                    const uint32_t wa = ptx::ld_u32(rowA + offw);
-                    const uint32_t wb = ptx::ld_u32(rowA8 + offw);
-                    const int kin = BITS == 4 ? (SEGK * s + 32 * i + 8 * c) : (SEGK * s + 16 * i + 4 * c);
-                    const uint32_t boff = uint32_t(kin) * 2u;
-                    if (BITS == 4) {
-                        uint32_t hg[4], hg8[4];
-                        if (SMODE == kScalePre) {
-                            const int si = kin >> a.lbs;
-                            const __half2 s0 = __float2half2_rn(ptx::ld_f32(sS + uint32_t(r_g * a.nsc + si) * 4u));
-                            const __half2 s8 = __float2half2_rn(ptx::ld_f32(sS + uint32_t((r_g + 8) * a.nsc + si) * 4u));
-                            dequant4_scaled(wa, s0, hg);
-                            dequant4_scaled(wb, s8, hg8);
-                        } else {
-                            dequant4(wa, hg);
-                            dequant4(wb, hg8);
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            if (nt == 1 && !two) break;
-                            ptx::ld128_pred(bq[nt], sB + uint32_t(g + 8 * nt) * a.pitch_b + boff,
-                                            nt == 0 ? ld0 : ld1);
-                            // low pairs (K 0,4 | 2,6) with b.x|b.z; high pairs (K 1,5 | 3,7),
-                            // 16x larger, with b.y|b.w stored divided by 16
-                            if (SMODE == kScalePost) {
-                                float tmp[4];
-                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[2], hg8[2], bq[nt].x, bq[nt].z);
-                                ptx::mma_16816(tmp, hg[1], hg8[1], hg[3], hg8[3], bq[nt].y, bq[nt].w);
-                                acc[nt][0] = fmaf(sgv[i], tmp[0], acc[nt][0]);
-                                acc[nt][1] = fmaf(sgv[i], tmp[1], acc[nt][1]);
-                                acc[nt][2] = fmaf(sg8v[i], tmp[2], acc[nt][2]);
-                                acc[nt][3] = fmaf(sg8v[i], tmp[3], acc[nt][3]);
-                            } else {
-                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[2], hg8[2], bq[nt].x, bq[nt].z);
-                                ptx::mma_16816(accB[nt], hg[1], hg8[1], hg[3], hg8[3], bq[nt].y, bq[nt].w);
-                            }
-                        }
-                    } else {
-                        uint32_t hg[2], hg8[2];
-                        dequant8(wa, hg);
-                        dequant8(wb, hg8);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            if (nt == 1 && !two) break;
-                            ptx::ld64_pred(bq[nt].x, bq[nt].y,
-                                           sB + uint32_t(g + 8 * nt) * a.pitch_b + boff,
-                                           nt == 0 ? ld0 : ld1);
-                            if (SMODE == kScalePost) {
-                                float tmp[4];
-                                ptx::mma_16816_z(tmp, hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
-                                acc[nt][0] = fmaf(sgv[i], tmp[0], acc[nt][0]);
-                                acc[nt][1] = fmaf(sgv[i], tmp[1], acc[nt][1]);
-                                acc[nt][2] = fmaf(sg8v[i], tmp[2], acc[nt][2]);
-                                acc[nt][3] = fmaf(sg8v[i], tmp[3], acc[nt][3]);
-                            } else if (i & 1) {
-                                ptx::mma_16816(accB[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
-                            } else {
-                                ptx::mma_16816(acc[nt], hg[0], hg8[0], hg[1], hg8[1], bq[nt].x, bq[nt].y);
-                            }
-                        }
-                    }
-                }
-            }
-            // every shared load of this stage feeds the accumulators: finish them first
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    ptx::depend(acc[nt][q]);
-                    ptx::depend(accB[nt][q]);
-                }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty_bar[st]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[nt][q] += accB[nt][q];
-            if (SCOL) {
-                acc[nt][0] *= scol_g; acc[nt][1] *= scol_g;
-                acc[nt][2] *= scol_g8; acc[nt][3] *= scol_g8;
-            }
-        }
+        float acc[2][4];
+        const bool ok = ne > 8
+            ? consume_unit<BITS, SMODE, NBS, 2>(a, full_bar, empty_bar, &abort_flag, sbase0, o, ring,
+                                                c0, c1, tail_nsp, ne, g, lane, scol_g, scol_g8, acc)
+            : consume_unit<BITS, SMODE, NBS, 1>(a, full_bar, empty_bar, &abort_flag, sbase0, o, ring,
+                                                c0, c1, tail_nsp, ne, g, lane, scol_g, scol_g8, acc);
+        if (!ok) return;
 
         // ---- K-half 1 hands its partial sums to K-half 0 through shared memory ----
         const int rb_buf = int(un & 1u);
@@ -489,9 +583,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     }
 }
 
-template <int BITS, int SMODE, bool FC1>
+template <int BITS, int SMODE, int NBS, bool FC1>
 cudaError_t launch_variant(const DecodeArgs& args, int grid, size_t smem, cudaStream_t s) {
-    auto kern = decode_gemv_kernel<BITS, SMODE, FC1>;
+    auto kern = decode_gemv_kernel<BITS, SMODE, NBS, FC1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, kDecThreads, smem, s>>>(args);
@@ -572,8 +666,10 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     a.pitch_b = uint32_t(KC * 2 + (p.bits == 4 ? 64 : 32));
     a.off_s = bytes_a;
     a.off_b = bytes_a + ((bytes_s + 127u) & ~127u);
-    const int max_tok = int(std::min<int64_t>(p.T, kDecMaxTokens));
-    a.stage_bytes = (a.off_b + uint32_t(max_tok) * a.pitch_b + 1023u) & ~1023u;
+    // token rows per stage: every consumer lane reads row g < 8 (and g + 8 when
+    // more than 8 tokens can be routed), so those rows exist even when unused
+    const int b_rows = p.T > 8 ? kDecMaxTokens : 8;
+    a.stage_bytes = (a.off_b + uint32_t(b_rows) * a.pitch_b + 1023u) & ~1023u;
     a.act_out = static_cast<__half*>(w.act);
     a.act_pitch = pl.Ip;
     a.act = p.act;
@@ -598,13 +694,22 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
     note_launch(kid, s, true);
     cudaError_t e;
     const int smode = scol ? kScaleCol : (p.bits == 4 && p.bs < 32 ? kScalePre : kScalePost);
-#define QMOE_DEC_LAUNCH(B, M) \
-    (fc1 ? launch_variant<B, M, true>(a, grid, smem, s) : launch_variant<B, M, false>(a, grid, smem, s))
+    // block scales per 64-byte segment (128 K for 4-bit, 64 K for 8-bit codes), at most 4
+    const int64_t segk = p.bits == 4 ? 128 : 64;
+    const int nbs = scol ? 0 : (segk / p.bs >= 4 ? 4 : segk / p.bs >= 2 ? 2 : 1);
+#define QMOE_DEC_LAUNCH(B, M, NB) \
+    (fc1 ? launch_variant<B, M, NB, true>(a, grid, smem, s) : launch_variant<B, M, NB, false>(a, grid, smem, s))
     if (p.bits == 4) {
-        e = smode == kScaleCol ? QMOE_DEC_LAUNCH(4, kScaleCol)
-            : smode == kScalePost ? QMOE_DEC_LAUNCH(4, kScalePost) : QMOE_DEC_LAUNCH(4, kScalePre);
+        if (smode == kScaleCol) e = QMOE_DEC_LAUNCH(4, kScaleCol, 0);
+        else if (smode == kScalePre) e = QMOE_DEC_LAUNCH(4, kScalePre, 0);
+        else if (nbs == 4) e = QMOE_DEC_LAUNCH(4, kScalePost, 4);
+        else if (nbs == 2) e = QMOE_DEC_LAUNCH(4, kScalePost, 2);
+        else e = QMOE_DEC_LAUNCH(4, kScalePost, 1);
     } else {
-        e = smode == kScaleCol ? QMOE_DEC_LAUNCH(8, kScaleCol) : QMOE_DEC_LAUNCH(8, kScalePost);
+        if (smode == kScaleCol) e = QMOE_DEC_LAUNCH(8, kScaleCol, 0);
+        else if (nbs == 4) e = QMOE_DEC_LAUNCH(8, kScalePost, 4);
+        else if (nbs == 2) e = QMOE_DEC_LAUNCH(8, kScalePost, 2);
+        else e = QMOE_DEC_LAUNCH(8, kScalePost, 1);
     }
 #undef QMOE_DEC_LAUNCH
     note_launch(kid, s, false);

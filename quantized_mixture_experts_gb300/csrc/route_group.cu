@@ -75,8 +75,10 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
 //   0  natural order;
 //   1  each group of eight stored in the order 0,4,1,5,2,6,3,7 (the pair order
 //      of the 4-bit conversion);
-//   2  as 1, with the odd elements (1,3,5,7) divided by 16 (exact): the 4-bit
-//      decode kernel feeds those K positions with 16 * (q - 8).
+//   2  each group of eight stored in the order 0,4,2,6,1,5,3,7 with the odd
+//      elements divided by 16 (exact): the 4-bit decode kernel pairs
+//      (0,4),(2,6) with low nibbles and (1,5),(3,7) with high nibbles, which
+//      it feeds with 16x the code.
 // Threads stride over the (row, group) pairs.
 __device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, int64_t H,
                              __half* __restrict__ x16, int64_t Hp, int mode, int64_t g_lo,
@@ -106,11 +108,15 @@ __device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, 
             for (int q = 0; q < 8; ++q) v[q] = (g * 8 + q < H) ? xr[g * 8 + q] : 0.f;
         }
         __half2 h[4];
-        if (mode != 0) {
+        if (mode == 1) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+        } else if (mode == 2) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float f = (mode == 2 && (q & 1)) ? 0.0625f : 1.f;
-                h[q] = __floats2half2_rn(v[q] * f, v[q + 4] * f);
+                const int src = (q >> 1) + 2 * (q & 1);     // pairs (0,4),(2,6),(1,5),(3,7)
+                const float f = (src & 1) ? 0.0625f : 1.f;
+                h[q] = __floats2half2_rn(v[src] * f, v[src + 4] * f);
             }
         } else {
 #pragma unroll
