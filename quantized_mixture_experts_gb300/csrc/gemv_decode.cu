@@ -31,16 +31,16 @@ namespace qmoe {
 namespace {
 
 constexpr int kDecRowGroups = 8;               // 16-row MMA groups per unit
-constexpr int kDecConsumers = 2 * kDecRowGroups; // two K halves per row group
+constexpr int kDecKParts = 2;                  // consumer warps per row group (K split among them)
+constexpr int kDecConsumers = kDecKParts * kDecRowGroups;
 constexpr int kDecThreads = 32 * (1 + kDecConsumers);
 constexpr int kDecStages = 4;                  // upper bound; the launch picks what fits
 constexpr int kDecRows = 16 * kDecRowGroups;   // 128 weight rows per unit
-constexpr int kDecRedBytes = 2 * kDecRowGroups * 32 * 8 * 4;
+constexpr int kDecRedBytes = kDecKParts > 1 ? 2 * kDecRowGroups * 32 * 8 * 4 : 0;
 constexpr int kChunkBytes = 256;               // packed bytes per row per stage
 constexpr int kBoxBytes = 128;                 // one 128-byte swizzle span
 constexpr int kBoxTile = kBoxBytes * kDecRows; // 16 KB per weight box
 constexpr int kDecMaxTokens = 16;
-constexpr int kTargetUnitsPerSm = 10;
 constexpr unsigned kFull = 0xffffffffu;
 // Bound on the waits that drain a CTA's own copies / MMAs before it exits after
 // a timeout: independent of the (possibly tiny) configured wait limit.
@@ -156,17 +156,24 @@ __device__ __forceinline__ void store_act(__half* row, int64_t j, float v, int m
     else row[j] = __float2half_rn(v);
 }
 
+// Expert of work unit u (units are ordered expert-major: touched expert, then
+// 128-row block, then K split), or -1 past the last unit.
+__device__ __forceinline__ int unit_expert(const DecodeArgs& a, int64_t u, int64_t units) {
+    return u < units ? __ldg(a.active + u / (int64_t(a.splits) * a.n_rb)) : -1;
+}
+
 // Shared-memory byte offsets of one consumer thread relative to a stage's base.
-// Consumer warp (row group rgi, K half kh) owns rows r_g = 16 rgi + g and
-// r_g + 8 of the unit and the 64-byte segments s = kh and s = kh + 2 of each
+// Consumer warp (row group rgi, K part kh) owns rows r_g = 16 rgi + g and
+// r_g + 8 of the unit and the 64-byte segments s = kh, kh + kDecKParts, ... of each
 // row's 256 packed bytes; lane (g, c) reads word c of every 16-byte chunk.
 struct ThreadOffsets {
-    uint32_t a[4];   // A word of row r_g in step i of segment s = kh (128-byte swizzle applied)
-    uint32_t b;      // B fragment of token row g at step 0 of segment s = kh
-    uint32_t b8;     // the same for token row g + 8
-    uint32_t s[2];   // block-scaled: scales of row r_g for segments kh and kh + 2
-                     // (post-scaled) or the scale of step 0 (pre-scaled)
-    uint32_t s8;     // distance from row r_g's scales to row r_g + 8's
+    uint32_t a[2][4];   // A word of row r_g in step i of an even / odd segment
+                        // (128-byte swizzle applied; first box)
+    uint32_t b;         // B fragment of token row g at step 0 of the warp's first segment
+    uint32_t b8;        // the same for token row g + 8
+    uint32_t s;         // block scales of row r_g for the warp's first segment (post-scaled)
+                        // or the scale of its step 0 (pre-scaled)
+    uint32_t s8;        // distance from row r_g's scales to row r_g + 8's
 };
 
 // The NBS block scales of one row that one 64-byte segment spans.
@@ -194,21 +201,26 @@ template <int BITS, int SMODE, int NBS, int NT>
 __device__ __forceinline__ void consume_stage(uint32_t sA, const ThreadOffsets& o, int nsp, bool ld0,
                                               bool ld1, uint4 (&bq)[NT], float (&acc)[NT][4],
                                               float (&accB)[NT][4]) {
-    constexpr uint32_t kSegB = BITS == 4 ? 512u : 256u;   // B bytes between a warp's segments
+    constexpr int SPW = 4 / kDecKParts;                    // segments per warp per stage
+    constexpr uint32_t kSegB = (BITS == 4 ? 256u : 128u) * kDecKParts;   // B bytes between them
     constexpr uint32_t kStepB = BITS == 4 ? 64u : 32u;    // B bytes per step
     constexpr int IPB = NBS > 0 ? 4 / NBS : 1;            // steps per scale block
 #pragma unroll
-    for (int sp = 0; sp < 2; ++sp) {
+    for (int sp = 0; sp < SPW; ++sp) {
         if (sp >= nsp) break;
+        // segment s = kh + kDecKParts * sp: box s / 2, parity s % 2 (kh is folded into o)
+        const int par = kDecKParts == 1 ? (sp & 1) : 0;
+        const uint32_t box = uint32_t(kDecKParts == 1 ? (sp >> 1) : (kDecKParts * sp) >> 1) * kBoxTile;
         float sg[4], s8[4];
         if constexpr (SMODE == kScalePost) {
-            load_seg_scales<NBS>(sA + o.s[sp], sg);
-            load_seg_scales<NBS>(sA + o.s[sp] + o.s8, s8);
+            const uint32_t sa = sA + o.s + uint32_t(kDecKParts * sp * NBS) * 4u;
+            load_seg_scales<NBS>(sa, sg);
+            load_seg_scales<NBS>(sa + o.s8, s8);
         }
         float tmp[NT][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t aw = sA + o.a[i] + uint32_t(sp) * kBoxTile;
+            const uint32_t aw = sA + o.a[par][i] + box;
             const uint32_t wa = ptx::ld_u32(aw);
             const uint32_t wb = ptx::ld_u32(aw + 8u * kBoxBytes);
             // B fragment: 8 fp16 (16 bytes) per step for 4-bit codes, 4 (8 bytes) for
@@ -246,7 +258,7 @@ __device__ __forceinline__ void consume_stage(uint32_t sA, const ThreadOffsets& 
             } else if constexpr (BITS == 4) {
                 uint32_t ha[4], hb[4];
                 if constexpr (SMODE == kScalePre) {
-                    const uint32_t sa = sA + o.s[0] + uint32_t(sp) * 64u + uint32_t(i) * 8u;
+                    const uint32_t sa = sA + o.s + uint32_t(32 * kDecKParts * sp + 8 * i);
                     dequant4_scaled(wa, __float2half2_rn(ptx::ld_f32(sa)), ha);
                     dequant4_scaled(wb, __float2half2_rn(ptx::ld_f32(sa + o.s8)), hb);
                 } else {
@@ -315,7 +327,7 @@ __device__ __forceinline__ bool consume_unit(const DecodeArgs& a, uint64_t* full
         }
         const uint32_t sA = ptx::launder(sbase0 + ring.st * a.stage_bytes);
         // the warp's segments in this chunk: both, except on a ragged last chunk
-        const int nsp = kc == a.nkc - 1 ? tail_nsp : 2;
+        const int nsp = kc == a.nkc - 1 ? tail_nsp : 4 / kDecKParts;
         consume_stage<BITS, SMODE, NBS, NT>(sA, o, nsp, ld0, ld1, bq, acc, accB);
         // every shared load of this stage feeds the accumulators: finish them first
 #pragma unroll
@@ -383,17 +395,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
         uint32_t it = 0;   // stages issued (for the drain after a timeout)
         Ring ring;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        // Unit metadata is a chain of dependent loads (expert -> its token count
+        // and offset -> its token rows); it is loaded ahead of use (experts three
+        // units ahead, counts two, token rows one) so that the producer never waits
+        // on it between units.
+        const int64_t G = gridDim.x;
+        int64_t u = blockIdx.x;
+        int e0 = unit_expert(a, u, units), e1 = unit_expert(a, u + G, units);
+        int e2 = unit_expert(a, u + 2 * G, units);
+        int ne0 = e0 >= 0 ? __ldg(a.counts + e0) : 0, off0 = e0 >= 0 ? __ldg(a.offsets + e0) : 0;
+        int ne1 = e1 >= 0 ? __ldg(a.counts + e1) : 0, off1 = e1 >= 0 ? __ldg(a.offsets + e1) : 0;
+        auto token_row = [&](int ne_, int off_) -> int64_t {
+            if (lane >= ne_) return 0;
+            return FC1 ? int64_t(__ldg(a.perm + off_ + lane) / a.topk) : int64_t(off_ + lane);
+        };
+        int64_t brow0 = token_row(ne0, off0);
+        for (; u < units && ok; u += G) {
+            const int e3 = unit_expert(a, u + 3 * G, units);
+            const int ne2 = e2 >= 0 ? __ldg(a.counts + e2) : 0;
+            const int off2 = e2 >= 0 ? __ldg(a.offsets + e2) : 0;
+            const int64_t brow1 = token_row(ne1, off1);
+            const int e = e0, ne = ne0;
+            const int64_t brow = brow0;
             const int ks = int(u % a.splits);
             const int rb = int((u / a.splits) % a.n_rb);
-            const int ai = int(u / (int64_t(a.splits) * a.n_rb));
-            const int e = a.active[ai];
-            const int ne = a.counts[e];
-            const int off = a.offsets[e];
             const int c0 = ks * a.cps, c1 = min(a.nkc, c0 + a.cps);
             const int32_t row0 = int32_t(int64_t(e) * a.N + int64_t(rb) * kDecRows);
-            int64_t brow = 0;
-            if (lane < ne) brow = FC1 ? int64_t(a.perm[off + lane] / a.topk) : int64_t(off + lane);
             for (int kc = c0; kc < c1; ++kc, ++it, ring.advance(a.nstages)) {
                 const uint32_t st = ring.st;
                 if (!ptx::mbar_wait_sleep(&empty_bar[st], ring.ph ^ 1u, a.wait_ns, &abort_flag)) {
@@ -421,6 +448,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                                   a.b_src + brow * a.b_pitch + int64_t(kc) * KC, bbytes,
                                   &full_bar[st]);
             }
+            e0 = e1; ne0 = ne1; off0 = off1; brow0 = brow1;
+            e1 = e2; ne1 = ne2; off1 = off2;
+            e2 = e3;
         }
         if (!ok && lane == 0) {
             record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -444,34 +474,56 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     const uint32_t sbase0 = ptx::smem_u32(smem);
     ThreadOffsets o;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        o.a[i] = uint32_t(r_g) * kBoxBytes + (uint32_t(((kh << 2) + i) ^ g) << 4) + uint32_t(c) * 4u;
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // the warp's segments of parity p (one parity only with two K parts)
+            const int par = kDecKParts == 1 ? p : (kh & 1);
+            o.a[p][i] = uint32_t(r_g) * kBoxBytes + (uint32_t(((par << 2) + i) ^ g) << 4) +
+                        uint32_t(c) * 4u;
+        }
     o.b = a.off_b + uint32_t(g) * a.pitch_b +
           (BITS == 4 ? uint32_t(256 * kh + 16 * c) : uint32_t(128 * kh + 8 * c));
     o.b8 = o.b + 8u * a.pitch_b;
     o.s8 = 8u * uint32_t(a.nsc) * 4u;
     if (SMODE == kScalePost) {
-#pragma unroll
-        for (int sp = 0; sp < 2; ++sp)
-            o.s[sp] = a.off_s + uint32_t(r_g * a.nsc + ((SEGK * (kh + 2 * sp)) >> a.lbs)) * 4u;
+        // segment s spans scale blocks s * NBS .. s * NBS + NBS - 1 (block size <= segment)
+        o.s = a.off_s + uint32_t(r_g * a.nsc + kh * NBS) * 4u;
     } else {
         // pre-scaled (block size 16): the scale of K index 128 s + 32 i + 8 c
-        o.s[0] = a.off_s + uint32_t(r_g * a.nsc) * 4u + uint32_t(32 * kh + 4 * (c >> 1));
-        o.s[1] = 0;
+        o.s = a.off_s + uint32_t(r_g * a.nsc) * 4u + uint32_t(32 * kh + 4 * (c >> 1));
     }
     // segments of this warp in the last K chunk (ragged when K is not a multiple of KC)
     const int tail_seg = int((a.K - int64_t(a.nkc - 1) * KC) / SEGK);
-    const int tail_nsp = int(tail_seg > kh) + int(tail_seg > kh + 2);
+    const int tail_nsp = tail_seg > kh ? (tail_seg - kh + kDecKParts - 1) / kDecKParts : 0;
     Ring ring;
     uint32_t un = 0;   // units processed by this CTA (reduction buffer parity)
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++un) {
+    // unit metadata loaded ahead of use (experts two units ahead, counts one)
+    const int64_t G = gridDim.x;
+    int e_cur = unit_expert(a, blockIdx.x, units);
+    int ne_cur = e_cur >= 0 ? __ldg(a.counts + e_cur) : 0;
+    int off_cur = e_cur >= 0 ? __ldg(a.offsets + e_cur) : 0;
+    int e_nxt = unit_expert(a, blockIdx.x + G, units);
+    for (int64_t u = blockIdx.x; u < units; u += G, ++un) {
+        const int ne_nxt = e_nxt >= 0 ? __ldg(a.counts + e_nxt) : 0;
+        const int off_nxt = e_nxt >= 0 ? __ldg(a.offsets + e_nxt) : 0;
+        const int e_nn = unit_expert(a, u + 2 * G, units);
+        const int e = e_cur, ne = ne_cur, off = off_cur;
+        e_cur = e_nxt; ne_cur = ne_nxt; off_cur = off_nxt; e_nxt = e_nn;
         const int ks = int(u % a.splits);
         const int rb = int((u / a.splits) % a.n_rb);
-        const int ai = int(u / (int64_t(a.splits) * a.n_rb));
-        const int e = a.active[ai];
-        const int ne = a.counts[e];
-        const int off = a.offsets[e];
         const int c0 = ks * a.cps, c1 = min(a.nkc, c0 + a.cps);
+        // FC2 stores by original slot: fetch the slot ids now, use them after the K loop
+        int32_t slot_of[2][2] = {{0, 0}, {0, 0}};
+        if (!FC1) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = nt * 8 + 2 * c + q;
+                    if (n < ne) slot_of[nt][q] = __ldg(a.perm + off + n);
+                }
+        }
         const int64_t rg = int64_t(rb) * kDecRows + r_g;   // row within the expert
         const int64_t rg8 = rg + 8;
         float scol_g = 1.f, scol_g8 = 1.f;
@@ -488,7 +540,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                                                 c0, c1, tail_nsp, ne, g, lane, scol_g, scol_g8, acc);
         if (!ok) return;
 
-        // ---- K-half 1 hands its partial sums to K-half 0 through shared memory ----
+        // ---- with K parts, part 1 hands its partial sums to part 0 through shared memory ----
+        if (kDecKParts > 1) {
         const int rb_buf = int(un & 1u);
         const uint32_t rph = (un >> 1) & 1u;
         float* slot = red + ((rb_buf * kDecRowGroups + rgi) * 32 + lane) * 8;
@@ -515,6 +568,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             for (int q = 0; q < 4; ++q) acc[nt][q] += slot[nt * 4 + q];
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&red_empty[rb_buf]);
+        }
 
         // -------------------------------- epilogue --------------------------------
         if (FC1) {
@@ -573,8 +627,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                 for (int q = 0; q < 2; ++q) {
                     const int n = nt * 8 + 2 * c + q;
                     if (n >= ne) continue;
-                    const int64_t slot_id = a.perm[off + n];
-                    float* dst = a.slot_out + (int64_t(ks) * a.slots + slot_id) * a.N;
+                    float* dst = a.slot_out + (int64_t(ks) * a.slots + slot_of[nt][q]) * a.N;
                     if (rg < a.N) dst[rg] = acc[nt][q];
                     if (rg8 < a.N) dst[rg8] = acc[nt][2 + q];
                 }
@@ -612,15 +665,28 @@ bool decode_shape_ok(const Problem& p) {
 }
 
 int decode_fc2_splits(const Problem& p) {
+    // Split K so that the units (touched expert x 128-row block x K split) spread
+    // evenly over the SMs: minimise the chunks of the most loaded SM, counting
+    // half a chunk of fixed cost per unit (hand-off of the K halves, epilogue).
+    // The touched-expert count is bounded by min(E, T * k) here (routing has not
+    // run yet); the kernel iterates over the experts actually touched.
     const int64_t KC = int64_t(kChunkBytes) * p.pack;
     const int64_t nkc = (p.I + KC - 1) / KC;
     const int64_t n_rb = (p.H + kDecRows - 1) / kDecRows;
     const int64_t experts = std::min<int64_t>(p.E, p.T * p.k);
-    const int64_t want = int64_t(kTargetUnitsPerSm) * 152;
-    int64_t splits = (want + experts * n_rb - 1) / (experts * n_rb);
-    splits = std::max<int64_t>(1, std::min<int64_t>(splits, nkc));
-    const int64_t cps = (nkc + splits - 1) / splits;
-    return int((nkc + cps - 1) / cps);
+    const int64_t sms = device_sm_count();
+    int64_t best = 1;
+    double best_cost = 0.0;
+    for (int64_t cps = nkc; cps >= 1; --cps) {
+        const int64_t splits = (nkc + cps - 1) / cps;
+        const int64_t units = experts * n_rb * splits;
+        const double cost = double((units + sms - 1) / sms) * (double(cps) + 0.5);
+        if (best_cost == 0.0 || cost < best_cost) {
+            best_cost = cost;
+            best = splits;
+        }
+    }
+    return int(best);
 }
 
 cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
