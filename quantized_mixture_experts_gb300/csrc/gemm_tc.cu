@@ -53,6 +53,7 @@ constexpr uint32_t kTmemCols = kPair * kAccCols;
 constexpr uint32_t kBBytes = kTcMaxN * 128;   // token tile, fp16, swizzled
 constexpr uint32_t kABytes = kTcM * 128;      // one dequantised weight tile, fp16, swizzled
 constexpr uint32_t kAStageBytes = kPair * kABytes;
+// per epilogue warp: 32 tokens x 16 (SwiGLU) or 32 (ReLU) fp16 outputs
 constexpr unsigned kFull = 0xffffffffu;
 // Bound on the waits that drain a CTA's own copies / MMAs before it exits after
 // a timeout: independent of the (possibly tiny) configured wait limit.
@@ -81,6 +82,8 @@ struct TcArgs {
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t off_s, off_b, load_bytes, nload;
+    uint32_t off_epi;           // epilogue staging tiles (one per epilogue warp, FC1)
+    uint32_t epi_stage;         // bytes of one staging tile
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -211,9 +214,9 @@ __device__ __forceinline__ void deq8(uint32_t w, __half2 s, uint32_t* out) {
 
 // Position of column j in a row stored with groups of eight in the order
 // 0,4,1,5,2,6,3,7 (the 4-bit operand order).
-__device__ __forceinline__ int64_t perm8(int64_t j) {
-    const int q = int(j & 7);
-    return (j & ~int64_t(7)) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
+__device__ __forceinline__ int perm8(int j) {
+    const int q = j & 7;
+    return (j & ~7) + (q < 4 ? 2 * q : 2 * (q - 4) + 1);
 }
 
 template <int BITS, bool FC1, bool SCOL>
@@ -484,6 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         const int tile = ew / 4;                   // weight tile of the item
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row in the weight tile
+        __half* stile = reinterpret_cast<__half*>(smem + a.off_epi + uint32_t(ew) * a.epi_stage);
+        bool bad = false;                          // an FC1 output outside the fp16 range
         uint32_t item_it = 0;
         for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
@@ -512,35 +517,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     for (int q = 0; q < 32; ++q) v[q] *= srow;
                 }
                 if (FC1) {
+                    // The warp's outputs for these 32 tokens (16 SwiGLU or 32 ReLU
+                    // activation columns, already in the stored column order) go
+                    // through a shared-memory tile so that each token row leaves as
+                    // contiguous 16-byte stores.
+                    const int ncol = a.act == QMOE_ACT_SWIGLU ? 16 : 32;   // columns per warp
                     if (a.act == QMOE_ACT_SWIGLU) {
                         // even lane: gate row, tokens c0..c0+15; odd lane: tokens c0+16..c0+31
                         const bool even = (lane & 1) == 0;
-                        const int64_t j = BITS == 4 ? perm8(row >> 1) : (row >> 1);
+                        const int jl = lane >> 1;                       // column within the warp
+                        const int pos = BITS == 4 ? perm8(jl) : jl;
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
                             const float send = even ? v[16 + q] : v[q];
                             const float recv = __shfl_xor_sync(kFull, send, 1);
                             const float gate = even ? v[q] : recv;
                             const float lin = even ? recv : v[16 + q];
-                            const int col = c0 + (even ? q : 16 + q);
-                            if (col < w.rows && row < a.N) {
-                                const float o = swiglu(gate, lin, a.alpha, a.beta, a.has_limit, a.limit);
-                                if (!(fabsf(o) <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + j] = __float2half_rn(o);
-                            }
+                            const float o = swiglu(gate, lin, a.alpha, a.beta, a.has_limit, a.limit);
+                            // only stored outputs count (columns past the tile's rows are stale)
+                            bad |= (c0 + (even ? q : 16 + q) < w.rows) && !(fabsf(o) <= 65504.f);
+                            stile[(even ? q : 16 + q) * 16 + pos] = __float2half_rn(o);
                         }
                     } else {
+                        const int pos = BITS == 4 ? perm8(lane) : lane;
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
-                            const int col = c0 + q;
-                            if (col < w.rows && row < a.N) {
-                                const float o = fmaxf(v[q], 0.f);
-                                if (!(o <= 65504.f)) record_error(a.err, QMOE_DEVERR_NONFINITE);
-                                a.act_out[int64_t(w.row0 + col) * a.act_pitch + (BITS == 4 ? perm8(row) : row)] =
-                                    __float2half_rn(o);
-                            }
+                            const float o = fmaxf(v[q], 0.f);
+                            bad |= (c0 + q < w.rows) && !(o <= 65504.f);
+                            stile[q * 32 + pos] = __float2half_rn(o);
                         }
                     }
+                    __syncwarp();
+                    // lane = token of the chunk; its ncol outputs are 2 or 4 16-byte pieces
+                    const int64_t jbase = (int64_t(w.m + tile) * kTcM + quad * 32) / (ncol == 16 ? 2 : 1);
+                    // rows past N (a partial last weight tile) produce no outputs
+                    if (c0 + lane < w.rows && jbase < a.N / (ncol == 16 ? 2 : 1)) {
+                        const uint4* src = reinterpret_cast<const uint4*>(stile + lane * ncol);
+                        uint4* dst = reinterpret_cast<uint4*>(a.act_out + int64_t(w.row0 + c0 + lane) * a.act_pitch + jbase);
+                        for (int h = 0; h < ncol / 8; ++h) dst[h] = src[h];
+                    }
+                    __syncwarp();
                 } else {
                     const int my_col = c0 + lane;
                     const int my_slot = my_col < w.rows ? a.perm[w.row0 + my_col] : 0;
@@ -556,6 +572,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
         }
+        if (__any_sync(kFull, bad) && lane == 0) record_error(a.err, QMOE_DEVERR_NONFINITE);
     }
 
     tc_fence_before();
@@ -672,14 +689,16 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.wait_ns = wait_limit_ns();
     a.drop_it = drop_stage();
     const uint32_t raw_bytes = uint32_t(kItemRows * (kTcK / pack));
-    a.off_s = raw_bytes;                          // 256 rows x 4 scales
-    a.off_b = (raw_bytes + kItemRows * 16u + 1023u) & ~1023u;
+    a.off_s = raw_bytes;                          // 256 rows x 4 scales (TMA-staged scales only)
+    a.off_b = (raw_bytes + (a.scale_tma ? kItemRows * 16u : 0u) + 1023u) & ~1023u;
+    a.epi_stage = fc1 ? 32u * (p.act == QMOE_ACT_SWIGLU ? 16u : 32u) * 2u : 0u;
     a.load_bytes = a.off_b + kBBytes;
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
-    a.nload = uint32_t(std::min<size_t>(kLoadStages, (smem_cap - 1024 - size_t(kAStages) * kAStageBytes) /
-                                                         a.load_bytes));
+    const size_t fixed = size_t(kAStages) * kAStageBytes + size_t(kEpiWarps) * a.epi_stage;
+    a.nload = uint32_t(std::min<size_t>(kLoadStages, (smem_cap - 1024 - fixed) / a.load_bytes));
     if (a.nload < 2) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + size_t(a.nload) * a.load_bytes + size_t(kAStages) * kAStageBytes;
+    a.off_epi = a.nload * a.load_bytes + uint32_t(kAStages) * kAStageBytes;
+    const size_t smem = 1024 + size_t(a.nload) * a.load_bytes + fixed;
     const int64_t items_max = pl.max_tiles * a.split_n * a.n_pairs;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
     const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
