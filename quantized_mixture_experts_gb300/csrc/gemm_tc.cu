@@ -15,9 +15,11 @@
 //
 // Per CTA (one per SM, persistent), warp-specialised:
 //   warp 0      TMA producer: the weight tile's packed bytes for a 64-wide K
-//               block and its block scales (2-D boxes) and the tile's token
-//               rows (16-row boxes of the expert-sorted fp16 activations,
-//               128-byte swizzle) into a 3-stage ring;
+//               block and its block scales (2-D boxes; scales only when a new
+//               group of four blocks starts) and the tile's token rows into a
+//               3-stage ring.  The token rows are stored K-blocked with the
+//               128-byte swizzle already applied, so one 1-D bulk copy of up to
+//               32 KB lands the whole swizzled tile;
 //   warp 1      TMEM allocator and MMA issuer (one lane): 4 x tcgen05.mma
 //               (K = 16) per stage into one of two 256-column accumulators;
 //   warps 2-9   dequantisers: packed codes -> (q - mid) * scale in fp16,
@@ -61,25 +63,25 @@ constexpr uint64_t kDrainWaitNs = 200000000ull;
 
 struct TcArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 256}
-    CUtensorMap tm_b;           // expert-sorted fp16 token rows [slots, Kp], box {64, 16},
-                                // 128-byte swizzle
     CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 256}
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, 0)
     const int32_t* perm;        // sorted position -> slot
+    const __half* bsrc;         // token rows, K-blocked [K/64][srows][64], pre-swizzled
+    int64_t srows;
     int64_t N, K;
     int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
     int topk, n_pairs, gm;
     int split_n;                // 2: items take half a token tile (N <= 128), double-buffered
                                 // accumulators; 1: whole tile (N <= 256), single buffer
-    __half* act_out;
-    int64_t act_pitch;
+    __half* act_out;            // FC1 output, K-blocked like bsrc
     int act, has_limit;
     float alpha, beta, limit;
     float* slot_out;
     int32_t* err;
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
+    int scale_every;            // stages per TMA-staged group of four scale blocks
     int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t off_s, off_b, load_bytes, nload;
     uint32_t off_epi;           // epilogue staging tiles (one per epilogue warp, FC1)
@@ -276,7 +278,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             ptx::prefetch_tmap(&a.tm_w);
-            ptx::prefetch_tmap(&a.tm_b);
             if (a.scale_tma) ptx::prefetch_tmap(&a.tm_s);
         }
         uint32_t it = 0;
@@ -295,19 +296,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 if (int64_t(it) == a.drop_it) continue;   // test hook: this stage never fills
                 uint8_t* sp = smem + size_t(sl) * a.load_bytes;
                 if (lane == 0) {
+                    // a staged group of four scale blocks covers scale_every stages
+                    const bool scales = a.scale_tma && kb % a.scale_every == 0;
                     ptx::mbar_arrive_expect_tx(&load_full[sl], kItemRows * kRawRow +
-                                               (a.scale_tma ? kItemRows * 16u : 0u) +
+                                               (scales ? kItemRows * 16u : 0u) +
                                                uint32_t(w.nt) * 128u);
                     ptx::tma_load_2d(sp, &a.tm_w, kb * int(kRawRow), wrow0, &load_full[sl]);
-                    if (a.scale_tma)
+                    if (scales)
                         ptx::tma_load_2d(sp + a.off_s, &a.tm_s, ((kb * kTcK) >> a.lbs) & ~3,
                                          wrow0, &load_full[sl]);
+                    // the token tile of this K block: nt contiguous 128-byte rows
+                    ptx::bulk_g2s(sp + a.off_b, a.bsrc + (int64_t(kb) * a.srows + w.row0) * kTcK,
+                                  uint32_t(w.nt) * 128u, &load_full[sl]);
                 }
                 __syncwarp();
-                // expert-sorted token rows are contiguous: one 16-row box per lane
-                if (lane < w.nt / 16)
-                    ptx::tma_load_2d(sp + a.off_b + lane * 2048, &a.tm_b, kb * kTcK,
-                                     w.row0 + lane * 16, &load_full[sl]);
             }
         }
         if (!ok && lane == 0) {
@@ -390,6 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             const int64_t row = int64_t(w.m) * kTcM + r;   // weight row within the expert
             const bool valid = row < a.N;
             const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);   // staged group of four scale blocks
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int sl = int(it % a.nload);
                 const int sa = int(it % kAStages);
@@ -407,9 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 if (!SCOL) {
                     // the four staged blocks start at ((kb * 64) >> lbs) & ~3; rows whose scale
                     // row is not 16-byte aligned (nb % 4 != 0) read them from global memory
-                    float4 s4;
                     if (a.scale_tma) {
-                        s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
+                        if (kb % a.scale_every == 0) s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(r) * 16u);
                     } else {
                         const int g0 = ((kb * kTcK) >> a.lbs) & ~3;
                         s4.x = valid && g0 < a.nb ? __ldg(srow + g0) : 0.f;
@@ -548,13 +550,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         }
                     }
                     __syncwarp();
-                    // lane = token of the chunk; its ncol outputs are 2 or 4 16-byte pieces
+                    // lane = token of the chunk; its ncol outputs are 2 or 4 16-byte chunks
+                    // of one 64-column K block of the K-blocked FC2 input, stored at
+                    // chunk ^ (token & 7): the 128-byte swizzle of the token's row in a
+                    // tile (tiles start on multiples of 8 rows of their expert)
                     const int64_t jbase = (int64_t(w.m + tile) * kTcM + quad * 32) / (ncol == 16 ? 2 : 1);
                     // rows past N (a partial last weight tile) produce no outputs
-                    if (c0 + lane < w.rows && jbase < a.N / (ncol == 16 ? 2 : 1)) {
+                    const int col = c0 + lane;
+                    if (col < w.rows && jbase < a.N / (ncol == 16 ? 2 : 1)) {
                         const uint4* src = reinterpret_cast<const uint4*>(stile + lane * ncol);
-                        uint4* dst = reinterpret_cast<uint4*>(a.act_out + int64_t(w.row0 + c0 + lane) * a.act_pitch + jbase);
-                        for (int h = 0; h < ncol / 8; ++h) dst[h] = src[h];
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            a.act_out + ((jbase / kTcK) * a.srows + w.row0 + col) * kTcK);
+                        const int ch0 = int(jbase % kTcK) / 8;
+                        for (int h = 0; h < ncol / 8; ++h) dst[(ch0 + h) ^ (col & 7)] = src[h];
                     }
                     __syncwarp();
                 } else {
@@ -584,17 +592,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                      : "memory");
 }
 
-// xs16[pos] = x16[perm[pos] / k]: the fp16 activations in expert-sorted slot
-// order, so every token tile is a contiguous block of rows.
+// The fp16 activations in expert-sorted slot order (row pos = token
+// perm[pos] / k), K-blocked [H/64][srows][64] with the 128-byte swizzle of the
+// row's position in its token tile applied: 16-byte chunk c of a 64-column
+// block is stored at c ^ ((pos - offsets[expert]) & 7).  Token tiles start at
+// multiples of their expert's first row plus multiples of 8, so a tile's rows
+// of one K block are one contiguous, already swizzled 128-byte-row block.
 __global__ void sort_rows_kernel(const uint4* __restrict__ x16, int64_t row_vec,
-                                 const int32_t* __restrict__ perm, int k, int64_t slots,
-                                 uint4* __restrict__ xs16) {
+                                 const int32_t* __restrict__ perm, const int32_t* __restrict__ sel,
+                                 const int32_t* __restrict__ offsets, int k, int64_t slots,
+                                 int64_t srows, uint4* __restrict__ xs16) {
     const int64_t total = slots * row_vec;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t pos = i / row_vec, q = i % row_vec;
-        const int64_t t = perm[pos] / k;
-        xs16[i] = x16[t * row_vec + q];
+        const int32_t slot = perm[pos];
+        const int phase = int(pos - offsets[sel[slot]]) & 7;
+        const int64_t t = slot / k;
+        xs16[((q >> 3) * srows + pos) * 8 + ((q & 7) ^ phase)] = x16[t * row_vec + q];
     }
 }
 
@@ -629,8 +644,8 @@ cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cu
     const int blocks = int(std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 16));
     note_launch(QMOE_KERNEL_GROUP, s, true);
     sort_rows_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(w.x16), row_vec, w.perm, int(p.k), pl.slots,
-        reinterpret_cast<uint4*>(w.xs16));
+        reinterpret_cast<const uint4*>(w.x16), row_vec, w.perm, w.sel, w.offsets, int(p.k),
+        pl.slots, pl.srows, reinterpret_cast<uint4*>(w.xs16));
     note_launch(QMOE_KERNEL_GROUP, s, false);
     return cudaGetLastError();
 }
@@ -655,14 +670,11 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
                         uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kTcK / pack), kItemRows,
                         CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    const __half* bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
-    const int64_t brows = pl.slots;
-    const int64_t bpitch = fc1 ? pl.Hp : pl.Ip;
-    if (!encode_tmap_2d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bsrc, uint64_t(bpitch),
-                        uint64_t(brows), uint64_t(bpitch) * 2, kTcK, 16,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    a.bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
+    a.srows = pl.srows;
     a.scale_tma = (p.bs != 0 && a.nb % 4 == 0) ? 1 : 0;
+    // four staged scale blocks of bs columns cover 4 * bs / 64 stages (bs >= 16)
+    a.scale_every = p.bs >= 16 ? int(4 * p.bs / kTcK) : 1;
     if (a.scale_tma &&
         !encode_tmap_2d(&a.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, uint64_t(a.nb),
                         uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kItemRows,
@@ -678,7 +690,6 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     // next item's MMAs (FC1 keeps whole tiles: halves would double the dequantisation)
     a.split_n = 1;
     a.act_out = static_cast<__half*>(w.act);
-    a.act_pitch = pl.Ip;
     a.act = p.act;
     a.has_limit = p.has_limit;
     a.alpha = p.alpha;

@@ -170,6 +170,9 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.tile_tokens = p.path == QMOE_PATH_GROUPED ? grouped_tile_tokens() : 0;
     q.max_tiles = q.tile_tokens ? (q.slots + q.tile_tokens - 1) / q.tile_tokens + p.E : 0;
     q.fc2_splits = p.path == QMOE_PATH_DECODE ? decode_fc2_splits(p) : 1;
+    // grouped path: a token tile may read up to 15 rows past the last slot (its MMA
+    // width is rounded up to 16), so the K-blocked layouts carry 16 spare rows
+    q.srows = p.path == QMOE_PATH_GROUPED ? round_up(q.slots, 16) + 16 : 0;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -191,8 +194,10 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.off_active = take(4 * E);
     const bool generic = p.path == QMOE_PATH_GENERIC;
     q.off_x16 = take(generic ? 0 : 2 * size_t(p.T) * size_t(q.Hp));
-    q.off_xs16 = take(p.path == QMOE_PATH_GROUPED ? 2 * slots * size_t(q.Hp) : 0);
-    q.off_act = take(generic ? 4 * slots * size_t(p.I) : 2 * slots * size_t(q.Ip));
+    const bool grouped = p.path == QMOE_PATH_GROUPED;
+    q.off_xs16 = take(grouped ? 2 * size_t(q.srows) * size_t(q.Hp) : 0);
+    q.off_act = take(generic ? 4 * slots * size_t(p.I)
+                             : 2 * (grouped ? size_t(q.srows) : slots) * size_t(q.Ip));
     q.off_slot_out = take(4 * size_t(q.fc2_splits) * slots * size_t(p.H));
     q.bytes = off;
     *pl = q;

@@ -47,6 +47,7 @@ struct Plan {
     int64_t max_tiles = 0;      // expert token-tiles upper bound
     int tile_tokens = 0;        // tokens per expert tile (grouped path)
     int fc2_splits = 1;         // split-K factor of the decode FC2
+    int64_t srows = 0;          // grouped path: rows of the K-blocked activation layouts
     size_t bytes = 0;           // total workspace bytes
     // byte offsets into the workspace
     size_t off_ctrl, off_sel, off_pw, off_counts, off_offsets, off_hist, off_rank, off_perm,
@@ -67,8 +68,10 @@ struct Work {
     int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, 0)
     int32_t* active;      // [E] experts with at least one slot, ascending
     __half* x16;          // [T*Hp] fp16 copy of the activations
-    __half* xs16;         // [T*k*Hp] fp16 activations in expert-sorted slot order (grouped path)
-    void* act;            // [T*k*Ip] FC1 output (fp16; fp32 on the generic path)
+    __half* xs16;         // grouped path: fp16 activations in expert-sorted slot order,
+                          // K-blocked [Hp/64][srows][64] with the 128-byte swizzle applied
+    void* act;            // FC1 output: fp16 [T*k, Ip] (decode), fp32 (generic), or fp16
+                          // K-blocked [Ip/64][srows][64] like xs16 (grouped)
     float* slot_out;      // [fc2_splits*T*k*H] per-slot FC2 output
 };
 
