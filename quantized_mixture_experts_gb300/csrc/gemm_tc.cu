@@ -25,8 +25,10 @@
 //   warps 2-9   dequantisers: packed codes -> (q - mid) * scale in fp16,
 //               written to shared memory in the 128-byte-swizzled K-major
 //               layout the MMA descriptor expects;
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator, FC1 ReLU / SwiGLU to
-//               fp16 activations, FC2 fp32 rows per routing slot.
+//   warps 10-17 epilogue: tcgen05.ld of the accumulator, FC1 ReLU / SwiGLU to
+//               fp16 activations, FC2 rows per routing slot already multiplied
+//               by the slot's routing weight (fp16; the combine adds a token's k
+//               rows in fixed order).
 // Every wait is a bounded mbarrier wait; on expiry the CTA records
 // QMOE_DEVERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns.
 #include <algorithm>
@@ -55,7 +57,6 @@ constexpr uint32_t kTmemCols = kPair * kAccCols;
 constexpr uint32_t kBBytes = kTcMaxN * 128;   // token tile, fp16, swizzled
 constexpr uint32_t kABytes = kTcM * 128;      // one dequantised weight tile, fp16, swizzled
 constexpr uint32_t kAStageBytes = kPair * kABytes;
-// per epilogue warp: 32 tokens x 16 (SwiGLU) or 32 (ReLU) fp16 outputs
 constexpr unsigned kFull = 0xffffffffu;
 // Bound on the waits that drain a CTA's own copies / MMAs before it exits after
 // a timeout: independent of the (possibly tiny) configured wait limit.
@@ -67,6 +68,7 @@ struct TcArgs {
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, 0)
     const int32_t* perm;        // sorted position -> slot
+    const float* pw;            // routing weight of each slot
     const __half* bsrc;         // token rows, K-blocked [K/64][srows][64], pre-swizzled
     int64_t srows;
     int64_t N, K;
@@ -77,7 +79,7 @@ struct TcArgs {
     __half* act_out;            // FC1 output, K-blocked like bsrc
     int act, has_limit;
     float alpha, beta, limit;
-    float* slot_out;
+    __half* slot16;             // FC2 output: [slots, N] fp16, weighted by the slot's routing weight
     int32_t* err;
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row in the weight tile
         __half* stile = reinterpret_cast<__half*>(smem + a.off_epi + uint32_t(ew) * a.epi_stage);
-        bool bad = false;                          // an FC1 output outside the fp16 range
+        bool bad = false;                          // an output outside the fp16 range
         uint32_t item_it = 0;
         for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
@@ -566,14 +568,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     }
                     __syncwarp();
                 } else {
-                    const int my_col = c0 + lane;
-                    const int my_slot = my_col < w.rows ? a.perm[w.row0 + my_col] : 0;
+                    // FC2: lane = token c0 + lane, with its slot and routing weight.  The
+                    // warp's 32 output rows of each token are staged in shared memory and
+                    // leave as one 64-byte piece of the slot's row.
+                    const int col = c0 + lane;
+                    const bool valid_col = col < w.rows;
+                    const int my_slot = valid_col ? __ldg(a.perm + w.row0 + col) : 0;
+                    const float my_p = valid_col ? __ldg(a.pw + my_slot) : 0.f;
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
-                        const int col = c0 + q;
-                        const int64_t slot = __shfl_sync(kFull, my_slot, q);
-                        if (col < w.rows && row < a.N) a.slot_out[slot * a.N + row] = v[q];
+                        const float o = v[q] * __shfl_sync(kFull, my_p, q);
+                        bad |= (c0 + q < w.rows) && !(fabsf(o) <= 65504.f);
+                        stile[q * 32 + lane] = __float2half_rn(o);
                     }
+                    __syncwarp();
+                    const int64_t hbase = int64_t(w.m + tile) * kTcM + quad * 32;
+                    if (valid_col && hbase < a.N) {
+                        const uint4* src = reinterpret_cast<const uint4*>(stile + lane * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(a.slot16 + int64_t(my_slot) * a.N + hbase);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) dst[h] = src[h];
+                    }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -695,14 +711,16 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.alpha = p.alpha;
     a.beta = p.beta;
     a.limit = p.limit;
-    a.slot_out = w.slot_out;
+    a.slot16 = reinterpret_cast<__half*>(w.slot_out);
+    a.pw = w.pw;
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
     a.drop_it = drop_stage();
     const uint32_t raw_bytes = uint32_t(kItemRows * (kTcK / pack));
     a.off_s = raw_bytes;                          // 256 rows x 4 scales (TMA-staged scales only)
     a.off_b = (raw_bytes + (a.scale_tma ? kItemRows * 16u : 0u) + 1023u) & ~1023u;
-    a.epi_stage = fc1 ? 32u * (p.act == QMOE_ACT_SWIGLU ? 16u : 32u) * 2u : 0u;
+    // per epilogue warp: 32 tokens x 16 (SwiGLU) or 32 (ReLU, FC2) fp16 outputs
+    a.epi_stage = 32u * (fc1 && p.act == QMOE_ACT_SWIGLU ? 16u : 32u) * 2u;
     a.load_bytes = a.off_b + kBBytes;
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
     const size_t fixed = size_t(kAStages) * kAStageBytes + size_t(kEpiWarps) * a.epi_stage;

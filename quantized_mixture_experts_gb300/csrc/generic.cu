@@ -189,6 +189,56 @@ cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, 
     return cudaGetLastError();
 }
 
+// y[t] = sum over i < k of s16[t * k + i]: the grouped path's FC2 rows, already
+// weighted by their routing weight, added in fp32 in ascending slot order.
+// One thread per 8 output columns (H % 8 == 0 on the grouped path).
+__global__ void combine16_kernel(const uint4* __restrict__ s16, float* __restrict__ y, int64_t T,
+                                 int64_t H, int k, int aligned) {
+    const int64_t H8 = H / 8;
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= T * H8) return;
+    const int64_t t = idx / H8, d8 = idx % H8;
+    const uint4* base = s16 + t * k * H8 + d8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i0 = 0; i0 < k; i0 += 8) {
+        // issue up to eight slots' loads first; the sum keeps ascending slot order
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (i0 + j < k) v[j] = __ldg(base + int64_t(i0 + j) * H8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (i0 + j < k) {
+                const __half2* h = reinterpret_cast<const __half2*>(&v[j]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __half22float2(h[q]);
+                    acc[2 * q] += f.x;
+                    acc[2 * q + 1] += f.y;
+                }
+            }
+    }
+    float* out = y + t * H + 8 * d8;
+    if (aligned) {
+        reinterpret_cast<float4*>(out)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        reinterpret_cast<float4*>(out)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) out[q] = acc[q];
+    }
+}
+
+cudaError_t launch_combine16(const Problem& p, const Work& w, cudaStream_t s) {
+    const int64_t n = p.T * (p.H / 8);
+    note_launch(QMOE_KERNEL_COMBINE, s, true);
+    const int threads = n < 152 * 256 ? 64 : 256;
+    combine16_kernel<<<blocks_for(n, threads), threads, 0, s>>>(
+        reinterpret_cast<const uint4*>(w.slot_out), p.y, p.T, p.H, int(p.k),
+        (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 ? 1 : 0);
+    note_launch(QMOE_KERNEL_COMBINE, s, false);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,
                            cudaStream_t s) {
     const int vec = (p.H & 3) == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 &&

@@ -296,7 +296,7 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
-            if ((e = launch_combine(p, pl, w, 1, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_combine16(p, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             return QMOE_OK;
         }
         default:

@@ -72,7 +72,8 @@ struct Work {
                           // K-blocked [Hp/64][srows][64] with the 128-byte swizzle applied
     void* act;            // FC1 output: fp16 [T*k, Ip] (decode), fp32 (generic), or fp16
                           // K-blocked [Ip/64][srows][64] like xs16 (grouped)
-    float* slot_out;      // [fc2_splits*T*k*H] per-slot FC2 output
+    float* slot_out;      // [fc2_splits*T*k*H] per-slot FC2 output (fp32; the grouped path
+                          // keeps [T*k*H] fp16 rows weighted by routing weight here)
 };
 
 constexpr int kRouteTokensPerChunk = 64;
@@ -104,6 +105,8 @@ cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Wor
                                      int x16_mode, cudaStream_t s);
 cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+// Grouped path: the FC2 rows are fp16 [T*k, H] and already weighted by routing weight.
+cudaError_t launch_combine16(const Problem& p, const Work& w, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,
                            cudaStream_t s);
 // Decode path (few tokens): weight-streaming tensor-core GEMV.
