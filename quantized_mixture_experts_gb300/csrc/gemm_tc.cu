@@ -500,6 +500,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             const int buf = a.split_n == 2 ? int(item_it & 1u) : 0;
             const uint32_t aph = (a.split_n == 2 ? (item_it >> 1) : item_it) & 1u;
             ++item_it;
+            // FC2: each lane's token of every 32-token chunk, its slot and routing
+            // weight, loaded before the accumulator is ready (the loads are a
+            // dependent chain and would otherwise stall every chunk)
+            int slot_c[kTcMaxN / 32];
+            float p_c[kTcMaxN / 32];
+            if (!FC1) {
+#pragma unroll
+                for (int ch = 0; ch < kTcMaxN / 32; ++ch) {
+                    const int col = ch * 32 + lane;
+                    slot_c[ch] = col < w.rows ? __ldg(a.perm + w.row0 + col) : 0;
+                }
+#pragma unroll
+                for (int ch = 0; ch < kTcMaxN / 32; ++ch)
+                    p_c[ch] = ch * 32 + lane < w.rows ? __ldg(a.pw + slot_c[ch]) : 0.f;
+            }
             if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -573,8 +588,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                     // leave as one 64-byte piece of the slot's row.
                     const int col = c0 + lane;
                     const bool valid_col = col < w.rows;
-                    const int my_slot = valid_col ? __ldg(a.perm + w.row0 + col) : 0;
-                    const float my_p = valid_col ? __ldg(a.pw + my_slot) : 0.f;
+                    int my_slot = 0;
+                    float my_p = 0.f;
+#pragma unroll
+                    for (int ch = 0; ch < kTcMaxN / 32; ++ch)   // registers: select, not index
+                        if (ch * 32 == c0) { my_slot = slot_c[ch]; my_p = p_c[ch]; }
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const float o = v[q] * __shfl_sync(kFull, my_p, q);
@@ -614,18 +632,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
 // block is stored at c ^ ((pos - offsets[expert]) & 7).  Token tiles start at
 // multiples of their expert's first row plus multiples of 8, so a tile's rows
 // of one K block are one contiguous, already swizzled 128-byte-row block.
-__global__ void sort_rows_kernel(const uint4* __restrict__ x16, int64_t row_vec,
+__global__ void sort_rows_kernel(const uint4* __restrict__ x16, int row_vec,
                                  const int32_t* __restrict__ perm, const int32_t* __restrict__ sel,
                                  const int32_t* __restrict__ offsets, int k, int64_t slots,
                                  int64_t srows, uint4* __restrict__ xs16) {
-    const int64_t total = slots * row_vec;
-    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t pos = i / row_vec, q = i % row_vec;
-        const int32_t slot = perm[pos];
-        const int phase = int(pos - offsets[sel[slot]]) & 7;
-        const int64_t t = slot / k;
-        xs16[((q >> 3) * srows + pos) * 8 + ((q & 7) ^ phase)] = x16[t * row_vec + q];
+    // one warp per sorted row, lanes over the row's 16-byte chunks
+    const int lane = threadIdx.x & 31;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t nwarps = int64_t(gridDim.x) * wpb;
+    for (int64_t pos = int64_t(blockIdx.x) * wpb + (threadIdx.x >> 5); pos < slots; pos += nwarps) {
+        const int32_t slot = __ldg(perm + pos);
+        const int phase = int(pos - __ldg(offsets + __ldg(sel + slot))) & 7;
+        const uint4* __restrict__ src = x16 + int64_t(slot / k) * row_vec;
+        for (int q = lane; q < row_vec; q += 32)
+            xs16[(int64_t(q >> 3) * srows + pos) * 8 + ((q & 7) ^ phase)] = __ldg(src + q);
     }
 }
 
@@ -655,9 +675,9 @@ int pick_group(int n_mtiles) {
 int grouped_tile_tokens() { return kTcMaxN; }
 
 cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
-    const int64_t row_vec = pl.Hp / 8;
-    const int64_t total = pl.slots * row_vec;
-    const int blocks = int(std::min<int64_t>((total + 255) / 256, int64_t(device_sm_count()) * 16));
+    const int row_vec = int(pl.Hp / 8);
+    const int64_t warps = std::max<int64_t>(1, pl.slots);
+    const int blocks = int(std::min<int64_t>((warps + 7) / 8, int64_t(device_sm_count()) * 8));
     note_launch(QMOE_KERNEL_GROUP, s, true);
     sort_rows_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(w.x16), row_vec, w.perm, w.sel, w.offsets, int(p.k),

@@ -70,8 +70,8 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
     for (int i = lane; i < k; i += 32) pw[i] = expf(pw[i] - vmax) / part;
 }
 
-// fp16 copy of rows [t0, t0+ntok) of the activations, columns [g_lo, g_hi)
-// in groups of eight, zero padded to Hp.  Layout mode:
+// One group of eight activations of row t (columns 8g..8g+7), converted to fp16
+// in layout mode:
 //   0  natural order;
 //   1  each group of eight stored in the order 0,4,1,5,2,6,3,7 (the pair order
 //      of the 4-bit conversion);
@@ -79,51 +79,65 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
 //      elements divided by 16 (exact): the 4-bit decode kernel pairs
 //      (0,4),(2,6) with low nibbles and (1,5),(3,7) with high nibbles, which
 //      it feeds with 16x the code.
-// Threads stride over the (row, group) pairs.
+// Columns past H are zero.
+__device__ __forceinline__ void convert_group(const float* __restrict__ x, int64_t t, int64_t g,
+                                              int64_t H, bool vec, __half* __restrict__ x16,
+                                              int64_t Hp, int mode) {
+    const float* __restrict__ xr = x + t * H;
+    float v[8];
+    if (vec) {
+        if (g * 8 < H) {
+            const float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
+            const float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = (g * 8 + q < H) ? xr[g * 8 + q] : 0.f;
+    }
+    __half2 h[4];
+    if (mode == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+    } else if (mode == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int src = (q >> 1) + 2 * (q & 1);     // pairs (0,4),(2,6),(1,5),(3,7)
+            const float f = (src & 1) ? 0.0625f : 1.f;
+            h[q] = __floats2half2_rn(v[src] * f, v[src + 4] * f);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+    }
+    reinterpret_cast<uint4*>(x16 + t * Hp)[g] = *reinterpret_cast<uint4*>(h);
+}
+
+// fp16 copy of rows [t0, t0+ntok) of the activations, groups of eight columns
+// [g_lo, g_hi), zero padded to Hp (see convert_group for the layout modes).
+// Thread tid of nthr takes a fixed group and every rows-per-pass-th row, so the
+// index arithmetic is one 32-bit division per thread.
 __device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, int64_t H,
                              __half* __restrict__ x16, int64_t Hp, int mode, int64_t g_lo,
                              int64_t g_hi, int tid, int nthr) {
-    const int64_t width = g_hi - g_lo;
+    const int width = int(g_hi - g_lo);
     if (width <= 0) return;
-    const int64_t total = int64_t(ntok) * width;
     const bool vec = (H & 7) == 0 && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
-#pragma unroll 4
-    for (int64_t idx = tid; idx < total; idx += nthr) {
-        const int64_t t = t0 + idx / width;
-        const int64_t g = g_lo + idx % width;
-        const float* __restrict__ xr = x + t * H;
-        float v[8];
-        if (vec) {
-            if (g * 8 < H) {
-                const float4 a = reinterpret_cast<const float4*>(xr)[2 * g];
-                const float4 b = reinterpret_cast<const float4*>(xr)[2 * g + 1];
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = 0.f;
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = (g * 8 + q < H) ? xr[g * 8 + q] : 0.f;
-        }
-        __half2 h[4];
-        if (mode == 1) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
-        } else if (mode == 2) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int src = (q >> 1) + 2 * (q & 1);     // pairs (0,4),(2,6),(1,5),(3,7)
-                const float f = (src & 1) ? 0.0625f : 1.f;
-                h[q] = __floats2half2_rn(v[src] * f, v[src + 4] * f);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
-        }
-        reinterpret_cast<uint4*>(x16 + t * Hp)[g] = *reinterpret_cast<uint4*>(h);
+    if (width >= nthr) {
+        for (int r = 0; r < ntok; ++r)
+            for (int g = tid; g < width; g += nthr)
+                convert_group(x, t0 + r, g_lo + g, H, vec, x16, Hp, mode);
+        return;
     }
+    const int rpp = nthr / width;            // rows per pass
+    const int r0 = tid / width, g = tid - r0 * width;
+    if (r0 >= rpp) return;
+#pragma unroll 4
+    for (int r = r0; r < ntok; r += rpp) convert_group(x, t0 + r, g_lo + g, H, vec, x16, Hp, mode);
 }
 
 // Grid (chunks, conv_split).  CTA (c, 0) routes the chunk's tokens (one warp
@@ -196,9 +210,12 @@ __global__ void __launch_bounds__(1024) route_group_small_kernel(
             const int64_t per = (total + nconv - 1) / nconv;
             const int64_t lo = int64_t(blockIdx.x - 1) * per;
             const int64_t hi = lo + per < total ? lo + per : total;
-            // rows are whole groups; walk the flat (token, group) range
-            for (int64_t idx = lo + threadIdx.x; idx < hi; idx += blockDim.x)
-                convert_rows(x, idx / G8, 1, H, x16, Hp, x16_mode, idx % G8, idx % G8 + 1, 0, 1);
+            // walk the flat (token, group) range
+            const bool vec = (H & 7) == 0 && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+            for (int64_t idx = lo + threadIdx.x; idx < hi; idx += blockDim.x) {
+                const int64_t t = idx / G8;
+                convert_group(x, t, idx - t * G8, H, vec, x16, Hp, x16_mode);
+            }
         }
         return;
     }
