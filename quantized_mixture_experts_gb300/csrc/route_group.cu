@@ -26,8 +26,9 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 
 // One warp selects the k best logits of row `row` (length E) in selection
 // order and writes experts, logits (temporarily) and routing weights.
-__device__ void route_one_token(const float* __restrict__ row, int E, int k, int32_t* sel,
-                                float* pw, int32_t* s_exp, int lane) {
+// General form: any E and k; every selection round re-reads the row.
+__device__ void route_one_token_any(const float* __restrict__ row, int E, int k, int32_t* sel,
+                                    float* pw, int32_t* s_exp, int lane) {
     float prev_v = 0.f;
     int prev_i = -1;
     float vmax = 0.f;
@@ -68,6 +69,66 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
     __syncwarp();
     for (int i = lane; i < k; i += 32) pw[i] = expf(pw[i] - vmax) / part;
+}
+
+// Same selection for E <= 32 * kRouteRegs and k <= 32: the row is read once into
+// registers and round i's winner stays in lane i, so the rounds and the softmax
+// touch no memory.  The softmax sums in the same shuffle tree as the general form.
+constexpr int kRouteRegs = 8;
+__device__ void route_one_token(const float* __restrict__ row, int E, int k, int32_t* sel,
+                                float* pw, int32_t* s_exp, int lane) {
+    if (E > 32 * kRouteRegs || k > 32) {
+        route_one_token_any(row, E, k, sel, pw, s_exp, lane);
+        return;
+    }
+    float v[kRouteRegs];
+#pragma unroll
+    for (int j = 0; j < kRouteRegs; ++j) v[j] = lane + 32 * j < E ? row[lane + 32 * j] : 0.f;
+    float prev_v = 0.f;
+    int prev_i = -1;
+    float vmax = 0.f;
+    float mine_v = 0.f;   // lane i: the logit selected in round i
+    int mine_i = -1;
+    for (int i = 0; i < k; ++i) {
+        float best_v = 0.f;
+        int best_i = -1;
+#pragma unroll
+        for (int j = 0; j < kRouteRegs; ++j) {
+            const int e = lane + 32 * j;
+            const bool after_prev = (prev_i < 0) || better(prev_v, prev_i, v[j], e);
+            if (e < E && after_prev && (best_i < 0 || better(v[j], e, best_v, best_i))) {
+                best_v = v[j];
+                best_i = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(kFull, best_v, off);
+            int oi = __shfl_xor_sync(kFull, best_i, off);
+            if (oi >= 0 && (best_i < 0 || better(ov, oi, best_v, best_i))) {
+                best_v = ov;
+                best_i = oi;
+            }
+        }
+        prev_v = best_v;
+        prev_i = best_i;
+        if (i == 0) vmax = best_v;
+        if (lane == i) {
+            mine_v = best_v;
+            mine_i = best_i;
+        }
+    }
+    // softmax over the k selected logits, max subtracted first
+    float part = lane < k ? expf(mine_v - vmax) : 0.f;
+    const float mine_e = part;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    if (lane < k) {
+        sel[lane] = mine_i;
+        s_exp[lane] = mine_i;
+        pw[lane] = mine_e / part;
+    }
+    __syncwarp();
 }
 
 // One group of eight activations of row t (columns 8g..8g+7), converted to fp16
