@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
 
+    // the combine after FC2 may start its prologue on SMs this grid leaves
+    ptx::griddep_launch_dependents();
     const int ntiles = a.tiles[0];
     const int64_t items = int64_t(ntiles) * a.split_n * a.n_pairs;
     const int acc_cols = kAccCols / a.split_n;     // TMEM columns per weight tile and buffer

@@ -364,6 +364,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     __shared__ __align__(8) uint64_t red_full[2];    // K-half 1 -> K-half 0 partial sums
     __shared__ __align__(8) uint64_t red_empty[2];
     __shared__ int abort_flag;
+    // FC2: token-row copies held back until FC1 has completed (see the producer)
+    __shared__ const __half* held_src[kDecStages][32];
+    __shared__ uint32_t held_meta[kDecStages][3];   // stage slot, bytes, token rows
     constexpr int KC = kChunkBytes * (BITS == 4 ? 2 : 1);   // K values per chunk
     constexpr int SEGK = BITS == 4 ? 128 : 64;              // K values per 64-byte segment
     constexpr bool SCOL = SMODE == kScaleCol;
@@ -383,6 +386,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
     }
     __syncthreads();
 
+    // the next kernel (FC2 after FC1, the combine after FC2) may start its
+    // prologue on SMs this grid leaves
+    ptx::griddep_launch_dependents();
     const int n_active = a.tiles[1];
     const int64_t units = int64_t(n_active) * a.n_rb * a.splits;
 
@@ -395,6 +401,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
         uint32_t it = 0;   // stages issued (for the drain after a timeout)
         Ring ring;
         bool ok = true;
+        // FC2 is launched as a dependent of FC1: the weight and scale boxes of the
+        // first stages are issued at once, the copies of FC1's output (the token
+        // rows) only after griddepcontrol.wait.  Up to nstages stages are held back.
+        bool dep_done = FC1;
+        uint32_t held = 0;
+        auto release_held = [&]() {
+            ptx::griddep_wait();
+            __syncwarp();
+            for (uint32_t h = 0; h < held; ++h) {
+                const uint32_t hs = held_meta[h][0];
+                if (lane < int(held_meta[h][2]))
+                    ptx::bulk_g2s(smem + size_t(hs) * a.stage_bytes + a.off_b + lane * a.pitch_b,
+                                  held_src[h][lane], held_meta[h][1], &full_bar[hs]);
+            }
+            held = 0;
+            dep_done = true;
+        };
         // Unit metadata is a chain of dependent loads (expert -> its token count
         // and offset -> its token rows); it is loaded ahead of use (experts three
         // units ahead, counts two, token rows one) so that the producer never waits
@@ -423,6 +446,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
             const int32_t row0 = int32_t(int64_t(e) * a.N + int64_t(rb) * kDecRows);
             for (int kc = c0; kc < c1; ++kc, ++it, ring.advance(a.nstages)) {
                 const uint32_t st = ring.st;
+                // a stage about to be reused needs the held copies of the first round
+                if (!dep_done && it >= a.nstages) release_held();
                 if (!ptx::mbar_wait_sleep(&empty_bar[st], ring.ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
@@ -443,15 +468,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_gemv_kernel(const __gri
                         ptx::tma_load_2d(sbase + a.off_s, &a.tm_s, kc * a.nsc, row0, &full_bar[st]);
                 }
                 __syncwarp();
-                if (lane < ne)
-                    ptx::bulk_g2s(sbase + a.off_b + lane * a.pitch_b,
-                                  a.b_src + brow * a.b_pitch + int64_t(kc) * KC, bbytes,
-                                  &full_bar[st]);
+                if (dep_done) {
+                    if (lane < ne)
+                        ptx::bulk_g2s(sbase + a.off_b + lane * a.pitch_b,
+                                      a.b_src + brow * a.b_pitch + int64_t(kc) * KC, bbytes,
+                                      &full_bar[st]);
+                } else {
+                    held_src[held][lane] = a.b_src + brow * a.b_pitch + int64_t(kc) * KC;
+                    if (lane == 0) {
+                        held_meta[held][0] = st;
+                        held_meta[held][1] = bbytes;
+                        held_meta[held][2] = uint32_t(ne);
+                    }
+                    __syncwarp();
+                    ++held;
+                }
             }
             e0 = e1; ne0 = ne1; off0 = off1; brow0 = brow1;
             e1 = e2; ne1 = ne2; off1 = off2;
             e2 = e3;
         }
+        if (!dep_done && held > 0) release_held();
         if (!ok && lane == 0) {
             record_error(a.err, QMOE_DEVERR_TIMEOUT);
             abort_flag = 1;
@@ -641,8 +678,12 @@ cudaError_t launch_variant(const DecodeArgs& args, int grid, size_t smem, cudaSt
     auto kern = decode_gemv_kernel<BITS, SMODE, NBS, FC1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kDecThreads, smem, s>>>(args);
-    return cudaGetLastError();
+    if (FC1) {
+        kern<<<grid, kDecThreads, smem, s>>>(args);
+        return cudaGetLastError();
+    }
+    // FC2 overlaps FC1's last wave: it waits for FC1 only before reading its output
+    return launch_dependent(kern, dim3(grid), dim3(kDecThreads), smem, s, args);
 }
 
 int ilog2(int64_t v) {

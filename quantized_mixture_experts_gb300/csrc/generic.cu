@@ -109,6 +109,8 @@ __global__ void generic_fc2_kernel(Problem p, const int32_t* __restrict__ perm,
 __global__ void combine_kernel(const float* __restrict__ slot_out, const float* __restrict__ pw,
                                float* __restrict__ y, int64_t T, int64_t H, int k, int splits,
                                int64_t slots, int vec) {
+    // launched as a dependent of the kernel that writes slot_out
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (vec) {
         const int64_t H4 = H / 4;
@@ -194,6 +196,8 @@ cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, 
 // One thread per 8 output columns (H % 8 == 0 on the grouped path).
 __global__ void combine16_kernel(const uint4* __restrict__ s16, float* __restrict__ y, int64_t T,
                                  int64_t H, int k, int aligned) {
+    // launched as a dependent of the kernel that writes the slot rows
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t H8 = H / 8;
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= T * H8) return;
@@ -232,11 +236,12 @@ cudaError_t launch_combine16(const Problem& p, const Work& w, cudaStream_t s) {
     const int64_t n = p.T * (p.H / 8);
     note_launch(QMOE_KERNEL_COMBINE, s, true);
     const int threads = n < 152 * 256 ? 64 : 256;
-    combine16_kernel<<<blocks_for(n, threads), threads, 0, s>>>(
+    cudaError_t e = launch_dependent(
+        combine16_kernel, dim3(unsigned(blocks_for(n, threads))), dim3(threads), 0, s,
         reinterpret_cast<const uint4*>(w.slot_out), p.y, p.T, p.H, int(p.k),
         (reinterpret_cast<uintptr_t>(p.y) & 15) == 0 ? 1 : 0);
     note_launch(QMOE_KERNEL_COMBINE, s, false);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,
@@ -246,10 +251,12 @@ cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int 
     const int64_t n = vec ? p.T * (p.H / 4) : p.T * p.H;
     note_launch(QMOE_KERNEL_COMBINE, s, true);
     const int threads = n < 152 * 256 ? 64 : 256;   // spread small batches over more SMs
-    combine_kernel<<<blocks_for(n, threads), threads, 0, s>>>(w.slot_out, w.pw, p.y, p.T, p.H,
-                                                              int(p.k), splits, pl.slots, vec);
+    cudaError_t e = launch_dependent(combine_kernel, dim3(unsigned(blocks_for(n, threads))),
+                                     dim3(threads), 0, s, static_cast<const float*>(w.slot_out),
+                                     static_cast<const float*>(w.pw), p.y, p.T, p.H, int(p.k),
+                                     splits, pl.slots, vec);
     note_launch(QMOE_KERNEL_COMBINE, s, false);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace qmoe
