@@ -66,6 +66,13 @@ SMALL = [
     Workload("decode_8bit_bs64", 33, (9, 512), 512, 256, 4, 3, 8, 64, "swiglu"),
     Workload("decode_limit", 34, (4, 256), 256, 256, 4, 2, 4, 0, "swiglu", alpha=1.3,
              beta=-0.2, swiglu_limit=0.3),
+    # block size 256: FC1 scales staged by TMA (4 blocks per row), FC2 scales read
+    # directly (2 blocks per row, not a multiple of four)
+    Workload("bs256", 35, (40, 1024), 1024, 512, 4, 2, 4, 256, "swiglu"),
+    # 4-bit column-wise codes with two token tiles per expert on the grouped path
+    Workload("col4_two_tiles_relu", 36, (600, 256), 256, 128, 4, 2, 4, 0, "relu"),
+    # k = E on the decode path: every token reaches every expert
+    Workload("decode_k_eq_E", 37, (8, 256), 256, 256, 4, 4, 4, 32, "swiglu"),
 ]
 
 
