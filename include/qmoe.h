@@ -222,8 +222,20 @@ qmoe_status qmoe_forward_noalloc(const float *input, const int64_t *input_shape,
 typedef enum { QMOE_DT_F32 = 0, QMOE_DT_F16 = 1, QMOE_DT_BF16 = 2, QMOE_DT_F64 = 3 } qmoe_dtype;
 typedef enum { QMOE_IDX_I32 = 0, QMOE_IDX_I64 = 1 } qmoe_index_dtype;
 
-/* Workspace bytes grouped_matmul needs (it holds the device error word). */
+/* Workspace bytes grouped_matmul needs at least (it holds the device error word). */
 qmoe_status grouped_matmul_workspace_size(size_t *bytes);
+
+/*
+ * Workspace bytes that let grouped_matmul run on the tensor cores for this
+ * shape: f16 or bf16, K a multiple of 64, N a multiple of 8, G <= 8191, with
+ * input, weights and output 16-byte aligned.  The workspace then holds the
+ * grouping of the (m, i) rows by index and the input rows gathered in group
+ * order (about 2 * K * M * S bytes).  For other shapes and types *bytes is the
+ * minimum of grouped_matmul_workspace_size.  A smaller workspace is valid: the
+ * call then uses the general kernel (fp32 accumulation either way).
+ */
+qmoe_status grouped_matmul_workspace_size_for(int64_t M, int64_t K, int64_t G, int64_t N,
+                                              int64_t S, int32_t dtype, size_t *bytes);
 
 /*
  * GroupedMatMul-29 (Summary, Inputs, Outputs):

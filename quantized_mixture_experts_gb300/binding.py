@@ -93,6 +93,9 @@ def load():
     lib.qmoe_forward_noalloc.restype = ctypes.c_int
     lib.grouped_matmul_workspace_size.argtypes = [ctypes.POINTER(SZ)]
     lib.grouped_matmul_workspace_size.restype = ctypes.c_int
+    lib.grouped_matmul_workspace_size_for.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int32,
+                                                      ctypes.POINTER(SZ)]
+    lib.grouped_matmul_workspace_size_for.restype = ctypes.c_int
     lib.grouped_matmul.argtypes = [P, I64, I64, P, I64, I64, P, I64, I32, P, P, I32, P, SZ, P]
     lib.grouped_matmul.restype = ctypes.c_int
     lib.qmoe_get_device_error.argtypes = [P, P, ctypes.POINTER(I32)]
@@ -289,7 +292,8 @@ def grouped_matmul(input, weights, group_indices, bias=None, *, output=None, wor
     if output is None:
         output = torch.empty((M, S, N), dtype=input.dtype, device=input.device)
     if workspace is None:
-        workspace = alloc_workspace(256, input.device)
+        workspace = alloc_workspace(grouped_matmul_workspace_size(M, K, G, N, S, input.dtype),
+                                    input.device)
     idt = IDX_I64 if group_indices.dtype == torch.int64 else IDX_I32
     st = load().grouped_matmul(_ptr(input), M, K, _ptr(weights), G, N, _ptr(group_indices), S,
                                idt, _ptr(bias) if bias is not None and bias.numel() else None,
@@ -297,6 +301,16 @@ def grouped_matmul(input, weights, group_indices, bias=None, *, output=None, wor
                                workspace.numel(), _stream(stream))
     _check(st, "grouped_matmul")
     return output
+
+
+def grouped_matmul_workspace_size(M, K, G, N, S, dtype) -> int:
+    """Workspace bytes that let grouped_matmul use the tensor cores for this shape
+    (include/qmoe.h grouped_matmul_workspace_size_for); 256 when it cannot."""
+    n = ctypes.c_size_t(0)
+    _check(load().grouped_matmul_workspace_size_for(int(M), int(K), int(G), int(N), int(S),
+                                                    _gmm_dtype(dtype), ctypes.byref(n)),
+           "grouped_matmul_workspace_size_for")
+    return n.value
 
 
 def get_device_error(workspace, stream=None) -> int:

@@ -469,6 +469,15 @@ qmoe_status grouped_matmul_workspace_size(size_t* bytes) {
     return QMOE_OK;
 }
 
+qmoe_status grouped_matmul_workspace_size_for(int64_t M, int64_t K, int64_t G, int64_t N,
+                                              int64_t S, int32_t dtype, size_t* bytes) {
+    if (!bytes) return QMOE_ERR_INVALID_ARGUMENT;
+    if (M < 0 || K < 0 || G < 0 || N < 0 || S < 0) return QMOE_ERR_INVALID_ARGUMENT;
+    const size_t tc = grouped_matmul_tc_workspace(M, K, G, N, S, dtype);
+    *bytes = std::max<size_t>(256, tc);
+    return QMOE_OK;
+}
+
 qmoe_status grouped_matmul(const void* input, int64_t M, int64_t K, const void* weights,
                            int64_t G, int64_t N, const void* group_indices, int64_t S,
                            int32_t index_dtype, const void* bias, void* output, int32_t dtype,
@@ -490,6 +499,16 @@ qmoe_status grouped_matmul(const void* input, int64_t M, int64_t K, const void* 
     if (!weights && K > 0) return QMOE_ERR_INVALID_ARGUMENT;
     if (G == 0) {
         // every index is out of range
+    }
+    // tensor cores when the shape, type, alignment and workspace allow it
+    const size_t tc = grouped_matmul_tc_workspace(M, K, G, N, S, dtype);
+    const auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+    if (tc > 0 && workspace_bytes >= tc && aligned16(input) && aligned16(weights) &&
+        aligned16(output) && (reinterpret_cast<uintptr_t>(bias) & 1) == 0) {
+        cudaError_t e = launch_grouped_matmul_tc(input, M, K, weights, G, N, group_indices, S,
+                                                 index_dtype == QMOE_IDX_I64, bias, output, dtype,
+                                                 workspace, s);
+        return e == cudaSuccess ? QMOE_OK : QMOE_ERR_CUDA;
     }
     cudaError_t e = launch_grouped_matmul(input, M, K, weights, G, N, group_indices, S,
                                           index_dtype == QMOE_IDX_I64, bias, output, dtype, err,

@@ -127,6 +127,19 @@ cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Wor
                                      int x16_mode, cudaStream_t s);
 cudaError_t launch_generic_fc1(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 cudaError_t launch_generic_fc2(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+// Grouping of arbitrary items by group id (shared by the layer and grouped_matmul).
+cudaError_t launch_group_items(int32_t* hist, int64_t chunks, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* tiles, int32_t* active, int tile_tokens,
+                               const int32_t* sel, const int32_t* rank, int64_t slots, int k,
+                               int32_t* perm, int32_t* inv, cudaStream_t s);
+// grouped_matmul on the tensor cores (f16/bf16): workspace bytes (0 when the
+// shape or type does not qualify) and launch.
+size_t grouped_matmul_tc_workspace(int64_t M, int64_t K, int64_t G, int64_t N, int64_t S,
+                                   int dtype);
+cudaError_t launch_grouped_matmul_tc(const void* input, int64_t M, int64_t K, const void* weights,
+                                     int64_t G, int64_t N, const void* idx, int64_t S, int idx64,
+                                     const void* bias, void* out, int dtype, void* workspace,
+                                     cudaStream_t s);
 // Grouped path: the FC2 rows are fp16 [T*k, H] and already weighted by routing weight.
 cudaError_t launch_combine16(const Problem& p, const Work& w, cudaStream_t s);
 cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int splits,

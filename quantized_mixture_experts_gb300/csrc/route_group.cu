@@ -529,6 +529,29 @@ cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Wor
     return cudaGetLastError();
 }
 
+// Counts, offsets, tile table and stable permutation of `slots` items with
+// group ids sel[0..slots) in [0, E), from per-chunk histograms (chunks of
+// kRouteTokensPerChunk * k items) and in-chunk ranks.
+cudaError_t launch_group_items(int32_t* hist, int64_t chunks, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* tiles, int32_t* active, int tile_tokens,
+                               const int32_t* sel, const int32_t* rank, int64_t slots, int k,
+                               int32_t* perm, int32_t* inv, cudaStream_t s) {
+    const int nthr = 1024;
+    const int P = E >= nthr ? 1 : nthr / E;
+    const size_t smem = sizeof(int32_t) * std::max<size_t>(size_t(P) * E, size_t(E));
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(group_scan_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    group_scan_kernel<<<1, nthr, smem, s>>>(hist, chunks, E, counts, offsets, tiles, active,
+                                            tile_tokens);
+    group_scatter_kernel<<<unsigned((slots + 255) / 256), 256, 0, s>>>(sel, rank, hist, offsets,
+                                                                       slots, k, E, perm, inv);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
     const int E = int(p.E);
     const int nthr = 1024;

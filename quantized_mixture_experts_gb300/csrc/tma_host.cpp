@@ -44,6 +44,23 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    const uint64_t dims[3], const uint64_t strides_bytes[2], const uint32_t box[3],
+                    CUtensorMapSwizzle swizzle) {
+    EncodeFn fn = encoder();
+    if (!fn) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    if ((strides_bytes[0] & 15) != 0 || (strides_bytes[1] & 15) != 0) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, b, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 152;

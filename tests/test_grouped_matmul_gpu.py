@@ -96,3 +96,79 @@ def test_out_of_range_index_sets_error_and_zero_row(dev):
     o = out.cpu().numpy()
     assert np.all(o[0] == 4.0) and np.all(o[1] == 0.0) and np.all(o[2] == 0.0)
     assert q.get_device_error(ws) == q.DEVERR_NONE   # read clears the word
+
+
+def _oracle_check(out, x, w, idx, b, dt, K):
+    xr, wr = x.double().cpu().numpy(), w.double().cpu().numpy()
+    br = None if b is None else b.double().cpu().numpy()
+    ix = idx.cpu().numpy()
+    ref, st = oracle.grouped_matmul(xr, wr, ix, br)
+    assert st == oracle.OK
+    mag = np.einsum("mk,mskn->msn", np.abs(xr), np.abs(wr)[ix])
+    if br is not None:
+        mag = mag + np.abs(br)[ix]
+    eps_out = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dt]
+    bound = 2 * (K + 2) * 2.0 ** -24 * mag + eps_out * np.abs(ref) + 1e-300
+    err = np.abs(out.double().cpu().numpy() - ref)
+    assert np.all(err <= bound), float(np.max(err / bound))
+
+
+def _launches():
+    import quantized_mixture_experts_gb300 as q
+    return q.load().qmoe_launch_count()
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("shape,idt", [((600, 512, 7, 384, 2), "int32"),
+                                       ((300, 128, 40, 200, 3), "int64"),
+                                       ((17, 64, 3, 8, 1), "int32")],
+                         ids=["tiles_bias", "ragged_n_i64", "tiny"])
+def test_tensor_core_path_vs_oracle(dev, dt, shape, idt):
+    """f16/bf16 with K % 64 == 0 and N % 8 == 0 take the tensor-core path (more
+    than one launch: grouping, gather, GEMM) when the workspace allows it."""
+    import quantized_mixture_experts_gb300 as q
+    M, K, G, N, S = shape
+    rng = np.random.default_rng(sum(shape) + len(dt))
+    tdt = getattr(torch, DTYPES[dt])
+    x = torch.from_numpy(rng.standard_normal((M, K))).to(tdt).to(dev)
+    w = torch.from_numpy(rng.standard_normal((G, K, N)) / np.sqrt(K)).to(tdt).to(dev)
+    b = torch.from_numpy(rng.standard_normal((G, N))).to(tdt).to(dev)
+    idx = torch.from_numpy(rng.integers(0, G, (M, S))).to(getattr(torch, idt)).to(dev)
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(M, K, G, N, S, tdt))
+    n0 = _launches()
+    out = q.grouped_matmul(x, w, idx, b, workspace=ws)
+    torch.cuda.synchronize()
+    n_tc = _launches() - n0
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+    _oracle_check(out, x, w, idx, b, dt, K)
+    # the same call with the minimal workspace runs the general kernel (one launch
+    # after clearing the error word): same bound
+    ws_small = q.alloc_workspace(256)
+    n0 = _launches()
+    out2 = q.grouped_matmul(x, w, idx, b, workspace=ws_small)
+    torch.cuda.synchronize()
+    n_general = _launches() - n0
+    assert n_general == 2 and n_tc > n_general, (n_tc, n_general)
+    _oracle_check(out2, x, w, idx, b, dt, K)
+
+
+def test_tensor_core_path_invalid_index(dev):
+    import quantized_mixture_experts_gb300 as q
+    M, K, G, N, S = 40, 64, 3, 64, 2
+    x = torch.ones((M, K), dtype=torch.float16, device=dev)
+    w = torch.ones((G, K, N), dtype=torch.float16, device=dev) / 64
+    idx = torch.zeros((M, S), dtype=torch.int64, device=dev)
+    idx[3, 1] = G
+    idx[7, 0] = -5
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(M, K, G, N, S, torch.float16))
+    out = torch.full((M, S, N), float("nan"), dtype=torch.float16, device=dev)
+    n0 = _launches()
+    q.grouped_matmul(x, w, idx, output=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert _launches() - n0 > 2   # the tensor-core path
+    assert q.get_device_error(ws) == q.DEVERR_INDEX
+    o = out.float().cpu().numpy()
+    assert np.all(o[3, 1] == 0.0) and np.all(o[7, 0] == 0.0)
+    mask = np.ones((M, S), dtype=bool)
+    mask[3, 1] = mask[7, 0] = False
+    assert np.all(o[mask] == 1.0)
