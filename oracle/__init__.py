@@ -1,15 +1,17 @@
-"""CPU reference oracle for the QMoE layer and GroupedMatMul (test infrastructure).
+"""CPU reference oracle for the QMoE layer, the float MoE layer and GroupedMatMul
+(test infrastructure).
 
 Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It is a ctypes wrapper over the plain
-double-precision C restatement in ``qmoe_oracle.c``; it shares no code with
+double-precision C restatements in ``qmoe_oracle.c`` and ``moe_oracle.c``
+(the float MoE of the [MoE README]); it shares no code with
 the CUDA library and never calls it.  The wrapper only marshals arrays and
 derives shapes ([QMoE manifest] derive.numTokens / derive.hiddenSize: the
 token count is the product of the leading input dimensions).
 
 Functions whose result has no independent pin say so here and in the design
 notes: ``swiglu_limit`` handling (reading of [QMoE manifest]
-attributeDescriptions.swiglu_limit) is "parity unpinned".
+attributeDescriptions.swiglu_limit) is "parity unpinned", in both layers.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "qmoe_oracle.c")
+_SRCS = [os.path.join(_HERE, "qmoe_oracle.c"), os.path.join(_HERE, "moe_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -32,12 +34,12 @@ BAD_ARG = -2
 
 
 def build(force: bool = False) -> str:
-    """Compile qmoe_oracle.c into liboracle.so with gcc (no CUDA involved)."""
+    """Compile the oracle's C sources into liboracle.so with gcc (no CUDA involved)."""
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(f) for f in _SRCS)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, *_SRCS,
            "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
@@ -72,6 +74,13 @@ def _load():
         lib.oracle_qmoe.argtypes = [P, I64, P, I64, P, P, P, P, I64, C, I64, C, D, D,
                                     C, D, I64, P, I64, C, P, P, P, C]
         lib.oracle_qmoe.restype = C
+        lib.oracle_moe_route.argtypes = [P, I64, I64, C, P, P]
+        lib.oracle_moe_route.restype = C
+        lib.oracle_moe_activation.argtypes = [P, P, I64, C, C, D, D, C, D, P]
+        lib.oracle_moe_activation.restype = None
+        lib.oracle_moe.argtypes = [P, I64, P, I64, P, P, P, P, P, P, I64, C, C, D, D, C, D,
+                                   I64, C, P, I64, C, P, P, P, C]
+        lib.oracle_moe.restype = C
         _lib = lib
         return lib
 
@@ -194,3 +203,77 @@ def qmoe(x, logits, w1, s1, w2, s2, *, k, expert_weight_bits=4, block_size=0,
     if st != OK:
         raise ValueError(f"oracle_qmoe failed with {st}")
     return y, sel, p
+
+
+# --------------------------------------------------------------------------
+# Float MoE  ([MoE README] Description, Inputs, Attributes)
+# --------------------------------------------------------------------------
+
+MOE_ACTIVATIONS = {"relu": 0, "gelu": 1, "silu": 2, "swiglu": 3, "identity": 4}
+
+
+def moe_route(logits, k, normalize_routing_weights=0):
+    """Softmax over all experts, the k most probable (descending), optionally
+    renormalised over the selection.  Returns (sel [T,k] int32, w [T,k] f64)."""
+    lib = _load()
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    sel = np.zeros((T, k), dtype=np.int32)
+    w = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        st = lib.oracle_moe_route(_ptr(lg[t]), E, k, int(normalize_routing_weights),
+                                  _ptr(sel[t]), _ptr(w[t]))
+        if st != OK:
+            raise ValueError(f"oracle_moe_route failed with {st}")
+    return sel, w
+
+
+def moe_activation(h1, inter, act, h3=None, swiglu_fusion=0, alpha=1.0, beta=0.0,
+                   swiglu_limit=None):
+    """The activation of one expert row: h1 (fusion*inter values), h3 (inter or None)."""
+    lib = _load()
+    a1 = _c(h1, np.float64)
+    a3 = None if h3 is None else _c(h3, np.float64)
+    out = np.zeros(inter, dtype=np.float64)
+    lib.oracle_moe_activation(_ptr(a1), None if a3 is None else _ptr(a3), inter,
+                              MOE_ACTIVATIONS[act], int(swiglu_fusion), float(alpha),
+                              float(beta), 0 if swiglu_limit is None else 1,
+                              0.0 if swiglu_limit is None else float(swiglu_limit), _ptr(out))
+    return out
+
+
+def moe(x, logits, fc1_w, fc2_w, *, k, fc1_bias=None, fc2_bias=None, fc3_w=None,
+        fc3_bias=None, activation_type="relu", swiglu_fusion=0, activation_alpha=1.0,
+        activation_beta=0.0, swiglu_limit=None, normalize_routing_weights=0,
+        tokens=None, dense=False, nthreads=1):
+    """Float MoE layer output for the listed tokens (all tokens when None).
+
+    Returns (y [ntok, H] float64, sel [ntok, k] int32, w [ntok, k] float64).
+    """
+    lib = _load()
+    xs = _c(x, np.float32)
+    H = xs.shape[-1]
+    xs = xs.reshape(-1, H)
+    lg = _c(logits, np.float32)
+    E = lg.shape[1]
+    w1 = _c(fc1_w, np.float32)
+    w2 = _c(fc2_w, np.float32)
+    I = w2.shape[2]
+    opt = [None if a is None else _c(a, np.float32) for a in (fc1_bias, fc2_bias, fc3_w, fc3_bias)]
+    tok = (np.arange(xs.shape[0], dtype=np.int64) if tokens is None
+           else _c(tokens, np.int64))
+    ntok = tok.shape[0]
+    y = np.zeros((ntok, H), dtype=np.float64)
+    sel = np.zeros((ntok, k), dtype=np.int32)
+    w = np.zeros((ntok, k), dtype=np.float64)
+    b1, b2, w3, b3 = [None if a is None else _ptr(a) for a in opt]
+    st = lib.oracle_moe(_ptr(xs), H, _ptr(lg), E, _ptr(w1), b1, _ptr(w2), b2, w3, b3, I,
+                        MOE_ACTIVATIONS[activation_type], int(swiglu_fusion),
+                        float(activation_alpha), float(activation_beta),
+                        0 if swiglu_limit is None else 1,
+                        0.0 if swiglu_limit is None else float(swiglu_limit), int(k),
+                        int(normalize_routing_weights), _ptr(tok), ntok, 1 if dense else 0,
+                        _ptr(y), _ptr(sel), _ptr(w), int(nthreads))
+    if st != OK:
+        raise ValueError(f"oracle_moe failed with {st}")
+    return y, sel, w
