@@ -1,4 +1,4 @@
-"""ctypes binding of the C ABI in include/qmoe.h.
+"""ctypes binding of the C ABI in include/qmoe.h and include/moe.h.
 
 Argument marshalling only: every step of the layer runs in the CUDA library
 ``libqmoe_gb300.so``.  Tensors are torch CUDA tensors (torch supplies device
@@ -15,6 +15,7 @@ from typing import Optional, Sequence
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmoe_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "qmoe.h")
+MOE_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
 
 # qmoe_status
 OK, ERR_INVALID_ARGUMENT, ERR_NOT_SUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
@@ -56,6 +57,26 @@ class Attrs(ctypes.Structure):
         ("path", ctypes.c_int32),
     ]
 
+
+class MoeAttrs(ctypes.Structure):
+    """Mirror of moe_attrs (same field order and C types)."""
+    _fields_ = [
+        ("k", ctypes.c_int64),
+        ("activation_type", ctypes.c_int32),
+        ("swiglu_fusion", ctypes.c_int32),
+        ("activation_alpha", ctypes.c_float),
+        ("activation_beta", ctypes.c_float),
+        ("has_swiglu_limit", ctypes.c_int32),
+        ("swiglu_limit", ctypes.c_float),
+        ("normalize_routing_weights", ctypes.c_int32),
+        ("use_sparse_mixer", ctypes.c_int32),
+        ("path", ctypes.c_int32),
+    ]
+
+
+# moe_activation / moe_path
+MOE_ACTIVATIONS = {"relu": 0, "gelu": 1, "silu": 2, "swiglu": 3, "identity": 4}
+MOE_PATH_AUTO, MOE_PATH_GROUPED, MOE_PATH_GENERIC = 0, 2, 3
 
 _lib = None
 
@@ -110,13 +131,28 @@ def load():
     lib.qmoe_profile_end.restype = ctypes.c_int
     lib.qmoe_launch_count.argtypes = []
     lib.qmoe_launch_count.restype = ctypes.c_uint64
+    PM = ctypes.POINTER(MoeAttrs)
+    lib.moe_attrs_default.argtypes = [PM]
+    lib.moe_attrs_default.restype = None
+    for name in ("moe_workspace_size", "moe_hostio_workspace_size"):
+        getattr(lib, name).argtypes = [PI64, I32, PI64, PM, ctypes.POINTER(SZ)]
+        getattr(lib, name).restype = ctypes.c_int
+    lib.moe_choose_path.argtypes = [PI64, I32, PI64, PM, ctypes.POINTER(I32)]
+    lib.moe_choose_path.restype = ctypes.c_int
+    mfwd = [P, PI64, I32, P, PI64, P, PI64, P, P, PI64, P, P, PI64, P, P, PM, P, SZ]
+    lib.moe_forward.argtypes = mfwd + [P, P, P]
+    lib.moe_forward.restype = ctypes.c_int
+    lib.moe_forward_hostio.argtypes = mfwd + [P]
+    lib.moe_forward_hostio.restype = ctypes.c_int
+    lib.moe_get_device_error.argtypes = [P, P, ctypes.POINTER(I32)]
+    lib.moe_get_device_error.restype = ctypes.c_int
     _lib = lib
     return lib
 
 
 def declared_functions() -> list:
-    """Names of the functions include/qmoe.h declares."""
-    text = open(HEADER_PATH).read()
+    """Names of the functions include/qmoe.h and include/moe.h declare."""
+    text = open(HEADER_PATH).read() + open(MOE_HEADER_PATH).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "while", "for", "switch")))
@@ -342,3 +378,97 @@ def profile_end():
 
 def launch_count() -> int:
     return int(load().qmoe_launch_count())
+
+
+# --------------------------------------------------------------------------
+# Float MoE (include/moe.h)
+# --------------------------------------------------------------------------
+
+def make_moe_attrs(k: int = 1, activation_type: str = "relu", swiglu_fusion: int = 0,
+                   activation_alpha: float = 1.0, activation_beta: float = 0.0,
+                   swiglu_limit: Optional[float] = None, normalize_routing_weights: int = 0,
+                   use_sparse_mixer: int = 0, path: int = MOE_PATH_AUTO) -> MoeAttrs:
+    a = MoeAttrs()
+    load().moe_attrs_default(ctypes.byref(a))
+    a.k = int(k)
+    a.activation_type = (MOE_ACTIVATIONS.get(activation_type, 99)
+                         if isinstance(activation_type, str) else int(activation_type))
+    a.swiglu_fusion = int(swiglu_fusion)
+    a.activation_alpha = float(activation_alpha)
+    a.activation_beta = float(activation_beta)
+    a.has_swiglu_limit = 0 if swiglu_limit is None else 1
+    a.swiglu_limit = 0.0 if swiglu_limit is None else float(swiglu_limit)
+    a.normalize_routing_weights = int(normalize_routing_weights)
+    a.use_sparse_mixer = int(use_sparse_mixer)
+    a.path = int(path)
+    return a
+
+
+def moe_workspace_size(input_shape, fc1_w_shape, attrs: MoeAttrs, hostio: bool = False) -> int:
+    lib = load()
+    out = ctypes.c_size_t(0)
+    fn = lib.moe_hostio_workspace_size if hostio else lib.moe_workspace_size
+    _check(fn(_shape(input_shape), len(input_shape), _shape(fc1_w_shape), ctypes.byref(attrs),
+              ctypes.byref(out)), "moe_workspace_size")
+    return out.value
+
+
+def moe_choose_path(input_shape, fc1_w_shape, attrs: MoeAttrs) -> int:
+    out = ctypes.c_int32(0)
+    _check(load().moe_choose_path(_shape(input_shape), len(input_shape), _shape(fc1_w_shape),
+                                  ctypes.byref(attrs), ctypes.byref(out)), "moe_choose_path")
+    return out.value
+
+
+def _opt_shape(t):
+    return None if t is None else _shape(t.shape)
+
+
+def moe_forward(input, router_probs, fc1_experts_weights, fc2_experts_weights, *,
+                fc1_experts_bias=None, fc2_experts_bias=None, fc3_experts_weights=None,
+                fc3_experts_bias=None, attrs: Optional[MoeAttrs] = None, output=None,
+                workspace=None, topk_idx=None, topk_w=None, stream=None, **attr_kwargs):
+    """Float MoE layer (include/moe.h moe_forward) on torch CUDA tensors."""
+    import torch
+    if attrs is None:
+        attrs = make_moe_attrs(**attr_kwargs)
+    if output is None:
+        output = torch.empty_like(input)
+    if workspace is None:
+        workspace = alloc_workspace(moe_workspace_size(tuple(input.shape),
+                                                       tuple(fc1_experts_weights.shape), attrs),
+                                    input.device)
+    st = load().moe_forward(
+        _ptr(input), _shape(input.shape), input.dim(),
+        _ptr(router_probs), _shape(router_probs.shape),
+        _ptr(fc1_experts_weights), _shape(fc1_experts_weights.shape), _ptr(fc1_experts_bias),
+        _ptr(fc2_experts_weights), _shape(fc2_experts_weights.shape), _ptr(fc2_experts_bias),
+        _ptr(fc3_experts_weights), _opt_shape(fc3_experts_weights), _ptr(fc3_experts_bias),
+        _ptr(output), ctypes.byref(attrs), _ptr(workspace), workspace.numel(),
+        _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    _check(st, "moe_forward")
+    return output
+
+
+def moe_forward_hostio(host_input, host_router_probs, fc1_experts_weights, fc2_experts_weights,
+                       host_output, *, attrs: MoeAttrs, workspace, fc1_experts_bias=None,
+                       fc2_experts_bias=None, fc3_experts_weights=None, fc3_experts_bias=None,
+                       stream=None):
+    """moe_forward_hostio: host (ideally pinned) activations in and out."""
+    st = load().moe_forward_hostio(
+        _ptr(host_input), _shape(host_input.shape), host_input.dim(),
+        _ptr(host_router_probs), _shape(host_router_probs.shape),
+        _ptr(fc1_experts_weights), _shape(fc1_experts_weights.shape), _ptr(fc1_experts_bias),
+        _ptr(fc2_experts_weights), _shape(fc2_experts_weights.shape), _ptr(fc2_experts_bias),
+        _ptr(fc3_experts_weights), _opt_shape(fc3_experts_weights), _ptr(fc3_experts_bias),
+        _ptr(host_output), ctypes.byref(attrs), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check(st, "moe_forward_hostio")
+    return host_output
+
+
+def moe_get_device_error(workspace, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(load().moe_get_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)),
+           "moe_get_device_error")
+    return code.value

@@ -50,6 +50,7 @@ struct Problem {
     int has_limit = 0;
     float limit = 0.f;
     int path = QMOE_PATH_GENERIC;
+    int full_softmax = 0; // routing denominator over every expert (float MoE, unnormalised)
     // device tensors
     const float* x = nullptr;
     const float* logits = nullptr;

@@ -6,6 +6,10 @@
 // routing for 0 and 1), passes QMoE.RouteStage and QMoE.GroupStage
 // (intermediates routeExpert, routeMix, slotList, tileMeta;
 // derive.groupSlots, derive.groupMaxTiles).
+// The float MoE (com.microsoft.MoE README, Description and Attributes) takes
+// the softmax over all experts before top-k; with normalize_routing_weights = 1
+// its weights are renormalised over the selection, which is the softmax over
+// the selected logits again.  `full` selects the all-expert denominator.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -28,7 +32,7 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // order and writes experts, logits (temporarily) and routing weights.
 // General form: any E and k; every selection round re-reads the row.
 __device__ void route_one_token_any(const float* __restrict__ row, int E, int k, int32_t* sel,
-                                    float* pw, int32_t* s_exp, int lane) {
+                                    float* pw, int32_t* s_exp, int lane, int full) {
     float prev_v = 0.f;
     int prev_i = -1;
     float vmax = 0.f;
@@ -62,9 +66,12 @@ __device__ void route_one_token_any(const float* __restrict__ row, int E, int k,
         }
     }
     __syncwarp();
-    // softmax over the k selected logits, max subtracted first
+    // softmax over the k selected logits (or every logit), max subtracted first
     float part = 0.f;
-    for (int i = lane; i < k; i += 32) part += expf(pw[i] - vmax);
+    if (full)
+        for (int e = lane; e < E; e += 32) part += expf(row[e] - vmax);
+    else
+        for (int i = lane; i < k; i += 32) part += expf(pw[i] - vmax);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
     __syncwarp();
@@ -76,9 +83,9 @@ __device__ void route_one_token_any(const float* __restrict__ row, int E, int k,
 // touch no memory.  The softmax sums in the same shuffle tree as the general form.
 constexpr int kRouteRegs = 8;
 __device__ void route_one_token(const float* __restrict__ row, int E, int k, int32_t* sel,
-                                float* pw, int32_t* s_exp, int lane) {
+                                float* pw, int32_t* s_exp, int lane, int full) {
     if (E > 32 * kRouteRegs || k > 32) {
-        route_one_token_any(row, E, k, sel, pw, s_exp, lane);
+        route_one_token_any(row, E, k, sel, pw, s_exp, lane, full);
         return;
     }
     float v[kRouteRegs];
@@ -118,9 +125,15 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
             mine_i = best_i;
         }
     }
-    // softmax over the k selected logits, max subtracted first
+    // softmax over the k selected logits (or every logit), max subtracted first
     float part = lane < k ? expf(mine_v - vmax) : 0.f;
     const float mine_e = part;
+    if (full) {
+        part = 0.f;
+#pragma unroll
+        for (int j = 0; j < kRouteRegs; ++j)
+            if (lane + 32 * j < E) part += expf(v[j] - vmax);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
     if (lane < k) {
@@ -209,7 +222,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
     float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
     const float* __restrict__ x, int64_t H, __half* __restrict__ x16, int64_t Hp,
-    int x16_mode, int32_t* __restrict__ ctrl) {
+    int x16_mode, int full, int32_t* __restrict__ ctrl) {
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;        // [E]
     int32_t* s_exp = smem + E;    // [chunk tokens * k]
@@ -228,7 +241,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
     for (int lt = warp; lt < ntok; lt += kRouteThreads / 32) {
         const int64_t t = t0 + lt;
-        route_one_token(logits + t * E, E, k, sel + t * k, pw + t * k, s_exp + lt * k, lane);
+        route_one_token(logits + t * E, E, k, sel + t * k, pw + t * k, s_exp + lt * k, lane, full);
     }
     __syncthreads();
     if (warp == 0) {
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(1024) route_group_small_kernel(
     float* __restrict__ pw, const float* __restrict__ x, int64_t H, __half* __restrict__ x16,
     int64_t Hp, int x16_mode, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ tiles, int32_t* __restrict__ active, int32_t* __restrict__ perm,
-    int32_t* __restrict__ inv, int tile_tokens, int32_t* __restrict__ ctrl) {
+    int32_t* __restrict__ inv, int tile_tokens, int full, int32_t* __restrict__ ctrl) {
     extern __shared__ int32_t smem[];
     if (blockIdx.x > 0) {
         if (x16) {
@@ -291,7 +304,7 @@ __global__ void __launch_bounds__(1024) route_group_small_kernel(
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
     for (int t = warp; t < T; t += nw)
         route_one_token(logits + int64_t(t) * E, E, k, sel + int64_t(t) * k, pw + int64_t(t) * k,
-                        s_exp + t * k, lane);
+                        s_exp + t * k, lane, full);
     __syncthreads();
     if (warp == 0) {
         for (int base = 0; base < slots; base += 32) {
@@ -500,7 +513,7 @@ cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, int x1
     note_launch(QMOE_KERNEL_ROUTE, s, true);
     route_kernel<<<dim3(unsigned(pl.route_chunks), unsigned(ysplit)), kRouteThreads, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
-        x16_mode, w.ctrl);
+        x16_mode, p.full_softmax, w.ctrl);
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
 }
@@ -524,7 +537,7 @@ cudaError_t launch_route_group_small(const Problem& p, const Plan& pl, const Wor
     route_group_small_kernel<<<unsigned(1 + conv), 1024, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, p.x, p.H, w.x16, pl.Hp,
         x16_mode, w.counts, w.offsets, w.tiles, w.active, w.perm, w.inv,
-        pl.tile_tokens, w.ctrl);
+        pl.tile_tokens, p.full_softmax, w.ctrl);
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
 }

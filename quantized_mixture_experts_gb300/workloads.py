@@ -153,3 +153,91 @@ def sample_tokens(logits_sel: np.ndarray, T: int, n: int, seed: int) -> np.ndarr
             first.setdefault(e, t)
     chosen.update(first.values())
     return np.array(sorted(chosen), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# Float (unquantized) MoE layer inputs
+# ---------------------------------------------------------------------------
+#
+# Recipe: activations fp32 ~ N(0, 1); router logits fp32 ~ N(0, sigma^2) with
+# the same tie redraw as above; expert weights fp32 ~ N(0, 1/fan_in) (fan_in =
+# H for FC1/FC3, I for FC2), so that every projection keeps unit scale; biases
+# fp32 ~ N(0, 0.1^2) when the workload has them.  Seeds are
+# ``workload_index * 1000 + tensor_id``.  The README names no benchmark shape;
+# the decode and prefill workloads reuse the QMoE layer's shapes with SwiGLU
+# from a separate FC3 (the README's default swiglu_fusion 0).
+
+
+@dataclasses.dataclass(frozen=True)
+class FloatWorkload:
+    name: str
+    index: int
+    input_shape: Tuple[int, ...]
+    hidden: int
+    inter: int
+    experts: int
+    k: int
+    activation: str              # relu | gelu | silu | swiglu | identity
+    swiglu_fusion: int = 0
+    fc3: bool = False            # FC3 weights present (needed by swiglu_fusion 0)
+    biases: bool = False
+    normalize: int = 0
+    logit_sigma: float = 1.0
+    alpha: float = 1.0
+    beta: float = 0.0
+    swiglu_limit: Optional[float] = None
+
+    @property
+    def tokens(self) -> int:
+        n = 1
+        for d in self.input_shape[:-1]:
+            n *= d
+        return n
+
+    @property
+    def fc1_rows(self) -> int:
+        fused = self.activation == "swiglu" and self.swiglu_fusion != 0
+        return (2 if fused else 1) * self.inter
+
+    def attrs(self) -> dict:
+        return dict(k=self.k, activation_type=self.activation, swiglu_fusion=self.swiglu_fusion,
+                    activation_alpha=self.alpha, activation_beta=self.beta,
+                    swiglu_limit=self.swiglu_limit,
+                    normalize_routing_weights=self.normalize)
+
+    def replace(self, **kw) -> "FloatWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+FLOAT_WORKLOADS = {
+    "float_tiny": FloatWorkload("float_tiny", 40, (16, 64), 64, 128, 4, 2, "relu", biases=True),
+    "float_decode": FloatWorkload("float_decode", 41, (8, 4096), 4096, 14336, 8, 2, "swiglu",
+                                  swiglu_fusion=0, fc3=True, logit_sigma=2.0),
+    "float_prefill": FloatWorkload("float_prefill", 42, (2, 2048, 4096), 4096, 14336, 8, 2,
+                                   "swiglu", swiglu_fusion=0, fc3=True, logit_sigma=2.0),
+}
+
+
+def make_float_inputs(wl: FloatWorkload, salt: int = 0) -> dict:
+    """Draw every input tensor of one float MoE call for workload ``wl``."""
+    T, H, I, E = wl.tokens, wl.hidden, wl.inter, wl.experts
+    fake = Workload(wl.name, wl.index, wl.input_shape, H, I, E, wl.k, 4, 0, "relu",
+                    logit_sigma=wl.logit_sigma)
+
+    def normal(tid, shape, sd):
+        g = _rng(fake, tid, salt)
+        return (g.standard_normal(shape, dtype=np.float32) * np.float32(sd))
+
+    out = dict(
+        input=_rng(fake, 1, salt).standard_normal(wl.input_shape, dtype=np.float32),
+        router_probs=_logits(fake, T, salt),
+        fc1_experts_weights=normal(3, (E, wl.fc1_rows, H), 1.0 / np.sqrt(H)),
+        fc2_experts_weights=normal(5, (E, H, I), 1.0 / np.sqrt(max(I, 1))))
+    if wl.fc3:
+        out["fc3_experts_weights"] = normal(9, (E, I, H), 1.0 / np.sqrt(H))
+    if wl.biases:
+        out["fc1_experts_bias"] = normal(4, (E, wl.fc1_rows), 0.1)
+        out["fc2_experts_bias"] = normal(6, (E, H), 0.1)
+        if wl.fc3:
+            out["fc3_experts_bias"] = normal(10, (E, I), 0.1)
+    return out
