@@ -3,6 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl reference]
 
+The float_* workloads measure the float MoE layer of the same library
+(moe_forward / moe_forward_hostio) in the same way, under the metric
+"MoE layer tokens/sec".
+
 One step is one full qmoe_forward call (routing, grouping, FC1 + activation,
 FC2, combine) over one batch of the workload's tokens, with inputs and
 weights resident in HBM.  `value` is whole-job tokens/s.  `e2e` measures the
@@ -34,12 +38,17 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from quantized_mixture_experts_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+from quantized_mixture_experts_gb300.workloads import (  # noqa: E402
+    FLOAT_WORKLOADS, WORKLOADS, make_float_inputs, make_inputs)
 
 METRIC = "QMoE layer tokens/sec"
 UNIT = "tokens/s"
 DEFAULT_STEPS = {"tiny": 2000, "decode": 8000, "prefill": 100, "many_small": 1000,
-                 "large_e": 100}
+                 "large_e": 100, "float_tiny": 2000, "float_decode": 1000, "float_prefill": 40,
+                 "float_prefill_e4": 100}
+FLOAT_METRIC = "MoE layer tokens/sec"
+# dense TF32 / dense BF16 tensor throughput, nominal (1.1 and 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -401,15 +410,245 @@ def run_gpu(args, wl):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------
+# Float MoE layer (moe_forward)
+# ----------------------------------------------------------------------------
+
+F_OPTIONAL = ("fc1_experts_bias", "fc2_experts_bias", "fc3_experts_weights", "fc3_experts_bias")
+
+
+def float_config(wl):
+    return {"workload": f"MoE {wl.name}", "input_shape": list(wl.input_shape),
+            "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
+            "experts": wl.experts, "k": wl.k, "activation": wl.activation,
+            "swiglu_fusion": wl.swiglu_fusion, "fc3": wl.fc3, "biases": wl.biases,
+            "normalize_routing_weights": wl.normalize}
+
+
+def float_fc1_rows(wl):
+    """Weight rows FC1 (with FC3) reads per expert."""
+    paired = wl.activation == "swiglu" or (wl.activation == "silu" and wl.fc3)
+    return (2 if paired else 1) * wl.inter
+
+
+def float_oracle(wl, inp, tok, cores):
+    import oracle
+    return oracle.moe(inp["input"], inp["router_probs"], inp["fc1_experts_weights"],
+                      inp["fc2_experts_weights"], fc1_bias=inp.get("fc1_experts_bias"),
+                      fc2_bias=inp.get("fc2_experts_bias"), fc3_w=inp.get("fc3_experts_weights"),
+                      fc3_bias=inp.get("fc3_experts_bias"), tokens=tok, nthreads=cores,
+                      **wl.attrs())
+
+
+def run_reference_float(args, wl):
+    if _env_int("RANK", 0) != 0:
+        return
+    inp = make_float_inputs(wl)
+    cores = os.cpu_count() or 1
+    sample = min(wl.tokens, 16)
+    rng = np.random.default_rng(7)
+    times = []
+    for step in range(args.warmup + args.steps):
+        tok = np.sort(rng.choice(wl.tokens, size=sample, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        float_oracle(wl, inp, tok, cores)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = sample * len(times) / total
+    line = {"impl": "reference", "metric": FLOAT_METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": float_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, sample),
+                             "kind": "oracle",
+                             "sample": f"{sample} of {wl.tokens} tokens per step, seeded"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_float(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import quantized_mixture_experts_gb300 as q
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    q.load()
+
+    inp = make_float_inputs(wl, salt=rank)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    opt = {k: t.get(k) for k in F_OPTIONAL}
+    attrs = q.make_moe_attrs(**wl.attrs())
+    fc1_shape = tuple(t["fc1_experts_weights"].shape)
+    path = q.moe_choose_path(wl.input_shape, fc1_shape, attrs)
+    ws = q.alloc_workspace(q.moe_workspace_size(wl.input_shape, fc1_shape, attrs), dev)
+    y = torch.empty_like(t["input"])
+    sel = torch.empty((wl.tokens, wl.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q.moe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"],
+                      t["fc2_experts_weights"], attrs=attrs, output=y, workspace=ws,
+                      topk_idx=sel, stream=stream, **opt)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    err = q.moe_get_device_error(ws, stream)
+    touched = int(torch.unique(sel).numel())
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = q.launch_count()
+    q.profile_begin(q.KERNEL_FC1)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    n_launch, fc1_ms = q.profile_end()
+    launches = q.launch_count() - launches0
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    value = wl.tokens * args.steps * world / (elapsed_ms / 1e3)
+
+    hx = torch.from_numpy(inp["input"]).pin_memory()
+    hl = torch.from_numpy(inp["router_probs"]).pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    ws_io = q.alloc_workspace(q.moe_workspace_size(wl.input_shape, fc1_shape, attrs,
+                                                   hostio=True), dev)
+    e2e_steps = max(1, min(args.steps, 1000))
+
+    def step_io():
+        q.moe_forward_hostio(hx, hl, t["fc1_experts_weights"], t["fc2_experts_weights"], hy,
+                             attrs=attrs, workspace=ws_io, stream=stream, **opt)
+        stream.synchronize()
+
+    for _ in range(3):
+        step_io()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_io()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    e2e_value = wl.tokens * e2e_steps * world / e2e_s
+    if not np.array_equal(hy.numpy(), y.cpu().numpy()):
+        raise RuntimeError("host-IO output differs from the device-resident output")
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peaks = measured_peaks()
+    avg_ms = fc1_ms / max(1, n_launch)
+    slots = wl.tokens * wl.k
+    # decode-sized batches stream the touched experts' fp32 weights; large ones are
+    # bound by the TF32 tensor cores
+    weight_bytes = float_fc1_rows(wl) * wl.hidden * 4 * touched
+    flops = 2.0 * slots * float_fc1_rows(wl) * wl.hidden
+    bound = "hbm" if flops / weight_bytes < 200 else "tensor"
+    if bound == "hbm":
+        algo = weight_bytes + slots * wl.hidden * 4
+        achieved = algo / (avg_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    else:
+        algo = flops
+        achieved = algo / (avg_ms / 1e3) / 1e12
+        bf16 = peaks["bf16_tflops_sustained"] if args.steps * avg_ms > 1000 else peaks["bf16_tflops"]
+        peak = bf16 * TF32_PER_BF16
+        unit = "TFLOP/s"
+    files = ["moe_float.cu", "ptx.cuh"]
+    traffic = ncu_traffic(f"float_fc1_{wl.name}.md", files)
+    cfg = float_config(wl)
+    cfg.update({"path": {q.MOE_PATH_GROUPED: "grouped", q.MOE_PATH_GENERIC: "generic"}.get(
+        path, str(path)), "touched_experts": touched,
+        "l2": ("weights of touched experts exceed the 129 MB L2; no flush"
+               if weight_bytes > L2_BYTES else "L2 flush not applied"),
+        "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+        "logits_sigma": wl.logit_sigma, "device_error": err})
+    line = {
+        "metric": FLOAT_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32",
+        "data": "synthetic (seeded; random fp32 weights)", "config": cfg,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak if peak else None, "traffic": traffic,
+                     "kernel": "FC1", "kernel_ms": avg_ms, "launches": n_launch,
+                     "algorithmic": algo,
+                     "peak_source": peaks["source"] + (
+                         "" if bound == "hbm" else " bf16 x nominal TF32/BF16 ratio")},
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(inp["input"].nbytes + inp["router_probs"].nbytes),
+                "d2h_bytes_per_step": int(inp["input"].nbytes), "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        sample = min(wl.tokens, 16)
+        tok = np.sort(np.random.default_rng(3).choice(wl.tokens, size=sample,
+                                                      replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        float_oracle(wl, inp, tok, cores)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": sample / dt, "unit": UNIT, "cores": min(cores, sample),
+                                "kind": "oracle",
+                                "sample": f"{sample} of {wl.tokens} tokens, {dt:.2f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="decode",
+                    choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.workload in FLOAT_WORKLOADS:
+        fwl = FLOAT_WORKLOADS[args.workload]
+        if args.steps is None:
+            args.steps = 10 if args.impl == "reference" else DEFAULT_STEPS[fwl.name]
+        args.warmup = max(3, args.warmup)
+        if args.impl == "reference":
+            run_reference_float(args, fwl)
+        else:
+            run_gpu_float(args, fwl)
+        return
     wl = WORKLOADS[args.workload]
     if args.steps is None:
         args.steps = 10 if args.impl == "reference" else DEFAULT_STEPS[wl.name]

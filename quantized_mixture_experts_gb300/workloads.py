@@ -215,6 +215,10 @@ FLOAT_WORKLOADS = {
                                   swiglu_fusion=0, fc3=True, logit_sigma=2.0),
     "float_prefill": FloatWorkload("float_prefill", 42, (2, 2048, 4096), 4096, 14336, 8, 2,
                                    "swiglu", swiglu_fusion=0, fc3=True, logit_sigma=2.0),
+    # prefill-like load per expert (about 1024 routed rows) with 1.4 GB of weights, for
+    # counter captures that must stay small
+    "float_prefill_e4": FloatWorkload("float_prefill_e4", 43, (2048, 4096), 4096, 7168, 4, 2,
+                                      "swiglu", swiglu_fusion=0, fc3=True, logit_sigma=2.0),
 }
 
 
