@@ -6,6 +6,7 @@
 // packSize (w = (q - mid) * scale, low nibble first), attributeDescriptions
 // (ReLU, interleaved SwiGLU, alpha, beta, swiglu_limit), pass QMoE.MixStage.
 #include "qmoe_internal.h"
+#include "tma_host.h"
 
 namespace qmoe {
 namespace {
@@ -169,6 +170,37 @@ __global__ void combine_kernel(const float* __restrict__ slot_out, const float* 
     }
 }
 
+// Same sums for large batches: CTA (t, column block); each thread owns eight
+// adjacent outputs of token t (two float4), so the index math is per CTA and a
+// thread keeps 2 * k * splits loads in flight.  H % 8 == 0, 16-byte aligned rows.
+__global__ void combine_rows_kernel(const float* __restrict__ slot_out,
+                                    const float* __restrict__ pw, float* __restrict__ y, int H4,
+                                    int k, int splits, int64_t slots) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t t = blockIdx.x;
+    const int d4 = 2 * (blockIdx.y * blockDim.x + threadIdx.x);
+    if (d4 >= H4) return;
+    const float4* __restrict__ base =
+        reinterpret_cast<const float4*>(slot_out) + (t * k) * H4 + d4;
+    const int64_t sstride = slots * H4;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    for (int i = 0; i < k; ++i) {
+        const float w = __ldg(pw + t * k + i);
+        float4 p0 = __ldg(base + int64_t(i) * H4), p1 = __ldg(base + int64_t(i) * H4 + 1);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 q0 = __ldg(base + int64_t(i) * H4 + sp * sstride);
+            const float4 q1 = __ldg(base + int64_t(i) * H4 + sp * sstride + 1);
+            p0.x += q0.x; p0.y += q0.y; p0.z += q0.z; p0.w += q0.w;
+            p1.x += q1.x; p1.y += q1.y; p1.z += q1.z; p1.w += q1.w;
+        }
+        a0.x += w * p0.x; a0.y += w * p0.y; a0.z += w * p0.z; a0.w += w * p0.w;
+        a1.x += w * p1.x; a1.y += w * p1.y; a1.z += w * p1.z; a1.w += w * p1.w;
+    }
+    float4* o = reinterpret_cast<float4*>(y + t * H4 * 4) + d4;
+    o[0] = a0;
+    o[1] = a1;
+}
+
 unsigned blocks_for(int64_t n, int per) { return unsigned((n + per - 1) / per); }
 
 }  // namespace
@@ -250,6 +282,18 @@ cudaError_t launch_combine(const Problem& p, const Plan& pl, const Work& w, int 
                     (reinterpret_cast<uintptr_t>(w.slot_out) & 15) == 0;
     const int64_t n = vec ? p.T * (p.H / 4) : p.T * p.H;
     note_launch(QMOE_KERNEL_COMBINE, s, true);
+    if (vec && (p.H & 7) == 0 && p.T * (p.H / 8) >= int64_t(device_sm_count()) * 256 &&
+        p.T < (int64_t(1) << 31)) {
+        const int H4 = int(p.H / 4);
+        const int threads = H4 / 2 >= 256 ? 256 : 128;
+        const dim3 grid(unsigned(p.T), unsigned((H4 / 2 + threads - 1) / threads));
+        cudaError_t e = launch_dependent(combine_rows_kernel, grid, dim3(threads), 0, s,
+                                         static_cast<const float*>(w.slot_out),
+                                         static_cast<const float*>(w.pw), p.y, H4, int(p.k),
+                                         splits, pl.slots);
+        note_launch(QMOE_KERNEL_COMBINE, s, false);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const int threads = n < 152 * 256 ? 64 : 256;   // spread small batches over more SMs
     cudaError_t e = launch_dependent(combine_kernel, dim3(unsigned(blocks_for(n, threads))),
                                      dim3(threads), 0, s, static_cast<const float*>(w.slot_out),

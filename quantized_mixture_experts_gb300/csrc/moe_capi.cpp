@@ -74,7 +74,7 @@ qmoe_status make_fplan(const FProblem& p, FPlan* out) {
     q.max_tiles = grouped ? (q.slots + kFTileTokens - 1) / kFTileTokens + p.E : 0;
     q.srows = grouped ? round_up(q.slots, 16) + 16 : 0;
     q.bmax = int(std::min<int64_t>(kFTileTokens, round_up(std::max<int64_t>(q.slots, 1), 16)));
-    q.fc2_splits = grouped ? moe_fc2_splits(p, q.slots) : 1;
+    q.fc2_splits = grouped ? moe_fc2_splits(p, q.slots, moe_cta_group(q)) : 1;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;

@@ -35,27 +35,41 @@ constexpr unsigned kFull = 0xffffffffu;
 // ---------------------------------------------------------------------------
 // Activations (README Attributes.activation_type, swiglu_fusion)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float sigm(float v) { return __fdividef(1.f, 1.f + __expf(-v)); }
+// sigmoid(v) = 1 / (1 + exp(-v)); the Fast form uses the identity
+// sigmoid(v) = (1 + tanh(v/2)) / 2 with the hardware tanh approximation (relative
+// error near 2^-11, the size of the TF32 rounding its result then takes).
+template <bool Fast>
+__device__ __forceinline__ float sigm(float v) {
+    if constexpr (Fast) {
+        float t;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * v));
+        return fmaf(0.5f, t, 0.5f);
+    } else {
+        return __fdividef(1.f, 1.f + __expf(-v));
+    }
+}
 
+template <bool Fast>
 __device__ __forceinline__ float act_single(int act, float h) {
     switch (act) {
         case MOE_ACT_RELU: return fmaxf(h, 0.f);
         case MOE_ACT_GELU: return 0.5f * h * erfcf(-h * 0.70710678118654752f);   // h * Phi(h)
-        case MOE_ACT_SILU: return h * sigm(h);
+        case MOE_ACT_SILU: return h * sigm<Fast>(h);
         default: return h;                                                       // identity
     }
 }
 
 // Activations of two projections: SiLU(g) * u, or SwiGLU g*sigmoid(alpha*g)*(u+beta)
 // after the optional clamp (gate from above, linear branch on both sides).
+template <bool Fast>
 __device__ __forceinline__ float act_pair(int act, float g, float u, float alpha, float beta,
                                           int has_limit, float limit) {
-    if (act == MOE_ACT_SILU) return g * sigm(g) * u;
+    if (act == MOE_ACT_SILU) return g * sigm<Fast>(g) * u;
     if (has_limit) {
         g = fminf(g, limit);
         u = fminf(fmaxf(u, -limit), limit);
     }
-    return g * sigm(alpha * g) * (u + beta);
+    return g * sigm<Fast>(alpha * g) * (u + beta);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -115,10 +129,10 @@ __global__ void moe_generic_fc1_kernel(FProblem p, const int32_t* __restrict__ p
         }
         g = warp_sum(g) + b0;
         u = warp_sum(u) + b1;
-        g = act_pair(p.act, g, u, p.alpha, p.beta, p.has_limit, p.limit);
+        g = act_pair<false>(p.act, g, u, p.alpha, p.beta, p.has_limit, p.limit);
     } else {
         for (int64_t kk = lane; kk < p.H; kk += 32) g += xt[kk] * r0[kk];
-        g = act_single(p.act, warp_sum(g) + b0);
+        g = act_single<false>(p.act, warp_sum(g) + b0);
     }
     if (lane == 0) act[pos * p.I + j] = g;
 }
@@ -178,19 +192,22 @@ __global__ void moe_gather_kernel(const float4* __restrict__ x, int64_t H4,
     }
 }
 
-constexpr int kFM = 128;                       // weight rows per MMA tile (M)
+constexpr int kFM = 128;                       // weight rows per CTA per MMA tile
 constexpr int kFMaxN = 256;                    // token rows per tile (MMA N upper bound)
 constexpr int kFK = 32;                        // K per stage: 32 fp32 = one 128-byte row
-constexpr uint32_t kFATile = kFM * 128;        // one weight tile per stage
+constexpr uint32_t kFATile = kFM * 128;        // one CTA's weight tile per stage
 constexpr uint32_t kFABytes = 2 * kFATile;
+constexpr int kFBBox = 32;                     // token rows per TMA box (CTA pairs)
 constexpr int kFMaxStages = 8;
-constexpr int kFEpiWarps = 8;
+constexpr int kFEpiWarps = 16;                 // 4 per TMEM lane quadrant
+constexpr int kFChunk = 16;                    // accumulator columns per TMEM load
 constexpr int kFThreads = 32 * (2 + kFEpiWarps);
 constexpr uint64_t kFDrainWaitNs = 200000000ull;
 
 struct FtcArgs {
     CUtensorMap tm0;         // weight rows {K, rows, E}, boxes {32, 128, 1}, 128-byte swizzle
     CUtensorMap tm1;         // second projection of a pair (same layout)
+    CUtensorMap tm_b;        // CTA pairs: token rows {32, srows, K/32}, boxes {32, 32, 1}
     const float* xs;         // token rows, K-blocked [K/32][srows][32], pre-swizzled TF32
     int64_t srows;
     const int32_t* tiles;    // header + (expert, first sorted row, rows, 0)
@@ -221,6 +238,25 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Every thread of both CTAs of the pair (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA 0 of the cluster.
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(ptx::smem_u32(p)), "r"(0));
+    return r;
+}
+
 // Shared-memory descriptor of a K-major operand with the 128-byte swizzle:
 // 128-byte rows, 8-row atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
@@ -238,55 +274,95 @@ __device__ __forceinline__ uint32_t tf32_idesc(int m, int n) {
            (uint32_t(m >> 4) << 24);
 }
 
+// One MMA.  With CTA pairs (issued by CTA 0) A is M = 256 rows, 128 from each
+// CTA's shared memory at the same offset, B is N rows, N/2 from each CTA, and
+// each CTA's tensor memory receives its 128 rows of D.
+template <int kCta>
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (kCta == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-        ::"r"(ptx::smem_u32(bar))
-        : "memory");
+// Arrive on `bar` when the issuing thread's MMAs complete: in this CTA, or (CTA
+// pairs, both = true) at the same offset in both CTAs.
+template <int kCta>
+__device__ __forceinline__ void mma_commit(uint64_t* bar, bool both) {
+    if constexpr (kCta == 2) {
+        if (both)
+            asm volatile(
+                "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                " [%0], %1;" ::"r"(ptx::smem_u32(bar)), "h"(uint16_t(3))
+                : "memory");
+        else
+            asm volatile(
+                "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                ::"r"(ptx::smem_u32(bar))
+                : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+            ::"r"(ptx::smem_u32(bar))
+            : "memory");
+    }
 }
 
+// Tiled 3-D load into this CTA's shared memory, completion counted on the
+// barrier at shared::cluster address `bar` (CTA pairs: CTA 0's barrier).
+template <int kCta>
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, int32_t z, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(ptx::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(ptx::smem_u32(bar))
-        : "memory");
+                                            int32_t y, int32_t z, uint32_t bar) {
+    if constexpr (kCta == 2)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];"
+            ::"r"(ptx::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];"
+            ::"r"(ptx::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+            : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
+// 16 consecutive accumulator columns of this thread's TMEM lane; `wait` = false
+// leaves the wait to a later tmem_wait() so that two loads overlap.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 struct FItem {
     int e, row0, rows, n0, nt, kb0, kb1, sp;
 };
 
-// Work item i: batches of gm row pairs; inside a batch token tile by token
-// tile, then row pair, then K split.
+// Work item i: batches of gm row groups; inside a batch token tile by token
+// tile, then row group, then K split.  A row group is 128 * kCta units of a
+// paired activation (gate and linear tiles) or 256 * kCta rows otherwise.
+template <int kCta>
 __device__ __forceinline__ FItem ft_item(const FtcArgs& a, int64_t i, int ntiles, int nkb) {
     const int64_t per_batch = int64_t(ntiles) * a.gm * a.splits;
     const int pg = int(i / per_batch);
@@ -300,18 +376,17 @@ __device__ __forceinline__ FItem ft_item(const FtcArgs& a, int64_t i, int ntiles
     it.e = t[0];
     it.row0 = t[1];
     it.rows = t[2];
-    it.n0 = (pg * a.gm + pm) * (a.paired ? kFM : 2 * kFM);
-    it.nt = (it.rows + 15) & ~15;
+    it.n0 = (pg * a.gm + pm) * (a.paired ? kFM * kCta : 2 * kFM * kCta);
+    it.nt = kCta == 2 ? (it.rows + 31) & ~31 : (it.rows + 15) & ~15;
     it.kb0 = it.sp * a.kb_per_split;
     it.kb1 = min(nkb, it.kb0 + a.kb_per_split);
     return it;
 }
 
-// Address of element (row, column j) of a K-blocked, swizzled activation layout.
-__device__ __forceinline__ int64_t kblocked_index(int64_t j, int64_t row, int phase, int64_t srows) {
-    return ((j >> 5) * srows + row) * 32 + ((((j & 31) >> 2) ^ phase) << 2) + (j & 3);
-}
-
+// kCta = 1: one CTA per item.  kCta = 2: a cluster of two CTAs per item; CTA 0
+// issues the MMAs (cta_group::2), both CTAs load their halves of A and B with
+// completion on CTA 0's barriers, and MMA completions are multicast to both.
+template <int kCta>
 __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_constant__ FtcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -325,25 +400,34 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stages = a.stages;
+    const uint32_t rank = kCta == 2 ? cluster_rank() : 0u;
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(&load_full[s], 1);
             ptx::mbar_init(&load_empty[s], 1);
         }
         ptx::mbar_init(&acc_full, 1);
-        ptx::mbar_init(&acc_empty, kFEpiWarps);
+        ptx::mbar_init(&acc_empty, kFEpiWarps * kCta);
         ptx::mbar_init(&drain_bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(ptx::smem_u32(&tmem_base_s)), "r"(512)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (kCta == 2) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(ptx::smem_u32(&tmem_base_s)), "r"(512)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(ptx::smem_u32(&tmem_base_s)), "r"(512)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kCta == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     // the next kernel in the stream may start its prologue
     ptx::griddep_launch_dependents();
@@ -352,17 +436,23 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
     const int64_t items = int64_t(ntiles) * a.n_pairs * a.splits;
     const int nkb = int(a.K / kFK);
     const uint32_t sbase = ptx::smem_u32(smem);
+    const int64_t first = blockIdx.x / kCta, step = gridDim.x / kCta;
+    // this CTA's first weight row of tile t of an item starting at n0
+    const int tile_stride = a.paired ? 0 : kFM * kCta;
+    const int row_off = kFM * int(rank);
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             ptx::prefetch_tmap(&a.tm0);
             if (a.paired) ptx::prefetch_tmap(&a.tm1);
+            if (kCta == 2) ptx::prefetch_tmap(&a.tm_b);
         }
         uint32_t it = 0, sl = 0, ph = 0;
         bool ok = true;
-        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
-            const FItem w = ft_item(a, i, ntiles, nkb);
+        for (int64_t i = first; i < items && ok; i += step) {
+            const FItem w = ft_item<kCta>(a, i, ntiles, nkb);
+            const int nbox = (w.nt / 2 + kFBBox - 1) / kFBBox;   // CTA pairs: B boxes per CTA
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                 if (!ptx::mbar_wait(&load_empty[sl], ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
@@ -370,14 +460,25 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
                 }
                 if (lane == 0) {
                     uint8_t* sp = smem + size_t(sl) * a.stage_bytes;
-                    ptx::mbar_arrive_expect_tx(&load_full[sl], kFABytes + uint32_t(w.nt) * 128u);
-                    tma_load_3d(sp, &a.tm0, kb * kFK, w.n0, w.e, &load_full[sl]);
-                    if (a.paired)
-                        tma_load_3d(sp + kFATile, &a.tm1, kb * kFK, w.n0, w.e, &load_full[sl]);
-                    else
-                        tma_load_3d(sp + kFATile, &a.tm0, kb * kFK, w.n0 + kFM, w.e, &load_full[sl]);
-                    ptx::bulk_g2s(sp + kFABytes, a.xs + (int64_t(kb) * a.srows + w.row0) * kFK,
-                                  uint32_t(w.nt) * 128u, &load_full[sl]);
+                    const uint32_t fb = kCta == 2 ? leader_addr(&load_full[sl])
+                                                  : ptx::smem_u32(&load_full[sl]);
+                    if (leader)
+                        ptx::mbar_arrive_expect_tx(
+                            &load_full[sl],
+                            kCta == 2 ? 2u * (kFABytes + uint32_t(nbox) * kFBBox * 128u)
+                                      : kFABytes + uint32_t(w.nt) * 128u);
+                    tma_load_3d<kCta>(sp, &a.tm0, kb * kFK, w.n0 + row_off, w.e, fb);
+                    tma_load_3d<kCta>(sp + kFATile, a.paired ? &a.tm1 : &a.tm0, kb * kFK,
+                                      w.n0 + tile_stride + row_off, w.e, fb);
+                    if constexpr (kCta == 2) {
+                        const int r0 = w.row0 + int(rank) * (w.nt / 2);
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_3d<2>(sp + kFABytes + b * (kFBBox * 128), &a.tm_b, 0,
+                                           r0 + b * kFBBox, kb, fb);
+                    } else {
+                        ptx::bulk_g2s(sp + kFABytes, a.xs + (int64_t(kb) * a.srows + w.row0) * kFK,
+                                      uint32_t(w.nt) * 128u, &load_full[sl]);
+                    }
                 }
                 __syncwarp();
                 if (++sl == uint32_t(stages)) { sl = 0; ph ^= 1u; }
@@ -386,83 +487,90 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
         if (!ok && lane == 0) {
             atomicCAS(a.err, 0, int32_t(QMOE_DEVERR_TIMEOUT));
             abort_flag = 1;
-            // wait (bounded) for the copies still in flight before leaving
-            for (uint32_t j = it > uint32_t(stages) ? it - stages : 0; j < it; ++j) {
-                volatile int never = 0;
-                ptx::mbar_wait(&load_full[j % stages], (j / stages) & 1u, kFDrainWaitNs, &never);
-            }
+            // wait (bounded) for the copies still in flight before leaving; with CTA
+            // pairs they complete on CTA 0's barriers, and the final cluster barrier
+            // keeps CTA 1 resident until CTA 0 has drained
+            if (leader)
+                for (uint32_t j = it > uint32_t(stages) ? it - stages : 0; j < it; ++j) {
+                    volatile int never = 0;
+                    ptx::mbar_wait(&load_full[j % stages], (j / stages) & 1u, kFDrainWaitNs, &never);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------- MMA issuer -------------------------------
-        uint32_t sl = 0, ph = 0, item_it = 0;
-        bool ok = true, issued = false;
-        for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
-            const FItem w = ft_item(a, i, ntiles, nkb);
-            if (!ptx::mbar_wait(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            ++item_it;
-            tc_fence_after();
-            const uint32_t idesc = tf32_idesc(kFM, w.nt);
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                if (!ptx::mbar_wait(&load_full[sl], ph, a.wait_ns, &abort_flag)) {
+        if (leader) {
+            uint32_t sl = 0, ph = 0, item_it = 0;
+            bool ok = true, issued = false;
+            for (int64_t i = first; i < items && ok; i += step) {
+                const FItem w = ft_item<kCta>(a, i, ntiles, nkb);
+                if (!ptx::mbar_wait(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
+                ++item_it;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sa = sbase + sl * a.stage_bytes;
-                    const uint32_t sb = sa + kFABytes;
-#pragma unroll
-                    for (int kk = 0; kk < kFK / 8; ++kk) {   // K = 8 per MMA (32 bytes)
-                        const uint64_t bd = kmajor_sw128_desc(sb + 32u * kk);
-#pragma unroll
-                        for (int t = 0; t < 2; ++t)
-                            mma_tf32(tmem_base + uint32_t(t * kFMaxN),
-                                     kmajor_sw128_desc(sa + uint32_t(t) * kFATile + 32u * kk), bd,
-                                     idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                const uint32_t idesc = tf32_idesc(kFM * kCta, w.nt);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!ptx::mbar_wait(&load_full[sl], ph, a.wait_ns, &abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(&load_empty[sl]);
-                    issued = true;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = sbase + sl * a.stage_bytes;
+                        const uint32_t sb = sa + kFABytes;
+#pragma unroll
+                        for (int kk = 0; kk < kFK / 8; ++kk) {   // K = 8 per MMA (32 bytes)
+                            const uint64_t bd = kmajor_sw128_desc(sb + 32u * kk);
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+                                mma_tf32<kCta>(tmem_base + uint32_t(t * kFMaxN),
+                                               kmajor_sw128_desc(sa + uint32_t(t) * kFATile + 32u * kk),
+                                               bd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit<kCta>(&load_empty[sl], true);
+                        issued = true;
+                    }
+                    __syncwarp();
+                    if (++sl == uint32_t(stages)) { sl = 0; ph ^= 1u; }
                 }
+                if (!ok) break;
+                if (lane == 0) mma_commit<kCta>(&acc_full, true);
                 __syncwarp();
-                if (++sl == uint32_t(stages)) { sl = 0; ph ^= 1u; }
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(&acc_full);
+            if (!ok && lane == 0) {
+                atomicCAS(a.err, 0, int32_t(QMOE_DEVERR_TIMEOUT));
+                abort_flag = 1;
+            }
+            if (lane == 0 && issued) {
+                mma_commit<kCta>(&drain_bar, false);
+                volatile int never = 0;
+                ptx::mbar_wait(&drain_bar, 0, kFDrainWaitNs, &never);
+            }
             __syncwarp();
         }
-        if (!ok && lane == 0) {
-            atomicCAS(a.err, 0, int32_t(QMOE_DEVERR_TIMEOUT));
-            abort_flag = 1;
-        }
-        if (lane == 0 && issued) {
-            mma_commit(&drain_bar);
-            volatile int never = 0;
-            ptx::mbar_wait(&drain_bar, 0, kFDrainWaitNs, &never);
-        }
-        __syncwarp();
     } else {
         // -------------------------------- epilogue --------------------------------
-        const int ew = warp - 2;                   // 0..7
+        const int ew = warp - 2;                   // 0..15
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = ew >> 2;                  // token chunks half, half + 2, ...
+        const int cg = ew >> 2;                    // column chunks cg, cg + 4, ... of 16
+        const uint32_t empty_addr = kCta == 2 ? leader_addr(&acc_empty) : ptx::smem_u32(&acc_empty);
+        constexpr int kChunks = kFMaxN / (4 * kFChunk);   // chunks per warp
         uint32_t item_it = 0;
-        for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
-            const FItem w = ft_item(a, i, ntiles, nkb);
+        for (int64_t i = first; i < items; i += step) {
+            const FItem w = ft_item<kCta>(a, i, ntiles, nkb);
             const uint32_t aph = item_it & 1u;
             ++item_it;
-            // FC2: the slot of this lane's token row in each of the warp's chunks
-            int slot_c[kFMaxN / 64];
+            // FC2: lane l < 16 holds the slot of token row c0 + l of each of the warp's chunks
+            int slot_c[kChunks];
 #pragma unroll
-            for (int m = 0; m < kFMaxN / 64; ++m) {
-                const int col = (2 * m + half) * 32 + lane;
-                slot_c[m] = (!a.fc1 && col < w.rows) ? __ldg(a.perm + w.row0 + col) : 0;
+            for (int m = 0; m < kChunks; ++m) {
+                const int col = (cg + 4 * m) * kFChunk + lane;
+                slot_c[m] = (!a.fc1 && lane < kFChunk && col < w.rows) ? __ldg(a.perm + w.row0 + col) : 0;
             }
             // this lane's output rows and their biases
-            const int64_t j0 = int64_t(w.n0) + quad * 32 + lane;                 // tile 0
-            const int64_t j1 = a.paired ? j0 : j0 + kFM;                          // tile 1
+            const int64_t j0 = int64_t(w.n0) + row_off + quad * 32 + lane;      // tile 0
+            const int64_t j1 = j0 + tile_stride;                                 // tile 1
             const bool use_bias = a.fc1 || w.sp == 0;
             float bias0 = 0.f, bias1 = 0.f;
             if (use_bias && a.bias0 && j0 < a.N) bias0 = __ldg(a.bias0 + w.e * a.b0_es + j0 * a.b0_js);
@@ -471,6 +579,11 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
             } else if (use_bias && a.bias0 && j1 < a.N) {
                 bias1 = __ldg(a.bias0 + w.e * a.b0_es + j1 * a.b0_js);
             }
+            // FC1: element (token row c0 + q, unit j) of the K-blocked output sits at
+            // rowbase(j) + q * 32 + ((chunk(j) ^ (q & 7)) << 2) for 16-aligned c0
+            float* const ob0 = a.act_out + ((j0 >> 5) * a.srows + w.row0) * 32 + (j0 & 3);
+            float* const ob1 = a.act_out + ((j1 >> 5) * a.srows + w.row0) * 32 + (j1 & 3);
+            const int ch0 = int((j0 & 31) >> 2), ch1 = int((j1 & 31) >> 2);
             if (!ptx::mbar_wait(&acc_full, aph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     atomicCAS(a.err, 0, int32_t(QMOE_DEVERR_TIMEOUT));
@@ -481,39 +594,41 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
             tc_fence_after();
             const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16);
 #pragma unroll
-            for (int m = 0; m < kFMaxN / 64; ++m) {
-                const int c0 = (2 * m + half) * 32;
+            for (int m = 0; m < kChunks; ++m) {
+                const int c0 = (cg + 4 * m) * kFChunk;
                 if (c0 >= w.nt) break;
-                float v0[32], v1[32];
-                tmem_ld32(tq + uint32_t(c0), v0);
-                tmem_ld32(tq + uint32_t(kFMaxN + c0), v1);
+                float v0[kFChunk], v1[kFChunk];
+                tmem_ld16(tq + uint32_t(c0), v0);
+                tmem_ld16(tq + uint32_t(kFMaxN + c0), v1);
+                tmem_wait();
                 if (a.fc1) {
+                    float* const p0 = ob0 + int64_t(c0) * 32;
+                    float* const p1 = ob1 + int64_t(c0) * 32;
                     if (a.paired) {
                         if (j0 < a.N) {
 #pragma unroll
-                            for (int q = 0; q < 32; ++q)
+                            for (int q = 0; q < kFChunk; ++q)
                                 if (c0 + q < w.rows)
-                                    a.act_out[kblocked_index(j0, w.row0 + c0 + q, (c0 + q) & 7, a.srows)] =
-                                        to_tf32(act_pair(a.act, v0[q] + bias0, v1[q] + bias1, a.alpha,
-                                                         a.beta, a.has_limit, a.limit));
+                                    p0[q * 32 + ((ch0 ^ (q & 7)) << 2)] =
+                                        to_tf32(act_pair<true>(a.act, v0[q] + bias0, v1[q] + bias1,
+                                                               a.alpha, a.beta, a.has_limit, a.limit));
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
+                        for (int q = 0; q < kFChunk; ++q) {
                             if (c0 + q >= w.rows) break;
-                            const int64_t row = w.row0 + c0 + q;
                             if (j0 < a.N)
-                                a.act_out[kblocked_index(j0, row, (c0 + q) & 7, a.srows)] =
-                                    to_tf32(act_single(a.act, v0[q] + bias0));
+                                p0[q * 32 + ((ch0 ^ (q & 7)) << 2)] =
+                                    to_tf32(act_single<true>(a.act, v0[q] + bias0));
                             if (j1 < a.N)
-                                a.act_out[kblocked_index(j1, row, (c0 + q) & 7, a.srows)] =
-                                    to_tf32(act_single(a.act, v1[q] + bias1));
+                                p1[q * 32 + ((ch1 ^ (q & 7)) << 2)] =
+                                    to_tf32(act_single<true>(a.act, v1[q] + bias1));
                         }
                     }
                 } else {
                     float* outp = a.slot_out + int64_t(w.sp) * a.slots * a.N;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) {
+                    for (int q = 0; q < kFChunk; ++q) {
                         const int slot = __shfl_sync(kFull, slot_c[m], q);
                         if (c0 + q < w.rows) {
                             if (j0 < a.N) outp[int64_t(slot) * a.N + j0] = v0[q] + bias0;
@@ -524,17 +639,29 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty);
+            if (lane == 0) {
+                if constexpr (kCta == 2)   // CTA 0's barrier counts both CTAs' epilogues
+                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                                 ::"r"(empty_addr) : "memory");
+                else
+                    ptx::mbar_arrive(&acc_empty);
+            }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kCta == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(512)
-                     : "memory");
+    if (warp == 1) {
+        if constexpr (kCta == 2)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(512)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(512)
+                         : "memory");
+    }
 }
 
 // Weight rows as a 3-D tensor {K, rows, E} of fp32 with the given row and
@@ -548,10 +675,17 @@ bool encode_rows(CUtensorMap* map, const float* base, int64_t K, int64_t rows, i
                           CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-int ring_stages(int bmax) {
-    const uint32_t stage = kFABytes + uint32_t(bmax) * 128u;
-    const int n = int((225u * 1024u) / stage);
+// Stages of the load ring that fit in shared memory.
+int ring_stages(uint32_t stage_bytes) {
+    const int n = int((225u * 1024u) / stage_bytes);
     return std::max(2, std::min(kFMaxStages, n));
+}
+
+// Token rows one CTA holds per stage: the whole tile, or half of it in boxes of
+// kFBBox rows for CTA pairs.
+uint32_t b_rows_per_cta(int bmax, int cta) {
+    if (cta == 1) return uint32_t(bmax);
+    return uint32_t((bmax / 2 + kFBBox - 1) / kFBBox * kFBBox);
 }
 
 }  // namespace
@@ -561,20 +695,29 @@ bool moe_grouped_shape_ok(const FProblem& p) {
            p.T * p.k <= (int64_t(1) << 30);
 }
 
-// Split-K factor of the grouped FC2: the count s that minimises the rounds of
-// work units per SM times the K blocks per unit (ties to the smaller s), with
-// the touched experts estimated from the slot count.
-int moe_fc2_splits(const FProblem& p, int64_t slots) {
-    const int64_t sms = device_sm_count();
-    const int64_t tiles = std::min<int64_t>(p.E, slots) + slots / kFTileTokens;
-    const int64_t items = tiles * ((p.H + 2 * kFM - 1) / (2 * kFM));
+// CTAs per work item: pairs (cta_group::2) once token tiles are large enough
+// that the shared-memory traffic per MMA matters; single CTAs for few tokens.
+int moe_cta_group(const FPlan& pl) { return pl.bmax >= 128 ? 2 : 1; }
+
+// Split-K factor of the grouped FC2: the count s that minimises the estimated
+// time, rounds of work units per SM times the K blocks of a unit (about 0.7 us
+// each, tensor- or HBM-bound alike) plus the partial rows every split writes
+// and the combine reads back (ties to the smaller s).  The token tiles are
+// estimated from the slot count.
+int moe_fc2_splits(const FProblem& p, int64_t slots, int cta) {
+    const int64_t sms = device_sm_count() / cta;
+    const int64_t tiles = std::max<int64_t>((slots + kFTileTokens - 1) / kFTileTokens,
+                                            std::min<int64_t>(p.E, slots));
+    const int64_t items = tiles * ((p.H + 2 * kFM * cta - 1) / (2 * kFM * cta));
     const int64_t nkb = p.I / kFK;
+    const double stage_us = 0.7, bytes_per_us = 6.5e6;
     int best = 1;
-    int64_t best_cost = -1;
+    double best_cost = -1.0;
     for (int s = 1; s <= 16 && s <= nkb; ++s) {
         const int64_t per = (nkb + s - 1) / s;
         if ((nkb + per - 1) / per != s) continue;   // every split non-empty
-        const int64_t cost = ((items * s + sms - 1) / sms) * per;
+        const double cost = double((items * s + sms - 1) / sms) * double(per) * stage_us +
+                            double(s) * double(slots) * double(p.H) * 8.0 / bytes_per_us;
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best = s;
@@ -657,6 +800,7 @@ cudaError_t launch_moe_grouped_fc(const FProblem& p, const FPlan& pl, const FWor
         a.slot_out = w.slot_out;
     }
     if (!ok) return cudaErrorInvalidValue;
+    const int cta = moe_cta_group(pl);
     const int nkb = int(a.K / kFK);
     a.kb_per_split = (nkb + a.splits - 1) / a.splits;
     a.fc1 = fc1 ? 1 : 0;
@@ -664,13 +808,13 @@ cudaError_t launch_moe_grouped_fc(const FProblem& p, const FPlan& pl, const FWor
     a.tiles = w.tiles;
     a.perm = w.perm;
     a.slots = pl.slots;
-    const int64_t rows_per_item = a.paired ? kFM : 2 * kFM;
+    const int64_t rows_per_item = (a.paired ? kFM : 2 * kFM) * cta;
     a.n_pairs = int((a.N + rows_per_item - 1) / rows_per_item);
     a.gm = 1;
     for (int g = 8; g > 1; --g)
         if (a.n_pairs % g == 0) { a.gm = g; break; }
-    a.stages = ring_stages(pl.bmax);
-    a.stage_bytes = kFABytes + uint32_t(pl.bmax) * 128u;
+    a.stage_bytes = kFABytes + b_rows_per_cta(pl.bmax, cta) * 128u;
+    a.stages = ring_stages(a.stage_bytes);
     a.act = p.act;
     a.alpha = p.alpha;
     a.beta = p.beta;
@@ -679,15 +823,54 @@ cudaError_t launch_moe_grouped_fc(const FProblem& p, const FPlan& pl, const FWor
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
     const size_t smem = 1024 + size_t(a.stages) * a.stage_bytes;
-    cudaError_t e = cudaFuncSetAttribute(moe_tf32_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
     const int64_t items_max = pl.max_tiles * a.n_pairs * a.splits;
-    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
+    cudaError_t e;
     note_launch(fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2, s, true);
-    moe_tf32_kernel<<<grid, kFThreads, smem, s>>>(a);
+    if (cta == 2) {
+        // token rows through TMA: {32 floats, srows, K/32}, boxes of kFBBox rows, copied as
+        // stored (the rows carry their swizzle already)
+        const uint64_t dims[3] = {32, uint64_t(pl.srows), uint64_t(a.K / kFK)};
+        const uint64_t strides[2] = {128, uint64_t(pl.srows) * 128};
+        const uint32_t box[3] = {32, uint32_t(kFBBox), 1};
+        if (!encode_tmap_3d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.xs, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        if ((e = cudaFuncSetAttribute(moe_tf32_kernel<2>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
+            cudaSuccess)
+            return e;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kFThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * unsigned(device_sm_count() / 2));
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, moe_tf32_kernel<2>, &cfg) != cudaSuccess ||
+            clusters <= 0) {
+            cudaGetLastError();
+            clusters = device_sm_count() / 2;
+        }
+        clusters = int(std::max<int64_t>(1, std::min<int64_t>(items_max, clusters)));
+        cfg.gridDim = dim3(2 * unsigned(clusters));
+        e = cudaLaunchKernelEx(&cfg, moe_tf32_kernel<2>, a);
+    } else {
+        if ((e = cudaFuncSetAttribute(moe_tf32_kernel<1>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
+            cudaSuccess)
+            return e;
+        const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
+        moe_tf32_kernel<1><<<grid, kFThreads, smem, s>>>(a);
+        e = cudaSuccess;
+    }
     note_launch(fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2, s, false);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace qmoe

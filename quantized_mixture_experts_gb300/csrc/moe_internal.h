@@ -46,7 +46,8 @@ struct FWork {
 constexpr int kFTileTokens = 256;
 
 bool moe_grouped_shape_ok(const FProblem& p);
-int moe_fc2_splits(const FProblem& p, int64_t slots);
+int moe_cta_group(const FPlan& pl);
+int moe_fc2_splits(const FProblem& p, int64_t slots, int cta);
 cudaError_t launch_moe_generic_fc1(const FProblem& p, const FPlan& pl, const FWork& w,
                                    cudaStream_t s);
 cudaError_t launch_moe_generic_fc2(const FProblem& p, const FPlan& pl, const FWork& w,

@@ -82,6 +82,15 @@ SMALL = [
     FloatWorkload("decode_like", 60, (8, 512), 512, 1024, 8, 2, "swiglu", swiglu_fusion=0,
                   fc3=True, logit_sigma=2.0),
     FloatWorkload("odd_hidden_generic", 61, (20, 40), 40, 24, 3, 2, "gelu", biases=True),
+    # batches of 128+ routed rows run on CTA pairs (cta_group::2): every SwiGLU layout, an
+    # unpaired activation, ragged tiles and several tiles per expert
+    FloatWorkload("pair_interleaved", 64, (300, 64), 64, 160, 4, 2, "swiglu", swiglu_fusion=1,
+                  biases=True),
+    FloatWorkload("pair_concat_limit", 65, (200, 96), 96, 96, 4, 2, "swiglu", swiglu_fusion=2,
+                  alpha=1.3, beta=0.2, swiglu_limit=0.8, normalize=1),
+    FloatWorkload("pair_gelu_k1", 66, (260, 96), 96, 288, 8, 1, "gelu", biases=True),
+    FloatWorkload("pair_fc3_tiles", 67, (700, 128), 128, 96, 2, 1, "swiglu", swiglu_fusion=0,
+                  fc3=True, biases=True),
 ]
 
 
