@@ -3,8 +3,9 @@
 
 Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It is a ctypes wrapper over the plain
-double-precision C restatements in ``qmoe_oracle.c`` and ``moe_oracle.c``
-(the float MoE of the [MoE README]); it shares no code with
+double-precision C restatements in ``qmoe_oracle.c``, ``moe_oracle.c`` (the
+float MoE of the [MoE README]) and ``qkv_oracle.c`` (the RMSNorm + 4-bit
+Q/K/V projection of the [MatMulNBitsQkv manifest]); it shares no code with
 the CUDA library and never calls it.  The wrapper only marshals arrays and
 derives shapes ([QMoE manifest] derive.numTokens / derive.hiddenSize: the
 token count is the product of the leading input dimensions).
@@ -23,7 +24,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "qmoe_oracle.c"), os.path.join(_HERE, "moe_oracle.c")]
+_SRCS = [os.path.join(_HERE, f) for f in ("qmoe_oracle.c", "moe_oracle.c", "qkv_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +82,11 @@ def _load():
         lib.oracle_moe.argtypes = [P, I64, P, I64, P, P, P, P, P, P, I64, C, C, D, D, C, D,
                                    I64, C, P, I64, C, P, P, P, C]
         lib.oracle_moe.restype = C
+        lib.oracle_qkv_code.argtypes = [P, I64, I64, I64, I64]
+        lib.oracle_qkv_code.restype = C
+        lib.oracle_qkv.argtypes = [P, P, P, I64, I64, P, P, I64, P, P, P, P, I64, I64, D,
+                                   P, P, P, P, P]
+        lib.oracle_qkv.restype = C
         _lib = lib
         return lib
 
@@ -277,3 +283,51 @@ def moe(x, logits, fc1_w, fc2_w, *, k, fc1_bias=None, fc2_bias=None, fc3_w=None,
     if st != OK:
         raise ValueError(f"oracle_moe failed with {st}")
     return y, sel, w
+
+
+# --------------------------------------------------------------------------
+# RMSNorm + 4-bit Q/K/V projection  ([MatMulNBitsQkv manifest])
+# --------------------------------------------------------------------------
+
+QKV_EPSILON = 9.999999974752427e-7   # attributes.epsilon default
+
+
+def qkv_code(packed, n, k, K, block_size=32):
+    """Code of element (n, k) of a [N, kBlocks, blob] packed weight."""
+    lib = _load()
+    pk = _c(packed, np.uint8)
+    kblocks = (K + block_size - 1) // block_size
+    return lib.oracle_qkv_code(_ptr(pk), int(n), int(k), kblocks, block_size)
+
+
+def qkv(A, norm_scale, q_B, q_scales, k_B, k_scales, v_B, v_scales, *, skip=None,
+        block_size=32, epsilon=QKV_EPSILON, residual=False, normed=False):
+    """Q, K, V [rows, N] float64 for A [..., K] (leading dims flattened); with
+    residual=True also x = A + skip, with normed=True also the normalised rows."""
+    lib = _load()
+    a = _c(A, np.float64)
+    K = a.shape[-1]
+    a = a.reshape(-1, K)
+    rows = a.shape[0]
+    sk = None if skip is None else _c(skip, np.float64).reshape(-1, K)
+    g = _c(norm_scale, np.float64)
+    qb, kb, vb = (_c(t, np.uint8) for t in (q_B, k_B, v_B))
+    qs, ks, vs = (_c(t, np.float64) for t in (q_scales, k_scales, v_scales))
+    Nq, Nkv = qb.shape[0], kb.shape[0]
+    Q = np.zeros((rows, Nq))
+    Ko = np.zeros((rows, Nkv))
+    V = np.zeros((rows, Nkv))
+    res = np.zeros((rows, K)) if residual else None
+    nrm = np.zeros((rows, K)) if normed else None
+    st = lib.oracle_qkv(_ptr(a), None if sk is None else _ptr(sk), _ptr(g), rows, K,
+                        _ptr(qb), _ptr(qs), Nq, _ptr(kb), _ptr(ks), _ptr(vb), _ptr(vs), Nkv,
+                        int(block_size), float(epsilon), _ptr(Q), _ptr(Ko), _ptr(V),
+                        None if res is None else _ptr(res), None if nrm is None else _ptr(nrm))
+    if st != OK:
+        raise ValueError(f"oracle_qkv failed with {st}")
+    out = [Q, Ko, V]
+    if residual:
+        out.append(res)
+    if normed:
+        out.append(nrm)
+    return tuple(out)
