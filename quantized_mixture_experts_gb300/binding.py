@@ -1,4 +1,4 @@
-"""ctypes binding of the C ABI in include/qmoe.h and include/moe.h.
+"""ctypes binding of the C ABI in include/qmoe.h, include/moe.h and include/qkv.h.
 
 Argument marshalling only: every step of the layer runs in the CUDA library
 ``libqmoe_gb300.so``.  Tensors are torch CUDA tensors (torch supplies device
@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmoe_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "qmoe.h")
 MOE_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+QKV_HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "qkv.h")
 
 # qmoe_status
 OK, ERR_INVALID_ARGUMENT, ERR_NOT_SUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
@@ -77,6 +78,22 @@ class MoeAttrs(ctypes.Structure):
 # moe_activation / moe_path
 MOE_ACTIVATIONS = {"relu": 0, "gelu": 1, "silu": 2, "swiglu": 3, "identity": 4}
 MOE_PATH_AUTO, MOE_PATH_GROUPED, MOE_PATH_GENERIC = 0, 2, 3
+
+class QkvAttrs(ctypes.Structure):
+    """Mirror of qkv_attrs (same field order and C types)."""
+    _fields_ = [
+        ("K", ctypes.c_int64),
+        ("Nq", ctypes.c_int64),
+        ("Nkv", ctypes.c_int64),
+        ("block_size", ctypes.c_int64),
+        ("bits", ctypes.c_int32),
+        ("accuracy_level", ctypes.c_int32),
+        ("epsilon", ctypes.c_float),
+        ("path", ctypes.c_int32),
+    ]
+
+
+QKV_PATH_AUTO, QKV_PATH_DECODE, QKV_PATH_GENERIC = 0, 1, 3
 
 _lib = None
 
@@ -146,13 +163,24 @@ def load():
     lib.moe_forward_hostio.restype = ctypes.c_int
     lib.moe_get_device_error.argtypes = [P, P, ctypes.POINTER(I32)]
     lib.moe_get_device_error.restype = ctypes.c_int
+    PQ = ctypes.POINTER(QkvAttrs)
+    lib.qkv_attrs_default.argtypes = [PQ]
+    lib.qkv_attrs_default.restype = None
+    lib.qkv_workspace_size.argtypes = [PI64, I32, PQ, I32, ctypes.POINTER(SZ)]
+    lib.qkv_workspace_size.restype = ctypes.c_int
+    lib.qkv_choose_path.argtypes = [PI64, I32, PQ, I32, ctypes.POINTER(I32)]
+    lib.qkv_choose_path.restype = ctypes.c_int
+    lib.matmul_nbits_qkv.argtypes = [P, PI64, I32, P, P, P, PI64, P, PI64, P, PI64, P, PI64,
+                                     P, PI64, P, PI64, P, P, P, P, I32, PQ, P, SZ, P]
+    lib.matmul_nbits_qkv.restype = ctypes.c_int
     _lib = lib
     return lib
 
 
 def declared_functions() -> list:
-    """Names of the functions include/qmoe.h and include/moe.h declare."""
-    text = open(HEADER_PATH).read() + open(MOE_HEADER_PATH).read()
+    """Names of the functions include/qmoe.h, include/moe.h and include/qkv.h declare."""
+    text = (open(HEADER_PATH).read() + open(MOE_HEADER_PATH).read() +
+            open(QKV_HEADER_PATH).read())
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "while", "for", "switch")))
@@ -472,3 +500,68 @@ def moe_get_device_error(workspace, stream=None) -> int:
     _check(load().moe_get_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)),
            "moe_get_device_error")
     return code.value
+
+
+# --------------------------------------------------------------------------
+# RMSNorm + 4-bit Q/K/V projection (include/qkv.h)
+# --------------------------------------------------------------------------
+
+def make_qkv_attrs(K: int, Nq: int, Nkv: int, block_size: int = 32, bits: int = 4,
+                   accuracy_level: int = 0, epsilon: Optional[float] = None,
+                   path: int = QKV_PATH_AUTO) -> QkvAttrs:
+    a = QkvAttrs()
+    load().qkv_attrs_default(ctypes.byref(a))
+    a.K, a.Nq, a.Nkv, a.block_size = int(K), int(Nq), int(Nkv), int(block_size)
+    a.bits, a.accuracy_level = int(bits), int(accuracy_level)
+    if epsilon is not None:
+        a.epsilon = float(epsilon)
+    a.path = int(path)
+    return a
+
+
+def qkv_workspace_size(a_shape, attrs: QkvAttrs, dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().qkv_workspace_size(_shape(a_shape), len(a_shape), ctypes.byref(attrs),
+                                     _gmm_dtype(dtype), ctypes.byref(out)), "qkv_workspace_size")
+    return out.value
+
+
+def qkv_choose_path(a_shape, attrs: QkvAttrs, dtype) -> int:
+    out = ctypes.c_int32(0)
+    _check(load().qkv_choose_path(_shape(a_shape), len(a_shape), ctypes.byref(attrs),
+                                  _gmm_dtype(dtype), ctypes.byref(out)), "qkv_choose_path")
+    return out.value
+
+
+def matmul_nbits_qkv(A, norm_scale, q_B, q_scales, k_B, k_scales, v_B, v_scales, *, skip=None,
+                     residual=None, attrs: Optional[QkvAttrs] = None, outputs=None,
+                     workspace=None, stream=None, **attr_kwargs):
+    """RMSNorm + 4-bit Q/K/V projection (include/qkv.h matmul_nbits_qkv) on torch CUDA
+    tensors.  residual=True allocates the input_skip_bias_sum output (needs skip).
+    Returns (Q, K, V) or (Q, K, V, residual)."""
+    import torch
+    Kdim = A.shape[-1]
+    if attrs is None:
+        attrs = make_qkv_attrs(K=Kdim, Nq=q_B.shape[0], Nkv=k_B.shape[0], **attr_kwargs)
+    lead = tuple(A.shape[:-1])
+    if outputs is None:
+        outputs = (torch.empty(lead + (attrs.Nq,), dtype=A.dtype, device=A.device),
+                   torch.empty(lead + (attrs.Nkv,), dtype=A.dtype, device=A.device),
+                   torch.empty(lead + (attrs.Nkv,), dtype=A.dtype, device=A.device))
+    res = None
+    if residual is True:
+        res = torch.empty_like(A)
+    elif residual is not None and residual is not False:
+        res = residual
+    if workspace is None:
+        workspace = alloc_workspace(qkv_workspace_size(tuple(A.shape), attrs, A.dtype), A.device)
+    Q, Ko, V = outputs
+    st = load().matmul_nbits_qkv(
+        _ptr(A), _shape(A.shape), A.dim(), _ptr(skip), _ptr(norm_scale),
+        _ptr(q_B), _shape(q_B.shape), _ptr(q_scales), _shape(q_scales.shape),
+        _ptr(k_B), _shape(k_B.shape), _ptr(k_scales), _shape(k_scales.shape),
+        _ptr(v_B), _shape(v_B.shape), _ptr(v_scales), _shape(v_scales.shape),
+        _ptr(Q), _ptr(Ko), _ptr(V), _ptr(res), _gmm_dtype(A.dtype), ctypes.byref(attrs),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "matmul_nbits_qkv")
+    return (Q, Ko, V) if res is None else (Q, Ko, V, res)

@@ -1,0 +1,40 @@
+// Internal declarations of the RMSNorm + 4-bit Q/K/V projection
+// (com.microsoft.MatMulNBitsQkv manifest): the weight-streaming GEMV shared
+// with the decode path of the QMoE layer, and the validated problem.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qkv.h"
+#include "qmoe_internal.h"
+
+namespace qmoe {
+
+// Few-row GEMV over the three projections in one launch.  Weights [N_p, K/2]
+// bytes (the [N, kBlocks, 16] blobs read as rows), block-32 scales [N_p, K/32]
+// (fp32, or fp16 when scales_f16).  Activations: the normalised rows in fp16,
+// in the 4-bit operand order of the decode path (groups of eight stored as
+// 0,4,2,6,1,5,3,7 with the odd elements divided by 16), b_pitch halves apart.
+// Writes fp32 partial sums part[p][split][row][N_p].  Launched as a
+// programmatic dependent of the kernel that writes b_src.
+struct QkvGemvParams {
+    const uint8_t* w[3] = {nullptr, nullptr, nullptr};
+    const void* s[3] = {nullptr, nullptr, nullptr};
+    int64_t N[3] = {0, 0, 0};
+    int64_t K = 0;
+    int rows = 0;
+    bool scales_f16 = false;
+    const __half* b_src = nullptr;
+    int64_t b_pitch = 0;
+    float* part[3] = {nullptr, nullptr, nullptr};
+    int splits = 1;
+    int32_t* err = nullptr;
+};
+
+constexpr int kQkvDecodeRows = 16;   // rows the GEMV path takes
+
+bool qkv_gemv_shape_ok(int64_t K, bool scales_f16);
+int qkv_gemv_splits(const int64_t N[3], int64_t K);
+cudaError_t launch_qkv_gemv(const QkvGemvParams& p, cudaStream_t s);
+
+}  // namespace qmoe

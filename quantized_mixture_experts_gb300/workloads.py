@@ -245,3 +245,64 @@ def make_float_inputs(wl: FloatWorkload, salt: int = 0) -> dict:
         if wl.fc3:
             out["fc3_experts_bias"] = normal(10, (E, I), 0.1)
     return out
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm + 4-bit Q/K/V projection inputs
+# ---------------------------------------------------------------------------
+#
+# Recipe: A ~ N(0, 1) and skip ~ N(0, 0.5^2) in T1; norm_scale ~ U[0.5, 1.5];
+# packed weights uniform random bytes [N, kBlocks, 16]; block scales
+# ~ U[0.002, 0.01] in T1.  The manifest names no benchmark shape: the decode
+# workloads take a wide grouped-query attention projection (K 8192, 64 query
+# heads and 8 key/value heads of 128: Nq 8192, Nkv 1024) for 8 rows.
+
+
+@dataclasses.dataclass(frozen=True)
+class QkvWorkload:
+    name: str
+    index: int
+    input_shape: Tuple[int, ...]
+    K: int
+    Nq: int
+    Nkv: int
+    dtype: str = "float32"       # T1: float32 | float16
+    skip: bool = False
+    residual: bool = False
+
+    @property
+    def rows(self) -> int:
+        n = 1
+        for d in self.input_shape[:-1]:
+            n *= d
+        return n
+
+    @property
+    def kblocks(self) -> int:
+        return (self.K + 31) // 32
+
+
+QKV_WORKLOADS = {
+    "qkv_tiny": QkvWorkload("qkv_tiny", 70, (4, 256), 256, 128, 64, "float32", True, True),
+    "qkv_decode": QkvWorkload("qkv_decode", 71, (8, 8192), 8192, 8192, 1024, "float16"),
+    "qkv_decode_f32": QkvWorkload("qkv_decode_f32", 72, (8, 8192), 8192, 8192, 1024, "float32",
+                                  True, True),
+}
+
+
+def make_qkv_inputs(wl: QkvWorkload, salt: int = 0) -> dict:
+    """Draw every input tensor of one Q/K/V projection call for workload ``wl``."""
+    fake = Workload(wl.name, wl.index, wl.input_shape, wl.K, 1, 1, 1, 4, 0, "relu")
+    dt = np.float16 if wl.dtype == "float16" else np.float32
+
+    def g(tid):
+        return _rng(fake, tid, salt)
+
+    out = dict(A=g(1).standard_normal(wl.input_shape, dtype=np.float32).astype(dt),
+               norm_scale=g(2).uniform(0.5, 1.5, wl.K).astype(dt))
+    for i, (name, n) in enumerate((("q", wl.Nq), ("k", wl.Nkv), ("v", wl.Nkv))):
+        out[f"{name}_B"] = g(10 + i).integers(0, 256, (n, wl.kblocks, 16), dtype=np.uint8)
+        out[f"{name}_scales"] = g(20 + i).uniform(0.002, 0.01, (n, wl.kblocks)).astype(dt)
+    if wl.skip:
+        out["skip"] = (g(3).standard_normal(wl.input_shape, dtype=np.float32) * 0.5).astype(dt)
+    return out
