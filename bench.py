@@ -5,7 +5,8 @@
 
 The float_* workloads measure the float MoE layer of the same library
 (moe_forward / moe_forward_hostio) in the same way, under the metric
-"MoE layer tokens/sec".
+"MoE layer tokens/sec"; the qkv_* workloads measure the RMSNorm + 4-bit
+Q/K/V projection (matmul_nbits_qkv) under "QKV projection rows/sec".
 
 One step is one full qmoe_forward call (routing, grouping, FC1 + activation,
 FC2, combine) over one batch of the workload's tokens, with inputs and
@@ -39,13 +40,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from quantized_mixture_experts_gb300.workloads import (  # noqa: E402
-    FLOAT_WORKLOADS, WORKLOADS, make_float_inputs, make_inputs)
+    FLOAT_WORKLOADS, QKV_WORKLOADS, WORKLOADS, make_float_inputs, make_inputs, make_qkv_inputs)
 
 METRIC = "QMoE layer tokens/sec"
 UNIT = "tokens/s"
 DEFAULT_STEPS = {"tiny": 2000, "decode": 8000, "prefill": 100, "many_small": 1000,
                  "large_e": 100, "float_tiny": 2000, "float_decode": 1000, "float_prefill": 40,
-                 "float_prefill_e4": 100}
+                 "float_prefill_e4": 100, "qkv_tiny": 2000, "qkv_decode": 5000,
+                 "qkv_decode_f32": 5000, "qkv_decode_wide": 2000}
+QKV_METRIC = "QKV projection rows/sec"
 FLOAT_METRIC = "MoE layer tokens/sec"
 # dense TF32 / dense BF16 tensor throughput, nominal (1.1 and 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
@@ -184,6 +187,24 @@ def ncu_traffic(profile_name, kernel_files):
     return float(m.group(1))
 
 
+def kernel_pass(q, step, steps, kernel_id, before=None):
+    """Average device time of the launches of one kernel of the path, from CUDA
+    events recorded around those launches on the call stream, over a second pass of
+    the timed steps.  The events are kept out of the timed pass itself: recorded
+    between two launches they would stop the second from starting as a
+    programmatic dependent of the first, and so change the time being measured."""
+    import torch
+    torch.cuda.synchronize()
+    q.profile_begin(kernel_id)
+    for i in range(steps):
+        if before is not None:
+            before(i)
+        step()
+    torch.cuda.synchronize()
+    n, ms = q.profile_end()
+    return n, ms
+
+
 # ----------------------------------------------------------------------------
 # Reference arm: the CPU oracle
 # ----------------------------------------------------------------------------
@@ -306,7 +327,6 @@ def run_gpu(args, wl):
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = q.launch_count()
-    q.profile_begin(dominant)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid) as clocks:
         start.record(stream)
@@ -314,8 +334,8 @@ def run_gpu(args, wl):
             step()
         stop.record(stream)
         torch.cuda.synchronize(dev)
-    n_launch, fc1_ms = q.profile_end()
     launches = q.launch_count() - launches0
+    n_launch, fc1_ms = kernel_pass(q, step, min(args.steps, 1000), dominant)
     if world > 1:
         dist.barrier()
     elapsed_ms = start.elapsed_time(stop)
@@ -520,7 +540,6 @@ def run_gpu_float(args, wl):
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = q.launch_count()
-    q.profile_begin(q.KERNEL_FC1)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid) as clocks:
         start.record(stream)
@@ -528,8 +547,8 @@ def run_gpu_float(args, wl):
             step()
         stop.record(stream)
         torch.cuda.synchronize(dev)
-    n_launch, fc1_ms = q.profile_end()
     launches = q.launch_count() - launches0
+    n_launch, fc1_ms = kernel_pass(q, step, min(args.steps, 1000), q.KERNEL_FC1)
     elapsed_ms = start.elapsed_time(stop)
     if world > 1:
         tt = torch.tensor([elapsed_ms], device=dev)
@@ -629,16 +648,219 @@ def run_gpu_float(args, wl):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------
+# RMSNorm + 4-bit Q/K/V projection (matmul_nbits_qkv)
+# ----------------------------------------------------------------------------
+
+def qkv_config(wl):
+    return {"workload": f"MatMulNBitsQkv {wl.name}", "input_shape": list(wl.input_shape),
+            "rows": wl.rows, "K": wl.K, "Nq": wl.Nq, "Nkv": wl.Nkv, "T1": wl.dtype,
+            "skip": wl.skip, "residual": wl.residual, "bits": 4, "block_size": 32}
+
+
+def qkv_weight_bytes(wl):
+    """Packed codes + block scales of the three projections."""
+    n = wl.Nq + 2 * wl.Nkv
+    return n * wl.kblocks * 16 + n * wl.kblocks * (2 if wl.dtype == "float16" else 4)
+
+
+def qkv_oracle(inp, wl, cores):
+    import oracle
+    f = lambda k: None if k not in inp else inp[k].astype(np.float64)
+    return oracle.qkv(f("A"), f("norm_scale"), inp["q_B"], f("q_scales"), inp["k_B"],
+                      f("k_scales"), inp["v_B"], f("v_scales"), skip=f("skip"),
+                      residual=wl.residual)
+
+
+def run_reference_qkv(args, wl):
+    if _env_int("RANK", 0) != 0:
+        return
+    inp = make_qkv_inputs(wl)
+    times = []
+    for step in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        qkv_oracle(inp, wl, 1)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = wl.rows * len(times) / total
+    line = {"impl": "reference", "metric": QKV_METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": qkv_config(wl),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"all {wl.rows} rows per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_qkv(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import quantized_mixture_experts_gb300 as q
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    q.load()
+    inp = make_qkv_inputs(wl, salt=rank)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    dt = t["A"].dtype
+    attrs = q.make_qkv_attrs(K=wl.K, Nq=wl.Nq, Nkv=wl.Nkv)
+    path = q.qkv_choose_path(wl.input_shape, attrs, dt)
+    ws = q.alloc_workspace(q.qkv_workspace_size(wl.input_shape, attrs, dt), dev)
+    lead = tuple(wl.input_shape[:-1])
+    outs = (torch.empty(lead + (wl.Nq,), dtype=dt, device=dev),
+            torch.empty(lead + (wl.Nkv,), dtype=dt, device=dev),
+            torch.empty(lead + (wl.Nkv,), dtype=dt, device=dev))
+    res = torch.empty_like(t["A"]) if wl.residual else None
+    stream = torch.cuda.current_stream(dev)
+    # a buffer six times L2, rewritten between timed steps: the weights (tens of MB)
+    # would otherwise stay in the 129 MB L2 from one step to the next
+    flush = torch.empty(6 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        q.matmul_nbits_qkv(t["A"], t["norm_scale"], t["q_B"], t["q_scales"], t["k_B"],
+                           t["k_scales"], t["v_B"], t["v_scales"], skip=t.get("skip"),
+                           residual=res if res is not None else None, attrs=attrs,
+                           outputs=outs, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    # A decode-sized call is shorter than its host-side enqueue (argument marshalling,
+    # tensor-map encoding, three launches).  Each timed step therefore starts with an
+    # L2 flush long enough (about 130 us of device time) for the host to enqueue the
+    # whole call behind it, so that the events around the call see device time only.
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = q.launch_count()
+    with ClockSampler(uuid) as clocks:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step()
+            stops[i].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = q.launch_count() - launches0
+    n_launch, gemv_ms = kernel_pass(q, step, min(args.steps, 1000), q.KERNEL_FC1,
+                                    before=lambda i: flush.fill_(float(i)))
+    elapsed_ms = sum(a.elapsed_time(b) for a, b in zip(starts, stops))
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    value = wl.rows * args.steps * world / (elapsed_ms / 1e3)
+
+    # end to end: pinned host activations in, the three projections back, every step
+    hA = torch.from_numpy(inp["A"]).pin_memory()
+    hs = torch.from_numpy(inp["skip"]).pin_memory() if "skip" in inp else None
+    hq = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    dA = torch.empty_like(t["A"])
+    ds = torch.empty_like(t["skip"]) if hs is not None else None
+    e2e_steps = max(1, min(args.steps, 2000))
+
+    def step_io():
+        dA.copy_(hA, non_blocking=True)
+        if ds is not None:
+            ds.copy_(hs, non_blocking=True)
+        q.matmul_nbits_qkv(dA, t["norm_scale"], t["q_B"], t["q_scales"], t["k_B"], t["k_scales"],
+                           t["v_B"], t["v_scales"], skip=ds,
+                           residual=res if res is not None else None, attrs=attrs, outputs=outs,
+                           workspace=ws, stream=stream)
+        for h, o in zip(hq, outs):
+            h.copy_(o, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step_io()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_io()
+    e2e_s = time.perf_counter() - t0
+    e2e_value = wl.rows * e2e_steps * world / e2e_s
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    avg_ms = gemv_ms / max(1, n_launch)
+    algo = qkv_weight_bytes(wl) + wl.rows * wl.K * 2
+    achieved = algo / (avg_ms / 1e3) / 1e9
+    cfg = qkv_config(wl)
+    cfg.update({"path": {q.QKV_PATH_DECODE: "decode", q.QKV_PATH_GENERIC: "generic"}.get(path),
+                "l2": "a 774 MB buffer is rewritten before every timed step (outside the events)",
+                "timing": "events around each call, enqueued behind the flush (device time)",
+                "parallelism": f"replicas{world}" if world > 1 else "single GPU"})
+    h2d = int(inp["A"].nbytes + (inp["skip"].nbytes if "skip" in inp else 0))
+    d2h = int(sum(o.numel() * o.element_size() for o in outs))
+    line = {
+        "metric": QKV_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if wl.dtype == "float16" else "f32",
+        "data": "synthetic (seeded; random packed weights)", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic(f"qkv_gemv_{wl.name}.md", ["gemv_decode.cu", "ptx.cuh"]),
+                     "kernel": "QKV GEMV", "kernel_ms": avg_ms, "launches": n_launch,
+                     "algorithmic": algo, "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        qkv_oracle(inp, wl, 1)
+        dt_s = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": wl.rows / dt_s, "unit": "rows/s", "cores": 1,
+                                "kind": "oracle", "sample": f"all {wl.rows} rows, {dt_s:.2f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
-                    choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS) + sorted(QKV_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.workload in QKV_WORKLOADS:
+        qwl = QKV_WORKLOADS[args.workload]
+        if args.steps is None:
+            args.steps = 10 if args.impl == "reference" else DEFAULT_STEPS[qwl.name]
+        args.warmup = max(3, args.warmup)
+        if args.impl == "reference":
+            run_reference_qkv(args, qwl)
+        else:
+            run_gpu_qkv(args, qwl)
+        return
     if args.workload in FLOAT_WORKLOADS:
         fwl = FLOAT_WORKLOADS[args.workload]
         if args.steps is None:

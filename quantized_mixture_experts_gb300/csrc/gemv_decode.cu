@@ -21,6 +21,7 @@
 // epilogue and writes fp16 activations; FC2 writes fp32 per-slot partial
 // sums per K split, reduced in fixed order by the combine kernel.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "ptx.cuh"
@@ -720,10 +721,18 @@ struct QkvArgs {
     int64_t K;
     int rows, nkc, splits, cps, nsc;
     uint32_t stage_bytes, off_s, off_b, pitch_b, nstages, ssize;
-    float* part[3];             // [splits][rows][N_p]
+    float* part[3];             // [splits][rows][N_p] partial sums (splits > 1)
+    void* out[3];               // [rows][N_p] results, fp32 or fp16 (out_f16), splits == 1
+    int out_f16;
     int32_t* err;
     uint64_t wait_ns;
 };
+
+// Result element idx of projection p (K not split).
+__device__ __forceinline__ void qkv_store(const QkvArgs& a, int p, int64_t idx, float v) {
+    if (a.out_f16) static_cast<__half*>(a.out[p])[idx] = __float2half_rn(v);
+    else static_cast<float*>(a.out[p])[idx] = v;
+}
 
 template <bool SH>
 __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_constant__ QkvArgs a) {
@@ -917,6 +926,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
             if (lane == 0) ptx::mbar_arrive(&red_empty[rb_buf]);
         }
         const int64_t Np = a.N[p];
+        if (a.splits == 1) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = nt * 8 + 2 * c + q;
+                    if (n >= ne) continue;
+                    if (rg < Np) qkv_store(a, p, int64_t(n) * Np + rg, acc[nt][q]);
+                    if (rg8 < Np) qkv_store(a, p, int64_t(n) * Np + rg8, acc[nt][2 + q]);
+                }
+            continue;
+        }
         float* part = a.part[p] + int64_t(ks) * a.rows * Np;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -945,7 +966,9 @@ bool qkv_gemv_shape_ok(int64_t K, bool scales_f16) {
 }
 
 // Split K so that the units (projection x 128-row block x K split) spread evenly
-// over the SMs, as decode_fc2_splits does for the layer's FC2.
+// over the SMs: minimise the K chunks of the most loaded SM, counting 1.5 chunks
+// of fixed cost per unit (pipeline ramp, K-half hand-off, stores) and 2 chunks
+// for the partial-sum reduction that any split needs.
 int qkv_gemv_splits(const int64_t N[3], int64_t K) {
     const int64_t KC = int64_t(kChunkBytes) * 2;
     const int64_t nkc = (K + KC - 1) / KC;
@@ -958,7 +981,8 @@ int qkv_gemv_splits(const int64_t N[3], int64_t K) {
         const int64_t splits = (nkc + cps - 1) / cps;
         if ((nkc + splits - 1) / splits != cps) continue;   // same cps as the launch derives
         const int64_t units = n_rb * splits;
-        const double cost = double((units + sms - 1) / sms) * (double(cps) + 0.5);
+        const double cost = double((units + sms - 1) / sms) * (double(cps) + 1.5) +
+                            (splits > 1 ? 2.0 : 0.0);
         if (best_cost == 0.0 || cost < best_cost) {
             best_cost = cost;
             best = splits;
@@ -987,7 +1011,9 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
         a.N[p] = q.N[p];
         a.n_rb[p] = int((q.N[p] + kDecRows - 1) / kDecRows);
         a.part[p] = q.part[p];
+        a.out[p] = q.out[p];
     }
+    a.out_f16 = q.scales_f16 ? 1 : 0;
     a.b_src = q.b_src;
     a.b_pitch = q.b_pitch;
     a.K = q.K;
@@ -1014,8 +1040,15 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
     const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes + kDecRedBytes;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(a.units, device_sm_count())));
     auto kern = q.scales_f16 ? qkv_gemv_kernel<true> : qkv_gemv_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
+    // the shared-memory limit is raised once per kernel (not inside a stream capture)
+    static std::atomic<size_t> smem_set[2] = {{0}, {0}};
+    std::atomic<size_t>& cur = smem_set[q.scales_f16 ? 1 : 0];
+    cudaError_t e = cudaSuccess;
+    if (cur.load() < smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        cur.store(smem);
+    }
     note_launch(QMOE_KERNEL_FC1, s, true);
     e = launch_dependent(kern, dim3(grid), dim3(kDecThreads), smem, s, a);
     note_launch(QMOE_KERNEL_FC1, s, false);

@@ -1,5 +1,5 @@
 // RMSNorm + 4-bit Q/K/V projection (com.microsoft.MatMulNBitsQkv manifest):
-// the normalisation kernel, the partial-sum reduction, the scalar path and the
+// the normalisation kernels, the scalar path and the
 // host side of the C ABI (validation per attributeConstraints and
 // derive.weightShapeOk / scaleShapeOk / ioShapeOk / normContractOk, workspace
 // planning, dispatch).  The few-row projection runs in the weight-streaming
@@ -22,6 +22,35 @@ __device__ __forceinline__ float ld(const float* p, int64_t i) { return __ldg(p 
 __device__ __forceinline__ float ld(const __half* p, int64_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ void st(float* p, int64_t i, float v) { p[i] = v; }
 __device__ __forceinline__ void st(__half* p, int64_t i, float v) { p[i] = __float2half_rn(v); }
+
+// Eight consecutive elements (16-byte aligned) to / from fp32 registers.
+__device__ __forceinline__ void load8(const float* p, float* v) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __half* p, float* v) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(ptx::u32_as_h2(w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void store8(float* p, const float* v) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__half* p, const float* v) {
+    uint4 u;
+    u.x = ptx::h2_as_u32(__floats2half2_rn(v[0], v[1]));
+    u.y = ptx::h2_as_u32(__floats2half2_rn(v[2], v[3]));
+    u.z = ptx::h2_as_u32(__floats2half2_rn(v[4], v[5]));
+    u.w = ptx::h2_as_u32(__floats2half2_rn(v[6], v[7]));
+    *reinterpret_cast<uint4*>(p) = u;
+}
 
 // Position of element j in a row whose groups of eight are stored in the order
 // 0,4,2,6,1,5,3,7: the operand layout of the 4-bit decode GEMV, which pairs
@@ -70,6 +99,73 @@ __global__ void __launch_bounds__(kNormThreads) qkv_norm_kernel(
     }
 }
 
+// The same normalisation for rows that fit in registers: 512 threads, each owning
+// up to G groups of eight consecutive elements (16-byte loads for fp16, two for
+// fp32), one pass over global memory.  K % 8 == 0, K <= 512 * 8 * G, 16-byte
+// aligned rows.
+template <typename T, int G>
+__global__ void __launch_bounds__(512) qkv_norm_regs_kernel(
+    const T* __restrict__ A, const T* __restrict__ skip, const T* __restrict__ gamma, int64_t K,
+    float eps, T* __restrict__ residual, __half* __restrict__ n16, int64_t pitch16,
+    float* __restrict__ n32, int32_t* __restrict__ err) {
+    ptx::griddep_launch_dependents();
+    __shared__ float s_part[16];
+    const int64_t r = blockIdx.x;
+    if (r == 0 && threadIdx.x == 0 && err) err[0] = 0;
+    const int64_t ngroups = K / 8;
+    float x[G][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+        const int64_t grp = threadIdx.x + int64_t(i) * blockDim.x;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[i][e] = 0.f;
+        if (grp < ngroups) {
+            load8(A + r * K + grp * 8, x[i]);
+            if (skip) {
+                float y[8];
+                load8(skip + r * K + grp * 8, y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[i][e] += y[e];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[i][e], x[i][e], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(kFull, ss, off);
+    if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) tot += s_part[w];   // fixed order
+    const float inv = rsqrtf(tot / float(K) + eps);
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+        const int64_t grp = threadIdx.x + int64_t(i) * blockDim.x;
+        if (grp >= ngroups) continue;
+        if (residual) store8(residual + r * K + grp * 8, x[i]);
+        float g[8], v[8];
+        load8(gamma + grp * 8, g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = x[i][e] * inv * g[e];
+        if (n16) {
+            // operand order 0,4,2,6,1,5,3,7 with the odd elements divided by 16
+            const __half2 h0 = __floats2half2_rn(v[0], v[4]);
+            const __half2 h1 = __floats2half2_rn(v[2], v[6]);
+            const __half2 h2 = __floats2half2_rn(v[1] * 0.0625f, v[5] * 0.0625f);
+            const __half2 h3 = __floats2half2_rn(v[3] * 0.0625f, v[7] * 0.0625f);
+            uint4 u;
+            u.x = ptx::h2_as_u32(h0);
+            u.y = ptx::h2_as_u32(h1);
+            u.z = ptx::h2_as_u32(h2);
+            u.w = ptx::h2_as_u32(h3);
+            *reinterpret_cast<uint4*>(n16 + r * pitch16 + grp * 8) = u;
+        }
+        if (n32) store8(n32 + r * K + grp * 8, v);
+    }
+}
+
 struct Proj3 {
     const uint8_t* B[3];
     const void* S[3];
@@ -77,7 +173,8 @@ struct Proj3 {
     void* out[3];
 };
 
-// out_p[r, n] = sum over K splits of the GEMV's partial sums, in split order.
+// out_p[r, n] = sum over the K splits of the GEMV's partial sums, in split order
+// (every split's load issued before the sum).
 template <typename T>
 __global__ void qkv_reduce_kernel(Proj3 pj, const float* __restrict__ p0, const float* __restrict__ p1,
                                   const float* __restrict__ p2, int splits, int64_t rows) {
@@ -88,8 +185,15 @@ __global__ void qkv_reduce_kernel(Proj3 pj, const float* __restrict__ p0, const 
     if (p >= 3) return;
     const float* part = p == 0 ? p0 : (p == 1 ? p1 : p2);
     const int64_t stride = rows * pj.N[p];
-    float s = part[idx];
-    for (int sp = 1; sp < splits; ++sp) s += part[int64_t(sp) * stride + idx];
+    float s = 0.f;
+    for (int sp0 = 0; sp0 < splits; sp0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = sp0 + j < splits ? part[int64_t(sp0 + j) * stride + idx] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (sp0 + j < splits) s += v[j];
+    }
     st(static_cast<T*>(pj.out[p]), idx, s);
 }
 
@@ -193,6 +297,28 @@ bool shape3(const int64_t* s, int64_t a, int64_t b, int64_t c) {
 }
 bool shape2(const int64_t* s, int64_t a, int64_t b) { return s && s[0] == a && s[1] == b; }
 
+// The normalisation launch: the register form when the row fits (K % 8 == 0,
+// K <= 16384, 16-byte aligned tensors), else one strided CTA per row.
+template <typename T>
+cudaError_t launch_norm(const QkvProblem& p, const void* A, const void* skip, const void* gamma,
+                        void* residual, __half* n16, int64_t pitch16, float* n32, int32_t* err,
+                        cudaStream_t s) {
+    const unsigned rows = unsigned(p.rows);
+    const bool regs = p.K % 8 == 0 && p.K <= 512 * 8 * 4 && aligned16(A) && aligned16(skip) &&
+                      aligned16(gamma) && aligned16(residual);
+    note_launch(QMOE_KERNEL_ROUTE, s, true);
+    if (regs)
+        qkv_norm_regs_kernel<T, 4><<<rows, 512, 0, s>>>(
+            static_cast<const T*>(A), static_cast<const T*>(skip), static_cast<const T*>(gamma), p.K,
+            p.eps, static_cast<T*>(residual), n16, pitch16, n32, err);
+    else
+        qkv_norm_kernel<T><<<rows, kNormThreads, 0, s>>>(
+            static_cast<const T*>(A), static_cast<const T*>(skip), static_cast<const T*>(gamma), p.K,
+            p.eps, static_cast<T*>(residual), n16, pitch16, n32, err);
+    note_launch(QMOE_KERNEL_ROUTE, s, false);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, const void* skip,
                       const void* gamma, const Proj3& pj, void* residual, void* ws, cudaStream_t s) {
@@ -203,18 +329,16 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
     cudaError_t e;
     if (p.path == QKV_PATH_DECODE) {
         __half* n16 = reinterpret_cast<__half*>(base + q.off_n16);
-        note_launch(QMOE_KERNEL_ROUTE, s, true);
-        qkv_norm_kernel<T><<<rows, kNormThreads, 0, s>>>(
-            static_cast<const T*>(A), static_cast<const T*>(skip), static_cast<const T*>(gamma), p.K,
-            p.eps, static_cast<T*>(residual), n16, q.pitch16, nullptr, err);
-        note_launch(QMOE_KERNEL_ROUTE, s, false);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_norm<T>(p, A, skip, gamma, residual, n16, q.pitch16, nullptr, err, s)) !=
+            cudaSuccess)
+            return e;
         float* part = reinterpret_cast<float*>(base + q.off_part);
         QkvGemvParams g;
         for (int i = 0; i < 3; ++i) {
             g.w[i] = pj.B[i];
             g.s[i] = pj.S[i];
             g.N[i] = p.N[i];
+            g.out[i] = pj.out[i];
         }
         g.part[0] = part;
         g.part[1] = part + int64_t(q.splits) * p.rows * p.N[0];
@@ -227,6 +351,7 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
         g.splits = q.splits;
         g.err = err;
         if ((e = launch_qkv_gemv(g, s)) != cudaSuccess) return e;
+        if (q.splits == 1) return cudaSuccess;   // the GEMV wrote the results
         const int64_t total = p.rows * (p.N[0] + p.N[1] + p.N[2]);
         note_launch(QMOE_KERNEL_COMBINE, s, true);
         e = launch_dependent(qkv_reduce_kernel<T>, dim3(unsigned((total + 255) / 256)), dim3(256), 0,
@@ -236,12 +361,8 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
         note_launch(QMOE_KERNEL_COMBINE, s, false);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
-    note_launch(QMOE_KERNEL_ROUTE, s, true);
-    qkv_norm_kernel<T><<<rows, kNormThreads, 0, s>>>(
-        static_cast<const T*>(A), static_cast<const T*>(skip), static_cast<const T*>(gamma), p.K,
-        p.eps, static_cast<T*>(residual), nullptr, 0, n32, err);
-    note_launch(QMOE_KERNEL_ROUTE, s, false);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_norm<T>(p, A, skip, gamma, residual, nullptr, 0, n32, err, s)) != cudaSuccess)
+        return e;
     const int64_t warps = p.rows * (p.N[0] + p.N[1] + p.N[2]);
     note_launch(QMOE_KERNEL_FC1, s, true);
     qkv_generic_kernel<T><<<unsigned((warps + 7) / 8), 256, 0, s>>>(pj, n32, p.rows, p.K);

@@ -15,8 +15,10 @@ namespace qmoe {
 // (fp32, or fp16 when scales_f16).  Activations: the normalised rows in fp16,
 // in the 4-bit operand order of the decode path (groups of eight stored as
 // 0,4,2,6,1,5,3,7 with the odd elements divided by 16), b_pitch halves apart.
-// Writes fp32 partial sums part[p][split][row][N_p].  Launched as a
-// programmatic dependent of the kernel that writes b_src.
+// Writes the results out[p][row][N_p] in T1 (fp16 when scales_f16, as T1 is the
+// scales' type) when K is not split, else fp32 partial sums
+// part[p][split][row][N_p] for a reduction kernel.  Launched as a programmatic
+// dependent of the kernel that writes b_src.
 struct QkvGemvParams {
     const uint8_t* w[3] = {nullptr, nullptr, nullptr};
     const void* s[3] = {nullptr, nullptr, nullptr};
@@ -27,6 +29,7 @@ struct QkvGemvParams {
     const __half* b_src = nullptr;
     int64_t b_pitch = 0;
     float* part[3] = {nullptr, nullptr, nullptr};
+    void* out[3] = {nullptr, nullptr, nullptr};
     int splits = 1;
     int32_t* err = nullptr;
 };

@@ -254,8 +254,9 @@ def make_float_inputs(wl: FloatWorkload, salt: int = 0) -> dict:
 # Recipe: A ~ N(0, 1) and skip ~ N(0, 0.5^2) in T1; norm_scale ~ U[0.5, 1.5];
 # packed weights uniform random bytes [N, kBlocks, 16]; block scales
 # ~ U[0.002, 0.01] in T1.  The manifest names no benchmark shape: the decode
-# workloads take a wide grouped-query attention projection (K 8192, 64 query
-# heads and 8 key/value heads of 128: Nq 8192, Nkv 1024) for 8 rows.
+# workloads take grouped-query attention projections (K 8192 with 64 query
+# heads and 8 key/value heads of 128: Nq 8192, Nkv 1024; and K 16384 with 128
+# query heads) for 8 rows.
 
 
 @dataclasses.dataclass(frozen=True)
@@ -287,6 +288,10 @@ QKV_WORKLOADS = {
     "qkv_decode": QkvWorkload("qkv_decode", 71, (8, 8192), 8192, 8192, 1024, "float16"),
     "qkv_decode_f32": QkvWorkload("qkv_decode_f32", 72, (8, 8192), 8192, 8192, 1024, "float32",
                                   True, True),
+    # a wider model: K 16384, 128 query heads and 8 key/value heads of 128 (170 MB of codes
+    # and fp16 scales, larger than L2)
+    "qkv_decode_wide": QkvWorkload("qkv_decode_wide", 73, (8, 16384), 16384, 16384, 1024,
+                                   "float16"),
 }
 
 
