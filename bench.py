@@ -390,7 +390,7 @@ def run_gpu(args, wl):
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
         profile_name = "decode_fc1_decode.md"
-        files = ["gemv_decode.cu", "ptx.cuh"]
+        files = ["gemv_decode.cu", "decode_core.cuh", "ptx.cuh"]
     else:
         slots = wl.tokens * wl.k
         algo = fc1_flops(wl, slots)
@@ -822,7 +822,8 @@ def run_gpu_qkv(args, wl):
         "data": "synthetic (seeded; random packed weights)", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic(f"qkv_gemv_{wl.name}.md", ["gemv_decode.cu", "ptx.cuh"]),
+                     "traffic": ncu_traffic(f"qkv_gemv_{wl.name}.md",
+                                            ["qkv_gemv.cu", "decode_core.cuh", "ptx.cuh"]),
                      "kernel": "QKV GEMV", "kernel_ms": avg_ms, "launches": n_launch,
                      "algorithmic": algo, "peak_source": peaks["source"]},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
