@@ -238,25 +238,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Every thread of both CTAs of the pair (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address of the same shared-memory object in CTA 0 of the cluster.
-__device__ __forceinline__ uint32_t leader_addr(const void* p) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(ptx::smem_u32(p)), "r"(0));
-    return r;
-}
-
 // Shared-memory descriptor of a K-major operand with the 128-byte swizzle:
 // 128-byte rows, 8-row atoms 1024 bytes apart.
 __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
@@ -400,7 +381,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stages = a.stages;
-    const uint32_t rank = kCta == 2 ? cluster_rank() : 0u;
+    const uint32_t rank = kCta == 2 ? ptx::cluster_rank() : 0u;
     const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -427,7 +408,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
         }
     }
     tc_fence_before();
-    if constexpr (kCta == 2) cluster_sync(); else __syncthreads();
+    if constexpr (kCta == 2) ptx::cluster_sync(); else __syncthreads();
     tc_fence_after();
     // the next kernel in the stream may start its prologue
     ptx::griddep_launch_dependents();
@@ -460,7 +441,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
                 }
                 if (lane == 0) {
                     uint8_t* sp = smem + size_t(sl) * a.stage_bytes;
-                    const uint32_t fb = kCta == 2 ? leader_addr(&load_full[sl])
+                    const uint32_t fb = kCta == 2 ? ptx::leader_addr(&load_full[sl])
                                                   : ptx::smem_u32(&load_full[sl]);
                     if (leader)
                         ptx::mbar_arrive_expect_tx(
@@ -503,7 +484,8 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
             bool ok = true, issued = false;
             for (int64_t i = first; i < items && ok; i += step) {
                 const FItem w = ft_item<kCta>(a, i, ntiles, nkb);
-                if (!ptx::mbar_wait(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
+                // both CTAs' epilogues arrive here: acquire at cluster scope
+                if (!ptx::mbar_wait_cluster(&acc_empty, (item_it & 1u) ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -554,7 +536,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
         const int ew = warp - 2;                   // 0..15
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int cg = ew >> 2;                    // column chunks cg, cg + 4, ... of 16
-        const uint32_t empty_addr = kCta == 2 ? leader_addr(&acc_empty) : ptx::smem_u32(&acc_empty);
+        const uint32_t empty_addr = kCta == 2 ? ptx::leader_addr(&acc_empty) : ptx::smem_u32(&acc_empty);
         constexpr int kChunks = kFMaxN / (4 * kFChunk);   // chunks per warp
         uint32_t item_it = 0;
         for (int64_t i = first; i < items; i += step) {
@@ -641,8 +623,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
             __syncwarp();
             if (lane == 0) {
                 if constexpr (kCta == 2)   // CTA 0's barrier counts both CTAs' epilogues
-                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-                                 ::"r"(empty_addr) : "memory");
+                    ptx::mbar_arrive_cluster(empty_addr);
                 else
                     ptx::mbar_arrive(&acc_empty);
             }
@@ -650,7 +631,7 @@ __global__ void __launch_bounds__(kFThreads, 1) moe_tf32_kernel(const __grid_con
     }
 
     tc_fence_before();
-    if constexpr (kCta == 2) cluster_sync(); else __syncthreads();
+    if constexpr (kCta == 2) ptx::cluster_sync(); else __syncthreads();
     tc_fence_after();
     if (warp == 1) {
         if constexpr (kCta == 2)
