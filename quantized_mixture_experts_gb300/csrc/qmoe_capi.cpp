@@ -193,7 +193,9 @@ qmoe_status make_plan(const Problem& p, Plan* pl) {
     q.off_tiles = take(4 * size_t(kTileHeader + 4 * q.max_tiles));
     q.off_active = take(4 * E);
     const bool generic = p.path == QMOE_PATH_GENERIC;
-    q.off_x16 = take(generic ? 0 : 2 * size_t(p.T) * size_t(q.Hp));
+    // fp16 copy of x: the decode path's operand (the grouped path converts into
+    // its sorted rows directly)
+    q.off_x16 = take(p.path == QMOE_PATH_DECODE ? 2 * size_t(p.T) * size_t(q.Hp) : 0);
     const bool grouped = p.path == QMOE_PATH_GROUPED;
     q.off_xs16 = take(grouped ? 2 * size_t(q.srows) * size_t(q.Hp) : 0);
     q.off_act = take(generic ? 4 * slots * size_t(p.I)
@@ -284,14 +286,16 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
             return QMOE_OK;
         }
         case QMOE_PATH_GROUPED: {
-            // 4-bit: activations in the interleaved operand order of the nibble conversion
-            const int mode = p.bits == 4 ? 1 : 0;
+            // routing and grouping only: the sorted fp16 rows are converted from x directly
+            // (in the operand order of the nibble conversion for 4-bit weights)
+            Work wr = w;
+            wr.x16 = nullptr;
             if (small_route_ok(p, pl)) {
-                if ((e = launch_route_group_small(p, pl, w, mode, s)) != cudaSuccess)
+                if ((e = launch_route_group_small(p, pl, wr, 0, s)) != cudaSuccess)
                     return QMOE_ERR_CUDA;
             } else {
-                if ((e = launch_route(p, pl, w, mode, s)) != cudaSuccess) return QMOE_ERR_CUDA;
-                if ((e = launch_group(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_route(p, pl, wr, 0, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+                if ((e = launch_group(p, pl, wr, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
             if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;

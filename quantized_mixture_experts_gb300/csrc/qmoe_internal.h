@@ -90,7 +90,7 @@ struct Work {
     int32_t* inv;         // [T*k] slot -> sorted position
     int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, 0)
     int32_t* active;      // [E] experts with at least one slot, ascending
-    __half* x16;          // [T*Hp] fp16 copy of the activations
+    __half* x16;          // [T*Hp] fp16 copy of the activations (decode path)
     __half* xs16;         // grouped path: fp16 activations in expert-sorted slot order,
                           // K-blocked [Hp/64][srows][64] with the 128-byte swizzle applied
     void* act;            // FC1 output: fp16 [T*k, Ip] (decode), fp32 (generic), or fp16

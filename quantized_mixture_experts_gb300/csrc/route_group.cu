@@ -14,13 +14,14 @@
 
 #include <algorithm>
 
+#include "ptx.cuh"
 #include "qmoe_internal.h"
 #include "tma_host.h"
 
 namespace qmoe {
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 1024;   // 32 routing warps: two tokens each per chunk
 constexpr unsigned kFull = 0xffffffffu;
 
 // Total order of the selection: larger logit first, equal logits by lower index.
@@ -78,51 +79,53 @@ __device__ void route_one_token_any(const float* __restrict__ row, int E, int k,
     for (int i = lane; i < k; i += 32) pw[i] = expf(pw[i] - vmax) / part;
 }
 
-// Same selection for E <= 32 * kRouteRegs and k <= 32: the row is read once into
-// registers and round i's winner stays in lane i, so the rounds and the softmax
-// touch no memory.  The softmax sums in the same shuffle tree as the general form.
-constexpr int kRouteRegs = 8;
-__device__ void route_one_token(const float* __restrict__ row, int E, int k, int32_t* sel,
-                                float* pw, int32_t* s_exp, int lane, int full) {
-    if (E > 32 * kRouteRegs || k > 32) {
-        route_one_token_any(row, E, k, sel, pw, s_exp, lane, full);
-        return;
-    }
-    float v[kRouteRegs];
+// Order-preserving 32-bit key of a logit: key(a) > key(b) exactly when a > b
+// (-0 is taken as +0 so that equal logits stay equal; NaN is out of contract).
+// Every real key is above 0, which marks a removed entry.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v == 0.f) v = 0.f;
+    const uint32_t u = __float_as_uint(v);
+    return u ^ ((u >> 31) ? 0xFFFFFFFFu : 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return __uint_as_float((k >> 31) ? (k ^ 0x80000000u) : ~k);
+}
+
+// Same selection for E <= 32 * RR and k <= 32: the key of expert lane + 32 j
+// sits in slot j of the lane's registers, read once.  Round i takes the
+// largest remaining key over the warp (one max reduction), then the lowest
+// expert index holding it (one min reduction), so ties go to the lower index
+// as in the general form; the winner's lane marks it taken, and lane i keeps
+// round i's winner, so the rounds and the softmax touch no memory.  The
+// softmax sums in the same shuffle tree as the general form.
+template <int RR>
+__device__ __forceinline__ void route_one_token_regs(const float* __restrict__ row, int E, int k,
+                                                     int32_t* sel, float* pw, int32_t* s_exp,
+                                                     int lane, int full) {
+    uint32_t key[RR];
 #pragma unroll
-    for (int j = 0; j < kRouteRegs; ++j) v[j] = lane + 32 * j < E ? row[lane + 32 * j] : 0.f;
-    float prev_v = 0.f;
-    int prev_i = -1;
+    for (int j = 0; j < RR; ++j) key[j] = lane + 32 * j < E ? logit_key(row[lane + 32 * j]) : 0u;
+    uint32_t taken = 0;   // bit j: slot j already selected
     float vmax = 0.f;
     float mine_v = 0.f;   // lane i: the logit selected in round i
     int mine_i = -1;
     for (int i = 0; i < k; ++i) {
-        float best_v = 0.f;
-        int best_i = -1;
+        uint32_t bk = 0;
+        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < kRouteRegs; ++j) {
-            const int e = lane + 32 * j;
-            const bool after_prev = (prev_i < 0) || better(prev_v, prev_i, v[j], e);
-            if (e < E && after_prev && (best_i < 0 || better(v[j], e, best_v, best_i))) {
-                best_v = v[j];
-                best_i = e;
+        for (int j = 0; j < RR; ++j)
+            if (!((taken >> j) & 1u) && key[j] > bk) {   // strict: the lower slot wins a tie
+                bk = key[j];
+                bj = j;
             }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(kFull, best_v, off);
-            int oi = __shfl_xor_sync(kFull, best_i, off);
-            if (oi >= 0 && (best_i < 0 || better(ov, oi, best_v, best_i))) {
-                best_v = ov;
-                best_i = oi;
-            }
-        }
-        prev_v = best_v;
-        prev_i = best_i;
-        if (i == 0) vmax = best_v;
+        const uint32_t m = __reduce_max_sync(kFull, bk);
+        const int win = __reduce_min_sync(kFull, bk == m ? lane + 32 * bj : 0x7FFFFFFF);
+        if (lane == (win & 31)) taken |= 1u << (win >> 5);
+        const float wv = key_logit(m);
+        if (i == 0) vmax = wv;
         if (lane == i) {
-            mine_v = best_v;
-            mine_i = best_i;
+            mine_v = wv;
+            mine_i = win;
         }
     }
     // softmax over the k selected logits (or every logit), max subtracted first
@@ -131,8 +134,8 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
     if (full) {
         part = 0.f;
 #pragma unroll
-        for (int j = 0; j < kRouteRegs; ++j)
-            if (lane + 32 * j < E) part += expf(v[j] - vmax);
+        for (int j = 0; j < RR; ++j)
+            if (lane + 32 * j < E) part += expf(key_logit(key[j]) - vmax);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
@@ -142,6 +145,43 @@ __device__ void route_one_token(const float* __restrict__ row, int E, int k, int
         pw[lane] = mine_e / part;
     }
     __syncwarp();
+}
+
+// Routing of one token by one warp: the register form for E <= 256 and k <= 32
+// (as few register slots per lane as E needs), the general form otherwise.
+__device__ __forceinline__ void route_one_token(const float* __restrict__ row, int E, int k,
+                                                int32_t* sel, float* pw, int32_t* s_exp, int lane,
+                                                int full) {
+    if (k > 32 || E > 256) route_one_token_any(row, E, k, sel, pw, s_exp, lane, full);
+    else if (E <= 32) route_one_token_regs<1>(row, E, k, sel, pw, s_exp, lane, full);
+    else if (E <= 64) route_one_token_regs<2>(row, E, k, sel, pw, s_exp, lane, full);
+    else if (E <= 128) route_one_token_regs<4>(row, E, k, sel, pw, s_exp, lane, full);
+    else route_one_token_regs<8>(row, E, k, sel, pw, s_exp, lane, full);
+}
+
+// Eight activations of row t (columns 8g..8g+7) stored as fp16 in layout mode
+// `mode` (see convert_group).
+__device__ __forceinline__ void store_group(const float* v, int64_t t, int64_t g,
+                                            __half* __restrict__ x16, int64_t Hp, int mode) {
+    __half2 h[4];
+    if (mode == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[q], v[q + 4]);
+    } else if (mode == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int src = (q >> 1) + 2 * (q & 1);     // pairs (0,4),(2,6),(1,5),(3,7)
+            const float f = (src & 1) ? 0.0625f : 1.f;
+            h[q] = __floats2half2_rn(v[src] * f, v[src + 4] * f);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+    }
+    uint4 o;
+    o.x = ptx::h2_as_u32(h[0]); o.y = ptx::h2_as_u32(h[1]);
+    o.z = ptx::h2_as_u32(h[2]); o.w = ptx::h2_as_u32(h[3]);
+    reinterpret_cast<uint4*>(x16 + t * Hp)[g] = o;
 }
 
 // One group of eight activations of row t (columns 8g..8g+7), converted to fp16
@@ -191,61 +231,109 @@ __device__ __forceinline__ void convert_group(const float* __restrict__ x, int64
     reinterpret_cast<uint4*>(x16 + t * Hp)[g] = *reinterpret_cast<uint4*>(h);
 }
 
-// fp16 copy of rows [t0, t0+ntok) of the activations, groups of eight columns
-// [g_lo, g_hi), zero padded to Hp (see convert_group for the layout modes).
-// Thread tid of nthr takes a fixed group and every rows-per-pass-th row, so the
-// index arithmetic is one 32-bit division per thread.
-__device__ void convert_rows(const float* __restrict__ x, int64_t t0, int ntok, int64_t H,
-                             __half* __restrict__ x16, int64_t Hp, int mode, int64_t g_lo,
-                             int64_t g_hi, int tid, int nthr) {
-    const int width = int(g_hi - g_lo);
-    if (width <= 0) return;
+// fp16 copy of all T rows of the activations, zero padded to Hp (layout modes
+// as in convert_group): the groups of eight columns of every row, flattened
+// row-major, are taken in a grid-stride loop by `ncta` CTAs, two per thread
+// per pass with both loads issued before the conversions.
+__device__ void convert_all(const float* __restrict__ x, int64_t T, int64_t H,
+                            __half* __restrict__ x16, int64_t Hp, int mode, int cta, int ncta) {
+    const int64_t G8 = Hp / 8;
+    const int64_t total = T * G8;
     const bool vec = (H & 7) == 0 && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
-    if (width >= nthr) {
-        for (int r = 0; r < ntok; ++r)
-            for (int g = tid; g < width; g += nthr)
-                convert_group(x, t0 + r, g_lo + g, H, vec, x16, Hp, mode);
-        return;
+    const int64_t stride = int64_t(ncta) * blockDim.x;
+    for (int64_t f0 = int64_t(cta) * blockDim.x + threadIdx.x; f0 < total; f0 += 2 * stride) {
+        float v[2][8];
+        int64_t t[2], g[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int64_t f = f0 + q * stride;
+            t[q] = f / G8;
+            g[q] = f - t[q] * G8;
+            const float* __restrict__ xr = x + t[q] * H;
+            if (f < total && vec && g[q] * 8 < H) {
+                const float4 lo = reinterpret_cast<const float4*>(xr)[2 * g[q]];
+                const float4 hi = reinterpret_cast<const float4*>(xr)[2 * g[q] + 1];
+                v[q][0] = lo.x; v[q][1] = lo.y; v[q][2] = lo.z; v[q][3] = lo.w;
+                v[q][4] = hi.x; v[q][5] = hi.y; v[q][6] = hi.z; v[q][7] = hi.w;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    v[q][c] = (f < total && !vec && g[q] * 8 + c < H) ? xr[g[q] * 8 + c] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (f0 + q * stride < total) store_group(v[q], t[q], g[q], x16, Hp, mode);
     }
-    const int rpp = nthr / width;            // rows per pass
-    const int r0 = tid / width, g = tid - r0 * width;
-    if (r0 >= rpp) return;
-#pragma unroll 4
-    for (int r = r0; r < ntok; r += rpp) convert_group(x, t0 + r, g_lo + g, H, vec, x16, Hp, mode);
 }
 
-// Grid (chunks, conv_split).  CTA (c, 0) routes the chunk's tokens (one warp
-// per token), then warp 0 ranks the chunk's slots per expert (stable, in slot
-// order) and writes the chunk histogram.  Every CTA (c, y) also converts its
-// share of the chunk's activation columns to fp16.
+// Blocks of 32 slots of a routing chunk, and the largest per-block count table
+// (blocks x experts) the parallel ranking keeps in shared memory.
+constexpr int kRankCap = 8192;
+__host__ __device__ inline int rank_blocks(int k) { return (kRouteTokensPerChunk * k + 31) / 32; }
+__host__ __device__ inline bool rank_parallel(int E, int k) {
+    return int64_t(rank_blocks(k)) * E <= kRankCap && rank_blocks(k) <= kRouteThreads / 32;
+}
+
+// Grid chunks + conv CTAs.  CTA c < chunks routes chunk c's tokens (one warp
+// per token), then ranks the chunk's slots per expert (stable, in slot order)
+// and writes the chunk histogram: block b of 32 slots is ranked by warp b
+// (in-block ranks and counts), an exclusive scan over blocks per expert gives
+// each block's bases.  The other `conv` CTAs convert the activations to fp16
+// (convert_all) while the routing CTAs run.
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ sel,
     float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
     const float* __restrict__ x, int64_t H, __half* __restrict__ x16, int64_t Hp,
-    int x16_mode, int full, int32_t* __restrict__ ctrl) {
+    int x16_mode, int full, int32_t* __restrict__ ctrl, int chunks) {
+    if (int(blockIdx.x) >= chunks) {
+        convert_all(x, T, H, x16, Hp, x16_mode, int(blockIdx.x) - chunks, int(gridDim.x) - chunks);
+        return;
+    }
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;        // [E]
     int32_t* s_exp = smem + E;    // [chunk tokens * k]
+    int32_t* s_blk = s_exp + kRouteTokensPerChunk * k;   // [rank_blocks(k)][E] (parallel ranking)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = int64_t(blockIdx.x) * kRouteTokensPerChunk;
     const int ntok = int(T - t0 < kRouteTokensPerChunk ? T - t0 : kRouteTokensPerChunk);
-    if (x16) {
-        const int64_t G8 = Hp / 8;
-        const int64_t per = (G8 + gridDim.y - 1) / gridDim.y;
-        const int64_t g_lo = int64_t(blockIdx.y) * per;
-        const int64_t g_hi = g_lo + per < G8 ? g_lo + per : G8;
-        convert_rows(x, t0, ntok, H, x16, Hp, x16_mode, g_lo, g_hi, threadIdx.x, blockDim.x);
-    }
-    if (blockIdx.y != 0) return;
     if (blockIdx.x == 0 && threadIdx.x == 0 && ctrl) ctrl[0] = 0;
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    const bool par = rank_parallel(E, k);
+    const int nslots = ntok * k;
+    const int nblk = (nslots + 31) / 32;
+    if (par)
+        for (int j = threadIdx.x; j < nblk * E; j += blockDim.x) s_blk[j] = 0;
     for (int lt = warp; lt < ntok; lt += kRouteThreads / 32) {
         const int64_t t = t0 + lt;
         route_one_token(logits + t * E, E, k, sel + t * k, pw + t * k, s_exp + lt * k, lane, full);
     }
     __syncthreads();
-    if (warp == 0) {
-        const int nslots = ntok * k;
+    if (par) {
+        int32_t* rank_out = rank + t0 * k;
+        // in-block rank of each slot and the block's count per expert
+        int e = -1, r = 0;
+        if (warp < nblk) {
+            const int j = warp * 32 + lane;
+            e = j < nslots ? s_exp[j] : -1 - lane;   // distinct dummies
+            const unsigned mask = __match_any_sync(kFull, e);
+            r = __popc(mask & ((1u << lane) - 1u));
+            if (e >= 0 && lane == __ffs(mask) - 1) s_blk[warp * E + e] = __popc(mask);
+        }
+        __syncthreads();
+        // exclusive scan over blocks, per expert; the totals are the chunk histogram
+        for (int x = threadIdx.x; x < E; x += blockDim.x) {
+            int run = 0;
+            for (int b = 0; b < nblk; ++b) {
+                const int c = s_blk[b * E + x];
+                s_blk[b * E + x] = run;
+                run += c;
+            }
+            s_cnt[x] = run;
+        }
+        __syncthreads();
+        if (warp < nblk && e >= 0) rank_out[warp * 32 + lane] = s_blk[warp * E + e] + r;
+    } else if (warp == 0) {
         int32_t* rank_out = rank + t0 * k;
         for (int base = 0; base < nslots; base += 32) {
             const int j = base + lane;
@@ -391,9 +479,19 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(
         const bool on = (e < E) && (part < P) && (e - e0 < nthr / P);
         const int64_t c_lo = chunks * part / P, c_hi = chunks * (part + 1) / P;
         int32_t sum = 0;
-        if (on)
-            for (int64_t c = c_lo; c < c_hi; ++c) sum += hist[c * E + e];
-        if (on) s_part[part * E + e] = sum;
+        if (on) {
+            // eight loads in flight per batch
+            int64_t c = c_lo;
+            for (; c + 8 <= c_hi; c += 8) {
+                int32_t v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = hist[(c + q) * E + e];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sum += v[q];
+            }
+            for (; c < c_hi; ++c) sum += hist[c * E + e];
+            s_part[part * E + e] = sum;
+        }
     }
     __syncthreads();
     // Phase 2: exclusive scan over parts for each expert; totals.
@@ -415,8 +513,19 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(
         if (on) {
             const int64_t c_lo = chunks * part / P, c_hi = chunks * (part + 1) / P;
             int32_t run = s_part[part * E + e];
-            for (int64_t c = c_lo; c < c_hi; ++c) {
-                int32_t v = hist[c * E + e];
+            int64_t c = c_lo;
+            for (; c + 8 <= c_hi; c += 8) {   // batches of eight: loads first, then stores
+                int32_t v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = hist[(c + q) * E + e];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    hist[(c + q) * E + e] = run;
+                    run += v[q];
+                }
+            }
+            for (; c < c_hi; ++c) {
+                const int32_t v = hist[c * E + e];
                 hist[c * E + e] = run;
                 run += v;
             }
@@ -496,24 +605,26 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ sel,
 
 cudaError_t launch_route(const Problem& p, const Plan& pl, const Work& w, int x16_mode,
                          cudaStream_t s) {
-    const size_t smem = sizeof(int32_t) * (size_t(p.E) + size_t(kRouteTokensPerChunk) * p.k);
+    const size_t smem = sizeof(int32_t) * (size_t(p.E) + size_t(kRouteTokensPerChunk) * p.k +
+                                           (rank_parallel(int(p.E), int(p.k))
+                                                ? size_t(rank_blocks(int(p.k))) * p.E : 0));
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(route_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(smem));
         if (e != cudaSuccess) return e;
     }
-    // split the fp16 conversion of each chunk over enough CTAs to cover the GPU
-    // (at least 32 groups of eight columns per CTA)
-    int ysplit = 1;
+    // conversion CTAs: the SMs the routing CTAs leave (at least half of them), one
+    // 1024-thread CTA per SM
+    int conv = 0;
     if (w.x16) {
-        const int64_t want = (int64_t(4) * device_sm_count() + pl.route_chunks - 1) / pl.route_chunks;
-        ysplit = int(std::max<int64_t>(1, std::min<int64_t>(want, pl.Hp / 256)));
+        const int sms = device_sm_count();
+        conv = std::max(sms / 2, sms - int(std::min<int64_t>(pl.route_chunks, sms)));
     }
     note_launch(QMOE_KERNEL_ROUTE, s, true);
-    route_kernel<<<dim3(unsigned(pl.route_chunks), unsigned(ysplit)), kRouteThreads, smem, s>>>(
+    route_kernel<<<unsigned(pl.route_chunks + conv), kRouteThreads, smem, s>>>(
         p.logits, p.T, int(p.E), int(p.k), w.sel, w.pw, w.hist, w.rank, p.x, p.H, w.x16, pl.Hp,
-        x16_mode, p.full_softmax, w.ctrl);
+        x16_mode, p.full_softmax, w.ctrl, int(pl.route_chunks));
     note_launch(QMOE_KERNEL_ROUTE, s, false);
     return cudaGetLastError();
 }
