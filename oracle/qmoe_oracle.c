@@ -178,9 +178,9 @@ void oracle_dequant_rows(const uint8_t *packed, const float *scales, int64_t row
 }
 
 /*
- * [QMOE] description ("Routing uses the softmax over the selected top-k
- * logits") and attributeDescriptions.normalize_routing_weights (the same
- * softmax for either value of the attribute).  Selection i is the i-th
+ * [QMOE] description (the routing weights are a softmax taken over the k
+ * selected logits only) and attributeDescriptions.normalize_routing_weights
+ * (the same softmax for either value of the attribute).  Selection i is the i-th
  * largest logit; equal logits go to the lower expert index.  Then
  *   p_i = exp(l_i - l_max) / sum_j exp(l_j - l_max)  over the k selected.
  */

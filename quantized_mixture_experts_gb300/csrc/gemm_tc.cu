@@ -628,80 +628,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                      : "memory");
 }
 
-// The fp16 activations in expert-sorted slot order (row pos = token
-// perm[pos] / k), K-blocked [Hp/64][srows][64] with the 128-byte swizzle of the
-// row's position in its token tile applied: 16-byte chunk c of a 64-column
-// block is stored at c ^ ((pos - offsets[expert]) & 7).  Token tiles start at
-// multiples of their expert's first row plus multiples of 8, so a tile's rows
-// of one K block are one contiguous, already swizzled 128-byte-row block.
-//
-// Written straight from the fp32 input: `parts` warps per token (interleaved
-// passes of 128 groups of eight columns, four per lane) read the row once,
-// convert it to fp16 in the operand order `mode` (0 natural; 1 each group of
-// eight as 0,4,1,5,2,6,3,7, the pair order of the 4-bit conversion), and store
-// it at each of the token's k sorted positions.  Columns past H are zero.
-__global__ void sort_convert_kernel(const float* __restrict__ x, int64_t T, int64_t H,
-                                    int64_t Hp, int vec, int mode, int parts,
-                                    const int32_t* __restrict__ inv,
-                                    const int32_t* __restrict__ sel,
-                                    const int32_t* __restrict__ offsets, int k, int64_t srows,
-                                    uint4* __restrict__ xs16) {
-    constexpr int U = 4;
-    const int lane = threadIdx.x & 31;
-    const int64_t wpb = blockDim.x >> 5;
-    const int64_t nwarps = int64_t(gridDim.x) * wpb;
-    const int G8 = int(Hp / 8);
-    for (int64_t wi = int64_t(blockIdx.x) * wpb + (threadIdx.x >> 5); wi < T * parts; wi += nwarps) {
-        const int64_t t = wi / parts;
-        const int part = int(wi - t * parts);
-        // lane i: sorted position of the token's slot i (i < 32) and its swizzle phase
-        int my_pos = 0, my_ph = 0;
-        if (lane < k) {
-            my_pos = __ldg(inv + t * k + lane);
-            my_ph = (my_pos - __ldg(offsets + __ldg(sel + t * k + lane))) & 7;
-        }
-        const float* __restrict__ xr = x + t * H;
-        for (int g0 = part * 32 * U; g0 < G8; g0 += parts * 32 * U) {
-            uint4 val[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int g = g0 + u * 32 + lane;
-                float v[8];
-                if (vec && int64_t(g) * 8 < H) {
-                    const float4 lo = __ldg(reinterpret_cast<const float4*>(xr) + 2 * g);
-                    const float4 hi = __ldg(reinterpret_cast<const float4*>(xr) + 2 * g + 1);
-                    v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
-                    v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        v[c] = (!vec && g < G8 && int64_t(g) * 8 + c < H) ? xr[int64_t(g) * 8 + c] : 0.f;
-                }
-                __half2 h[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    h[q] = mode == 1 ? __floats2half2_rn(v[q], v[q + 4])
-                                     : __floats2half2_rn(v[2 * q], v[2 * q + 1]);
-                val[u] = make_uint4(ptx::h2_as_u32(h[0]), ptx::h2_as_u32(h[1]),
-                                    ptx::h2_as_u32(h[2]), ptx::h2_as_u32(h[3]));
-            }
-            for (int i = 0; i < k; ++i) {
-                int pos = __shfl_sync(kFull, my_pos, i & 31);
-                int ph = __shfl_sync(kFull, my_ph, i & 31);
-                if (i >= 32) {   // slots past the first 32 (k > 32): read directly
-                    pos = __ldg(inv + t * k + i);
-                    ph = (pos - __ldg(offsets + __ldg(sel + t * k + i))) & 7;
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int g = g0 + u * 32 + lane;
-                    if (g < G8) xs16[(int64_t(g >> 3) * srows + pos) * 8 + ((g & 7) ^ ph)] = val[u];
-                }
-            }
-        }
-    }
-}
-
 template <int BITS, bool FC1, bool SCOL>
 cudaError_t launch_tc(const TcArgs& args, int grid, size_t smem, cudaStream_t s) {
     auto kern = grouped_gemm_kernel<BITS, FC1, SCOL>;
@@ -726,22 +652,6 @@ int pick_group(int n_mtiles) {
 }  // namespace
 
 int grouped_tile_tokens() { return kTcMaxN; }
-
-cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
-    // warps per token: enough warps for 32 per SM, at most one per 128-group pass
-    const int64_t passes = (pl.Hp / 8 + 127) / 128;
-    const int64_t want = (int64_t(32) * device_sm_count() + p.T - 1) / std::max<int64_t>(1, p.T);
-    const int parts = int(std::max<int64_t>(1, std::min<int64_t>(want, passes)));
-    const int64_t warps = std::max<int64_t>(1, p.T * parts);
-    const int blocks = int(std::min<int64_t>((warps + 7) / 8, int64_t(device_sm_count()) * 8));
-    const int vec = (p.H % 8 == 0 && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0) ? 1 : 0;
-    note_launch(QMOE_KERNEL_GROUP, s, true);
-    sort_convert_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
-        p.x, p.T, p.H, pl.Hp, vec, p.bits == 4 ? 1 : 0, parts, w.inv, w.sel, w.offsets, int(p.k),
-        pl.srows, reinterpret_cast<uint4*>(w.xs16));
-    note_launch(QMOE_KERNEL_GROUP, s, false);
-    return cudaGetLastError();
-}
 
 bool grouped_shape_ok(const Problem& p) {
     if (p.H % kTcK != 0 || p.I % kTcK != 0) return false;
