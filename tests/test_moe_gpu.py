@@ -91,6 +91,9 @@ SMALL = [
     FloatWorkload("pair_gelu_k1", 66, (260, 96), 96, 288, 8, 1, "gelu", biases=True),
     FloatWorkload("pair_fc3_tiles", 67, (700, 128), 128, 96, 2, 1, "swiglu", swiglu_fusion=0,
                   fc3=True, biases=True),
+    # past 4096 slots (multi-CTA routing): all-expert softmax over 200 experts (eight
+    # register slots per lane) with the serial in-chunk ranking (k = 20), renormalised
+    FloatWorkload("route_e200_k20", 68, (300, 64), 64, 64, 200, 20, "relu", normalize=1),
 ]
 
 

@@ -73,6 +73,13 @@ SMALL = [
     Workload("col4_two_tiles_relu", 36, (600, 256), 256, 128, 4, 2, 4, 0, "relu"),
     # k = E on the decode path: every token reaches every expert
     Workload("decode_k_eq_E", 37, (8, 256), 256, 256, 4, 4, 4, 32, "swiglu"),
+    # routing forms past 4096 slots (the multi-CTA routing kernel): eight register slots
+    # per lane (128 < E <= 256) with the serial in-chunk ranking (k > 16); the general
+    # selection and more than 32 sorted copies per token (k > 32); eight slots with the
+    # parallel ranking
+    Workload("route_e200_k20", 38, (300, 64), 64, 64, 200, 20, 4, 32, "swiglu"),
+    Workload("route_e96_k40", 39, (120, 64), 64, 64, 96, 40, 8, 0, "relu"),
+    Workload("route_e150_k8", 40, (600, 128), 128, 128, 150, 8, 4, 64, "swiglu"),
 ]
 
 
