@@ -517,6 +517,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 for (int ch = 0; ch < kTcMaxN / 32; ++ch)
                     p_c[ch] = ch * 32 + lane < w.rows ? __ldg(a.pw + slot_c[ch]) : 0.f;
             }
+            // column-wise scale of this output row (applied here, not in the operand), also
+            // loaded before the accumulator is ready
+            const int64_t row = int64_t(w.m + tile) * kTcM + r;
+            const float srow = SCOL && row < a.N ? __ldg(a.scales + int64_t(w.e) * a.N + row) : 1.f;
             if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -525,9 +529,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 break;
             }
             tc_fence_after();
-            const int64_t row = int64_t(w.m + tile) * kTcM + r;
-            // column-wise scale of this output row (applied here, not in the operand)
-            const float srow = SCOL && row < a.N ? __ldg(a.scales + int64_t(w.e) * a.N + row) : 1.f;
             const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) +
                                    uint32_t(buf * kAccCols + tile * acc_cols);
             for (int c0 = 0; c0 < w.nt; c0 += 32) {
