@@ -494,7 +494,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row in the weight tile
         __half* stile = reinterpret_cast<__half*>(smem + a.off_epi + uint32_t(ew) * a.epi_stage);
-        bool bad = false;                          // an output outside the fp16 range
+        // outputs outside the fp16 range: the largest magnitude and a NaN-propagating
+        // sum of every output this lane computes, checked once at the end
+        float omax = 0.f, osum = 0.f;
         uint32_t item_it = 0;
         for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
@@ -538,6 +540,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
 #pragma unroll
                     for (int q = 0; q < 32; ++q) v[q] *= srow;
                 }
+                // a tile's last chunk: columns past its rows hold stale sums; zero them so
+                // that their (unstored) outputs stay finite
+                if (c0 + 32 > w.rows) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (c0 + q >= w.rows) v[q] = 0.f;
+                }
                 if (FC1) {
                     // The warp's outputs for these 32 tokens (16 SwiGLU or 32 ReLU
                     // activation columns, already in the stored column order) go
@@ -556,8 +565,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                             const float gate = even ? v[q] : recv;
                             const float lin = even ? recv : v[16 + q];
                             const float o = swiglu(gate, lin, a.alpha, a.beta, a.has_limit, a.limit);
-                            // only stored outputs count (columns past the tile's rows are stale)
-                            bad |= (c0 + (even ? q : 16 + q) < w.rows) && !(fabsf(o) <= 65504.f);
+                            omax = fmaxf(omax, fabsf(o));
+                            osum += o;
                             stile[(even ? q : 16 + q) * 16 + pos] = __float2half_rn(o);
                         }
                     } else {
@@ -565,7 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const float o = fmaxf(v[q], 0.f);
-                            bad |= (c0 + q < w.rows) && !(o <= 65504.f);
+                            omax = fmaxf(omax, o);
                             stile[q * 32 + pos] = __float2half_rn(o);
                         }
                     }
@@ -599,7 +608,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
 #pragma unroll
                     for (int q = 0; q < 32; ++q) {
                         const float o = v[q] * __shfl_sync(kFull, my_p, q);
-                        bad |= (c0 + q < w.rows) && !(fabsf(o) <= 65504.f);
+                        omax = fmaxf(omax, fabsf(o));
+                        osum += o;
                         stile[q * 32 + lane] = __float2half_rn(o);
                     }
                     __syncwarp();
@@ -617,6 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
         }
+        const bool bad = !(omax <= 65504.f) || osum != osum;
         if (__any_sync(kFull, bad) && lane == 0) record_error(a.err, QMOE_DEVERR_NONFINITE);
     }
 

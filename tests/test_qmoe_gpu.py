@@ -198,6 +198,28 @@ def test_device_error_clean_after_forward(dev):
     assert q.get_device_error(ws) == q.DEVERR_NONE
 
 
+@pytest.mark.parametrize("path,which", [(2, "fc1"), (2, "fc2"), (1, "fc1")])
+def test_fp16_overflow_sets_nonfinite(dev, path, which):
+    """Scales so large that the FC1 activations (or the weighted FC2 rows of the
+    grouped path) leave the fp16 range: the call records QMOE_DEVERR_NONFINITE;
+    the same layer with its normal scales records nothing."""
+    import quantized_mixture_experts_gb300 as q
+    tokens = 8 if path == 1 else 40   # the decode path takes at most 16 tokens
+    wl = Workload("overflow", 41, (tokens, 256), 256, 128, 4, 2, 4, 32, "swiglu")
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(path=path, **wl.attrs())
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape, attrs))
+    q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], t["fc1_scales"],
+                   t["fc2_experts_weights"], t["fc2_scales"], attrs=attrs, workspace=ws)
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+    s1 = t["fc1_scales"] * (1e4 if which == "fc1" else 1.0)
+    s2 = t["fc2_scales"] * (1e7 if which == "fc2" else 1.0)
+    q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"], s1,
+                   t["fc2_experts_weights"], s2, attrs=attrs, workspace=ws)
+    assert q.get_device_error(ws) == q.DEVERR_NONFINITE
+
+
 # ----------------------------------------------------------------------------
 # Full-size workloads
 # ----------------------------------------------------------------------------
