@@ -20,8 +20,10 @@
 //               3-stage ring.  The token rows are stored K-blocked with the
 //               128-byte swizzle already applied, so one 1-D bulk copy of up to
 //               32 KB lands the whole swizzled tile;
-//   warp 1      TMEM allocator and MMA issuer (one lane): 4 x tcgen05.mma
-//               (K = 16) per stage into one of two 256-column accumulators;
+//   warp 1      TMEM allocator and MMA issuer (one lane): per stage four K = 16
+//               steps of one tcgen05.mma per weight tile, into the item's two
+//               256-column accumulators (one per weight tile; all 512 columns,
+//               so the epilogue of an item precedes the next item's MMAs);
 //   warps 2-9   dequantisers: packed codes -> (q - mid) * scale in fp16,
 //               written to shared memory in the 128-byte-swizzled K-major
 //               layout the MMA descriptor expects;
@@ -74,8 +76,6 @@ struct TcArgs {
     int64_t N, K;
     int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
     int topk, n_pairs, gm;
-    int split_n;                // 2: items take half a token tile (N <= 128), double-buffered
-                                // accumulators; 1: whole tile (N <= 256), single buffer
     __half* act_out;            // FC1 output, K-blocked like bsrc
     int act, has_limit;
     float alpha, beta, limit;
@@ -166,19 +166,20 @@ struct Item {
     int e, row0, rows, m, nt;   // expert, first sorted row, token rows, weight tile, MMA N
 };
 
+// Work item i: batches of gm weight-tile pairs; inside a batch token tile by
+// token tile, then pair, so that the items of a wave share token tiles and
+// weight tiles in L2.
 __device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntiles) {
-    const int64_t per_group = int64_t(ntiles) * a.split_n * a.gm;
+    const int64_t per_group = int64_t(ntiles) * a.gm;
     const int pg = int(i / per_group);
     const int64_t rem = i % per_group;
-    const int th = int(rem / a.gm);            // token tile and half
+    const int tau = int(rem / a.gm);           // token tile
     const int pm = int(rem % a.gm);
-    const int tau = th / a.split_n, half = th % a.split_n;
     const int32_t* t = a.tiles + kTileHeader + 4 * tau;
-    const int span = kTcMaxN / a.split_n;      // token rows per item
     Item it;
     it.e = t[0];
-    it.row0 = t[1] + half * span;
-    it.rows = min(t[2] - half * span, span);   // <= 0: nothing to do for this half
+    it.row0 = t[1];
+    it.rows = t[2];
     it.m = (pg * a.gm + pm) * kPair;           // first weight tile of the pair
     it.nt = (it.rows + 15) & ~15;
     return it;
@@ -232,8 +233,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     __shared__ __align__(8) uint64_t load_empty[kLoadStages];  // MMAs reading the stage done
     __shared__ __align__(8) uint64_t a_full[kAStages];         // dequantised weights written
     __shared__ __align__(8) uint64_t a_empty[kAStages];        // MMAs reading them done
-    __shared__ __align__(8) uint64_t acc_full[2];
-    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t acc_full;    // the item's MMAs done
+    __shared__ __align__(8) uint64_t acc_empty;   // its epilogue done
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
@@ -250,10 +251,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             ptx::mbar_init(&a_full[s], kDeqWarps);
             ptx::mbar_init(&a_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], kEpiWarps);
-        }
+        ptx::mbar_init(&acc_full, 1);
+        ptx::mbar_init(&acc_empty, kEpiWarps);
         ptx::mbar_init(&drain_bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
@@ -272,8 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
     // the combine after FC2 may start its prologue on SMs this grid leaves
     ptx::griddep_launch_dependents();
     const int ntiles = a.tiles[0];
-    const int64_t items = int64_t(ntiles) * a.split_n * a.n_pairs;
-    const int acc_cols = kAccCols / a.split_n;     // TMEM columns per weight tile and buffer
+    const int64_t items = int64_t(ntiles) * a.n_pairs;
     const int nkb = int(a.K / kTcK);
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t abase = sbase + a.nload * a.load_bytes;   // dequantised-weight ring
@@ -333,15 +331,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         for (int64_t i = blockIdx.x; i < items && ok; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
             if (w.rows <= 0) continue;
-            const int buf = a.split_n == 2 ? int(item_it & 1u) : 0;
-            const uint32_t aph = (a.split_n == 2 ? (item_it >> 1) : item_it) & 1u;
+            const uint32_t aph = item_it & 1u;
             ++item_it;
-            if (!ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, a.wait_ns, &abort_flag)) {
+            if (!ptx::mbar_wait(&acc_empty, aph ^ 1u, a.wait_ns, &abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t dbase = tmem_base + uint32_t(buf * kAccCols);
+            const uint32_t dbase = tmem_base;
             const uint32_t idesc = f16_idesc(kTcM, w.nt);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int sl = int(it % a.nload);
@@ -359,7 +356,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                         const uint64_t bd = sw128_desc(sb + 32u * kk);
 #pragma unroll
                         for (int t = 0; t < kPair; ++t)
-                            mma_f16(dbase + uint32_t(t * acc_cols),
+                            mma_f16(dbase + uint32_t(t * kAccCols),
                                     sw128_desc(sa0 + uint32_t(t) * kABytes + 32u * kk), bd, idesc,
                                     (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -370,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(&acc_full[buf]);
+            if (lane == 0) mma_commit(&acc_full);
             __syncwarp();
         }
         if (!ok && lane == 0) {
@@ -501,8 +498,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
         for (int64_t i = blockIdx.x; i < items; i += gridDim.x) {
             const Item w = decode_item(a, i, ntiles);
             if (w.rows <= 0) continue;
-            const int buf = a.split_n == 2 ? int(item_it & 1u) : 0;
-            const uint32_t aph = (a.split_n == 2 ? (item_it >> 1) : item_it) & 1u;
+            const uint32_t aph = item_it & 1u;
             ++item_it;
             // FC2: each lane's token of every 32-token chunk, its slot and routing
             // weight, loaded before the accumulator is ready (the loads are a
@@ -523,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             // loaded before the accumulator is ready
             const int64_t row = int64_t(w.m + tile) * kTcM + r;
             const float srow = SCOL && row < a.N ? __ldg(a.scales + int64_t(w.e) * a.N + row) : 1.f;
-            if (!ptx::mbar_wait(&acc_full[buf], aph, a.wait_ns, &abort_flag)) {
+            if (!ptx::mbar_wait(&acc_full, aph, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
@@ -532,7 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) +
-                                   uint32_t(buf * kAccCols + tile * acc_cols);
+                                   uint32_t(tile * kAccCols);
             for (int c0 = 0; c0 < w.nt; c0 += 32) {
                 float v[32];
                 tmem_ld32(tbase + uint32_t(c0), v);
@@ -625,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_gemm_kernel(const __gri
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+            if (lane == 0) ptx::mbar_arrive(&acc_empty);
         }
         const bool bad = !(omax <= 65504.f) || osum != osum;
         if (__any_sync(kFull, bad) && lane == 0) record_error(a.err, QMOE_DEVERR_NONFINITE);
@@ -701,9 +697,6 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     const int n_mtiles = int((a.N + kTcM - 1) / kTcM);
     a.n_pairs = (n_mtiles + kPair - 1) / kPair;
     a.gm = pick_group(a.n_pairs);
-    // FC2 with a short reduction: half-tile items so the fp32 epilogue overlaps the
-    // next item's MMAs (FC1 keeps whole tiles: halves would double the dequantisation)
-    a.split_n = 1;
     a.act_out = static_cast<__half*>(w.act);
     a.act = p.act;
     a.has_limit = p.has_limit;
@@ -727,7 +720,7 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     if (a.nload < 2) return cudaErrorInvalidValue;
     a.off_epi = a.nload * a.load_bytes + uint32_t(kAStages) * kAStageBytes;
     const size_t smem = 1024 + size_t(a.nload) * a.load_bytes + fixed;
-    const int64_t items_max = pl.max_tiles * a.split_n * a.n_pairs;
+    const int64_t items_max = pl.max_tiles * a.n_pairs;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
     const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
     note_launch(kid, s, true);
