@@ -297,7 +297,7 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
                 if ((e = launch_route(p, pl, wr, 0, s)) != cudaSuccess) return QMOE_ERR_CUDA;
                 if ((e = launch_group(p, pl, wr, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             }
-            if ((e = launch_sort_rows(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
+            if ((e = launch_sort_convert(p, pl, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, true, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_grouped_fc(p, pl, w, false, s)) != cudaSuccess) return QMOE_ERR_CUDA;
             if ((e = launch_combine16(p, w, s)) != cudaSuccess) return QMOE_ERR_CUDA;

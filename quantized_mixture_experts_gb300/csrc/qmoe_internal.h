@@ -152,7 +152,7 @@ cudaError_t launch_decode_fc(const Problem& p, const Plan& pl, const Work& w, bo
                              cudaStream_t s);
 // Grouped path (many tokens): tcgen05 expert-grouped GEMMs.
 int grouped_tile_tokens();
-cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
+cudaError_t launch_sort_convert(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s);
 bool grouped_shape_ok(const Problem& p);
 cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
                               cudaStream_t s);

@@ -772,7 +772,7 @@ cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_sort_rows(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
+cudaError_t launch_sort_convert(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
     // warps per token: enough warps for 32 per SM, at most one per 128-group pass
     const int64_t passes = (pl.Hp / 8 + 127) / 128;
     const int64_t want = (int64_t(32) * device_sm_count() + p.T - 1) / std::max<int64_t>(1, p.T);
