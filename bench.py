@@ -63,6 +63,52 @@ def _env_int(name, default):
 
 
 # ----------------------------------------------------------------------------
+# Ranks (one process per GPU, launched by torch.distributed.run; replicas only)
+# ----------------------------------------------------------------------------
+
+def ranks_init(device_kind):
+    """(world, rank, local) from the launcher's environment.  With more than one
+    rank the process group is set up: NCCL over the ranks' GPUs (each rank on
+    its LOCAL_RANK device), gloo for CPU-only use."""
+    import torch.distributed as dist
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    if world > 1:
+        if device_kind == "cuda":
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group(backend="nccl")
+        else:
+            dist.init_process_group(backend="gloo")
+    return world, rank, local
+
+
+def ranks_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x (the whole job's time is the slowest
+    rank's)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def ranks_done(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
 # Algorithmic work (bytes and FLOPs the method must move or compute)
 # ----------------------------------------------------------------------------
 
@@ -275,23 +321,16 @@ def cpu_baseline(wl, inp):
 
 def run_gpu(args, wl):
     import torch
-    import torch.distributed as dist
 
     import __graft_entry__
     import quantized_mixture_experts_gb300 as q
 
-    world = _env_int("WORLD_SIZE", 1)
-    rank = _env_int("RANK", 0)
-    local = _env_int("LOCAL_RANK", 0)
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group(backend="nccl")
+    world, rank, local = ranks_init("cuda")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     if rank == 0 or world == 1:
         __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     q.load()
 
     inp = make_inputs(wl, salt=rank)
@@ -323,8 +362,7 @@ def run_gpu(args, wl):
     except Exception:
         pass
 
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = q.launch_count()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -336,13 +374,9 @@ def run_gpu(args, wl):
         torch.cuda.synchronize(dev)
     launches = q.launch_count() - launches0
     n_launch, fc1_ms = kernel_pass(q, step, min(args.steps, 1000), dominant)
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     tokens_total = wl.tokens * args.steps * world
     value = tokens_total / (elapsed_ms / 1e3)
 
@@ -363,22 +397,18 @@ def run_gpu(args, wl):
 
     for _ in range(3):
         step_io()
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         step_io()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e_value = wl.tokens * e2e_steps * world / e2e_s
     if not np.array_equal(hy.numpy(), y.cpu().numpy()):
         raise RuntimeError("host-IO output differs from the device-resident output")
 
     if rank != 0:
-        dist.destroy_process_group()
+        ranks_done(world)
         return
 
     peaks = measured_peaks()
@@ -426,8 +456,7 @@ def run_gpu(args, wl):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks_done(world)
 
 
 # ----------------------------------------------------------------------------
@@ -491,23 +520,16 @@ def run_reference_float(args, wl):
 
 def run_gpu_float(args, wl):
     import torch
-    import torch.distributed as dist
 
     import __graft_entry__
     import quantized_mixture_experts_gb300 as q
 
-    world = _env_int("WORLD_SIZE", 1)
-    rank = _env_int("RANK", 0)
-    local = _env_int("LOCAL_RANK", 0)
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group(backend="nccl")
+    world, rank, local = ranks_init("cuda")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     if rank == 0 or world == 1:
         __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     q.load()
 
     inp = make_float_inputs(wl, salt=rank)
@@ -536,8 +558,7 @@ def run_gpu_float(args, wl):
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = q.launch_count()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -550,10 +571,7 @@ def run_gpu_float(args, wl):
     launches = q.launch_count() - launches0
     n_launch, fc1_ms = kernel_pass(q, step, min(args.steps, 1000), q.KERNEL_FC1)
     elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     value = wl.tokens * args.steps * world / (elapsed_ms / 1e3)
 
     hx = torch.from_numpy(inp["input"]).pin_memory()
@@ -570,21 +588,17 @@ def run_gpu_float(args, wl):
 
     for _ in range(3):
         step_io()
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         step_io()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e_value = wl.tokens * e2e_steps * world / e2e_s
     if not np.array_equal(hy.numpy(), y.cpu().numpy()):
         raise RuntimeError("host-IO output differs from the device-resident output")
     if rank != 0:
-        dist.destroy_process_group()
+        ranks_done(world)
         return
 
     peaks = measured_peaks()
@@ -644,8 +658,7 @@ def run_gpu_float(args, wl):
                                 "kind": "oracle",
                                 "sample": f"{sample} of {wl.tokens} tokens, {dt:.2f} s"}
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks_done(world)
 
 
 # ----------------------------------------------------------------------------
@@ -698,23 +711,16 @@ def run_reference_qkv(args, wl):
 
 def run_gpu_qkv(args, wl):
     import torch
-    import torch.distributed as dist
 
     import __graft_entry__
     import quantized_mixture_experts_gb300 as q
 
-    world = _env_int("WORLD_SIZE", 1)
-    rank = _env_int("RANK", 0)
-    local = _env_int("LOCAL_RANK", 0)
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group(backend="nccl")
+    world, rank, local = ranks_init("cuda")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     if rank == 0 or world == 1:
         __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     q.load()
     inp = make_qkv_inputs(wl, salt=rank)
     t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
@@ -746,8 +752,7 @@ def run_gpu_qkv(args, wl):
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    if world > 1:
-        dist.barrier()
+    ranks_barrier(world)
     torch.cuda.synchronize(dev)
     # A decode-sized call is shorter than its host-side enqueue (argument marshalling,
     # tensor-map encoding, three launches).  Each timed step therefore starts with an
@@ -767,10 +772,7 @@ def run_gpu_qkv(args, wl):
     n_launch, gemv_ms = kernel_pass(q, step, min(args.steps, 1000), q.KERNEL_FC1,
                                     before=lambda i: flush.fill_(float(i)))
     elapsed_ms = sum(a.elapsed_time(b) for a, b in zip(starts, stops))
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     value = wl.rows * args.steps * world / (elapsed_ms / 1e3)
 
     # end to end: pinned host activations in, the three projections back, every step
@@ -801,7 +803,7 @@ def run_gpu_qkv(args, wl):
     e2e_s = time.perf_counter() - t0
     e2e_value = wl.rows * e2e_steps * world / e2e_s
     if rank != 0:
-        dist.destroy_process_group()
+        ranks_done(world)
         return
     peaks = measured_peaks()
     avg_ms = gemv_ms / max(1, n_launch)
@@ -838,8 +840,7 @@ def run_gpu_qkv(args, wl):
         line["cpu_baseline"] = {"value": wl.rows / dt_s, "unit": "rows/s", "cores": 1,
                                 "kind": "oracle", "sample": f"all {wl.rows} rows, {dt_s:.2f} s"}
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    ranks_done(world)
 
 
 def main():
