@@ -32,6 +32,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -147,9 +148,8 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            self.out = open(os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv"), "w") \
-                if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
-                open(f"/tmp/.qmoe_clocks_{os.getpid()}.csv", "w")
+            self.out = open(os.path.join(tempfile.gettempdir(),
+                                         f".qmoe_clocks_{os.getpid()}.csv"), "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={QUERY}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
