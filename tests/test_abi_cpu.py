@@ -118,3 +118,30 @@ def test_gmm_rejections(lib):
 def test_status_strings(lib):
     assert q.binding.status_string(0) == "ok"
     assert "workspace" in q.binding.status_string(3)
+
+
+@pytest.mark.parametrize("name,expected", [("tiny", "grouped"), ("decode", "decode"),
+                                           ("prefill", "grouped"), ("many_small", "grouped"),
+                                           ("large_e", "grouped")])
+def test_auto_path_of_each_config(lib, name, expected):
+    """AUTO: the decode GEMV up to 16 tokens when its shape rules hold (H and I
+    multiples of 128, at least four scale blocks per 512-code chunk); the grouped
+    tensor-core path when H and I are multiples of 64; the scalar path otherwise."""
+    from quantized_mixture_experts_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[name]
+    a = q.make_attrs(**wl.attrs())
+    p = q.choose_path(wl.input_shape, (wl.experts, wl.fusion * wl.inter, wl.hidden // wl.pack), a)
+    assert q.PATH_NAMES[p] == expected
+
+
+@pytest.mark.parametrize("T,H,I,bs,expected", [
+    (16, 256, 256, 32, "decode"),     # the decode rules hold at 16 tokens
+    (17, 256, 256, 32, "grouped"),    # one token more
+    (8, 192, 256, 32, "grouped"),     # H not a multiple of 128
+    (8, 256, 256, 256, "grouped"),    # fewer than four scale blocks per 512 codes
+    (8, 96, 64, 32, "generic"),       # H not a multiple of 64
+    (300, 64, 96, 32, "generic"),     # I not a multiple of 64
+])
+def test_auto_path_boundaries(lib, T, H, I, bs, expected):
+    a = A(k=2, expert_weight_bits=4, block_size=bs, activation_type="swiglu")
+    assert q.PATH_NAMES[q.choose_path((T, H), (8, 2 * I, H // 2), a)] == expected
