@@ -6,7 +6,9 @@
 The float_* workloads measure the float MoE layer of the same library
 (moe_forward / moe_forward_hostio) in the same way, under the metric
 "MoE layer tokens/sec"; the qkv_* workloads measure the RMSNorm + 4-bit
-Q/K/V projection (matmul_nbits_qkv) under "QKV projection rows/sec".
+Q/K/V projection (matmul_nbits_qkv) under "QKV projection rows/sec"; the gmm_*
+workloads measure GroupedMatMul-29 on 16-bit operands (grouped_matmul) under
+"GroupedMatMul rows/sec", a row being one input row with its S selections.
 
 One step is one full qmoe_forward call (routing, grouping, FC1 + activation,
 FC2, combine) over one batch of the workload's tokens, with inputs and
@@ -41,16 +43,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from quantized_mixture_experts_gb300.workloads import (  # noqa: E402
-    FLOAT_WORKLOADS, QKV_WORKLOADS, WORKLOADS, make_float_inputs, make_inputs, make_qkv_inputs)
+    FLOAT_WORKLOADS, GMM_WORKLOADS, QKV_WORKLOADS, WORKLOADS, make_float_inputs, make_gmm_inputs,
+    make_inputs, make_qkv_inputs)
 
 METRIC = "QMoE layer tokens/sec"
 UNIT = "tokens/s"
 DEFAULT_STEPS = {"tiny": 2000, "decode": 8000, "prefill": 100, "many_small": 1000,
                  "large_e": 100, "float_tiny": 2000, "float_decode": 1000, "float_prefill": 40,
                  "float_prefill_e4": 100, "qkv_tiny": 2000, "qkv_decode": 5000,
-                 "qkv_decode_f32": 5000, "qkv_decode_wide": 2000}
+                 "qkv_decode_f32": 5000, "qkv_decode_wide": 2000, "gmm_tiny": 2000,
+                 "gmm_prefill": 200, "gmm_prefill_bf16": 200}
 QKV_METRIC = "QKV projection rows/sec"
 FLOAT_METRIC = "MoE layer tokens/sec"
+GMM_METRIC = "GroupedMatMul rows/sec"
 # dense TF32 / dense BF16 tensor throughput, nominal (1.1 and 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
 L2_BYTES = 129 * 1024 * 1024
@@ -843,16 +848,199 @@ def run_gpu_qkv(args, wl):
     ranks_done(world)
 
 
+# ----------------------------------------------------------------------------
+# GroupedMatMul-29 on 16-bit operands (grouped_matmul, tensor-core path)
+# ----------------------------------------------------------------------------
+
+def gmm_config(wl):
+    return {"workload": f"GroupedMatMul {wl.name}", "M": wl.M, "K": wl.K, "G": wl.G,
+            "N": wl.N, "S": wl.S, "T": wl.dtype, "Tind": "int64", "bias": None}
+
+
+def gmm_rounded(a, dtype):
+    """float32 host array -> float64 holding the values of the workload's 16-bit type."""
+    import torch
+    tdt = torch.float16 if dtype == "float16" else torch.bfloat16
+    return torch.from_numpy(np.ascontiguousarray(a)).to(tdt).double().numpy()
+
+
+def gmm_oracle_sample(inp, wl, seed, rows=256, cols=512):
+    """The oracle on a seeded sample of input rows and output columns: output[m, i, n]
+    for those rows and columns is the GroupedMatMul definition applied to the sampled
+    rows and to weights[:, :, cols].  Returns (seconds, rows-equivalent of work)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    r = np.sort(rng.choice(wl.M, size=min(rows, wl.M), replace=False))
+    c = np.sort(rng.choice(wl.N, size=min(cols, wl.N), replace=False))
+    x = gmm_rounded(inp["input"][r], wl.dtype)
+    w = gmm_rounded(inp["weights"][:, :, c], wl.dtype)
+    t0 = time.perf_counter()
+    _, st = oracle.grouped_matmul(x, w, inp["group_indices"][r])
+    dt = time.perf_counter() - t0
+    if st != oracle.OK:
+        raise RuntimeError("oracle rejected the GroupedMatMul sample")
+    return dt, len(r) * len(c) / wl.N, f"{len(r)} of {wl.M} rows x {len(c)} of {wl.N} columns"
+
+
+def run_reference_gmm(args, wl):
+    if _env_int("RANK", 0) != 0:
+        return
+    inp = make_gmm_inputs(wl)
+    times, work = [], 0.0
+    for step in range(args.warmup + args.steps):
+        dt, rows_eq, sample = gmm_oracle_sample(inp, wl, seed=step)
+        if step >= args.warmup:
+            times.append(dt)
+            work += rows_eq
+    total = sum(times)
+    value = work / total
+    line = {"impl": "reference", "metric": GMM_METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": gmm_config(wl),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{sample} per step, seeded; rows/s scaled by the "
+                                       "column fraction"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_gmm(args, wl):
+    import torch
+
+    import __graft_entry__
+    import quantized_mixture_experts_gb300 as q
+
+    world, rank, local = ranks_init("cuda")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    ranks_barrier(world)
+    q.load()
+    inp = make_gmm_inputs(wl, salt=rank)
+    tdt = torch.float16 if wl.dtype == "float16" else torch.bfloat16
+    x = torch.from_numpy(inp["input"]).to(dev).to(tdt)
+    w = torch.from_numpy(inp["weights"]).to(dev).to(tdt)
+    idx = torch.from_numpy(inp["group_indices"]).to(dev)
+    out = torch.empty((wl.M, wl.S, wl.N), dtype=tdt, device=dev)
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(wl.M, wl.K, wl.G, wl.N,
+                                                                   wl.S, tdt), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q.grouped_matmul(x, w, idx, output=out, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    err = q.get_device_error(ws, stream)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    ranks_barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = q.launch_count()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = q.launch_count() - launches0
+    n_launch, gemm_ms = kernel_pass(q, step, min(args.steps, 1000), q.KERNEL_GMM)
+    ranks_barrier(world)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
+    value = wl.M * args.steps * world / (elapsed_ms / 1e3)
+
+    # end to end: page-locked host rows and indices in, the output back, every step
+    hx = x.cpu().pin_memory()
+    hi = torch.from_numpy(inp["group_indices"]).pin_memory()
+    ho = torch.empty(out.shape, dtype=tdt).pin_memory()
+    dx, di = torch.empty_like(x), torch.empty_like(idx)
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def step_io():
+        dx.copy_(hx, non_blocking=True)
+        di.copy_(hi, non_blocking=True)
+        q.grouped_matmul(dx, w, di, output=out, workspace=ws, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step_io()
+    ranks_barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_io()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    e2e_value = wl.M * e2e_steps * world / e2e_s
+    if rank != 0:
+        ranks_done(world)
+        return
+    peaks = measured_peaks()
+    avg_ms = gemm_ms / max(1, n_launch)
+    achieved = wl.flops / (avg_ms / 1e3) / 1e12
+    # f16 and bf16 have the same nominal dense rate: the measured bf16 peak serves both
+    peak = peaks["bf16_tflops_sustained"] if args.steps * avg_ms > 1000 else peaks["bf16_tflops"]
+    cfg = gmm_config(wl)
+    cfg.update({"l2": f"weights {w.numel() * 2 / 1e9:.2f} GB per step exceed the 129 MB L2; "
+                      "no flush",
+                "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                "device_error": err})
+    line = {
+        "metric": GMM_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16" if wl.dtype == "float16" else "bf16",
+        "data": "synthetic (seeded; uniform activations and weights)", "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak if peak else None,
+                     "traffic": ncu_traffic(f"gmm_tc_{wl.name}.md", ["gemm_f16.cu", "ptx.cuh"]),
+                     "kernel": "GroupedMatMul GEMM", "kernel_ms": avg_ms, "launches": n_launch,
+                     "algorithmic": wl.flops, "peak_source": peaks["source"]},
+        "e2e": {"value": e2e_value, "unit": "rows/s",
+                "h2d_bytes_per_step": int(hx.numel() * 2 + hi.numel() * 8),
+                "d2h_bytes_per_step": int(ho.numel() * 2), "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        dt, rows_eq, sample = gmm_oracle_sample(inp, wl, seed=0)
+        line["cpu_baseline"] = {"value": rows_eq / dt, "unit": "rows/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{sample}, {dt:.2f} s; rows/s scaled by the "
+                                          "column fraction"}
+    print(json.dumps(line), flush=True)
+    ranks_done(world)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
-                    choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS) + sorted(QKV_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS) + sorted(QKV_WORKLOADS)
+                    + sorted(GMM_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.workload in GMM_WORKLOADS:
+        gwl = GMM_WORKLOADS[args.workload]
+        if args.steps is None:
+            args.steps = 3 if args.impl == "reference" else DEFAULT_STEPS[gwl.name]
+        args.warmup = max(3, args.warmup)
+        if args.impl == "reference":
+            run_reference_gmm(args, gwl)
+        else:
+            run_gpu_gmm(args, gwl)
+        return
     if args.workload in QKV_WORKLOADS:
         qwl = QKV_WORKLOADS[args.workload]
         if args.steps is None:

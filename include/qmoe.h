@@ -289,13 +289,15 @@ typedef enum {
     QMOE_KERNEL_GROUP = 1,
     QMOE_KERNEL_FC1 = 2,
     QMOE_KERNEL_FC2 = 3,
-    QMOE_KERNEL_COMBINE = 4
+    QMOE_KERNEL_COMBINE = 4,
+    QMOE_KERNEL_GMM = 5              /* grouped_matmul's tensor-core GEMM        */
 } qmoe_kernel_id;
 
 /*
  * Per-kernel device timing.  After qmoe_profile_begin(id), each launch of
- * kernel `id` by qmoe_forward is bracketed by CUDA events on the launching
- * stream.  qmoe_profile_end synchronizes those events and returns how many
+ * kernel `id` (by qmoe_forward, or by grouped_matmul for QMOE_KERNEL_GMM) is
+ * bracketed by CUDA events on the launching stream.  An id outside the enum
+ * returns INVALID_ARGUMENT.  qmoe_profile_end synchronizes those events and returns how many
  * launches were bracketed and their summed duration in milliseconds, then
  * stops recording.
  */

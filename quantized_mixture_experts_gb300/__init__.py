@@ -13,7 +13,7 @@ from .binding import (  # noqa: F401
     profile_end, launch_count, load, declared_functions,
     PATH_AUTO, PATH_DECODE, PATH_GROUPED, PATH_GENERIC, PATH_NAMES,
     DEVERR_NONE, DEVERR_INDEX, DEVERR_NONFINITE, DEVERR_TIMEOUT,
-    KERNEL_ROUTE, KERNEL_GROUP, KERNEL_FC1, KERNEL_FC2, KERNEL_COMBINE,
+    KERNEL_ROUTE, KERNEL_GROUP, KERNEL_FC1, KERNEL_FC2, KERNEL_COMBINE, KERNEL_GMM,
     MoeAttrs, make_moe_attrs, moe_workspace_size, moe_choose_path, moe_forward,
     moe_forward_hostio, moe_get_device_error, MOE_PATH_AUTO, MOE_PATH_GROUPED, MOE_PATH_GENERIC,
     QkvAttrs, make_qkv_attrs, qkv_workspace_size, qkv_choose_path, matmul_nbits_qkv,

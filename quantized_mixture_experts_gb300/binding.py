@@ -30,7 +30,7 @@ PATH_NAMES = {PATH_AUTO: "auto", PATH_DECODE: "decode", PATH_GROUPED: "grouped",
 DT_F32, DT_F16, DT_BF16, DT_F64 = range(4)
 IDX_I32, IDX_I64 = range(2)
 # qmoe_kernel_id
-KERNEL_ROUTE, KERNEL_GROUP, KERNEL_FC1, KERNEL_FC2, KERNEL_COMBINE = range(5)
+KERNEL_ROUTE, KERNEL_GROUP, KERNEL_FC1, KERNEL_FC2, KERNEL_COMBINE, KERNEL_GMM = range(6)
 
 
 class QmoeError(RuntimeError):

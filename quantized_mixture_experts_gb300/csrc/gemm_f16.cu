@@ -547,8 +547,10 @@ cudaError_t launch_grouped_matmul_tc(const void* input, int64_t M, int64_t K, co
         return e;
     const int64_t items_max = pl.max_tiles * a.n_pairs;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_max, device_sm_count())));
+    note_launch(-1, s, false, 4);   // ranking, the two grouping launches, the gather
+    note_launch(QMOE_KERNEL_GMM, s, true);
     gmm_tc_kernel<<<grid, kGThreads, smem, s>>>(a);
-    note_launch(-1, s, false, 5);
+    note_launch(QMOE_KERNEL_GMM, s, false, 1);
     return cudaGetLastError();
 }
 

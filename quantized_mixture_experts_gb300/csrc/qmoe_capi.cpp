@@ -537,7 +537,7 @@ void qmoe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 void qmoe_debug_drop_stage(int64_t stage) { g_drop_stage.store(stage < 0 ? -1 : stage); }
 
 qmoe_status qmoe_profile_begin(int32_t kernel_id) {
-    if (kernel_id < QMOE_KERNEL_ROUTE || kernel_id > QMOE_KERNEL_COMBINE)
+    if (kernel_id < QMOE_KERNEL_ROUTE || kernel_id > QMOE_KERNEL_GMM)
         return QMOE_ERR_INVALID_ARGUMENT;
     std::lock_guard<std::mutex> lock(g_prof_mu);
     g_prof_kernel = kernel_id;

@@ -311,3 +311,58 @@ def make_qkv_inputs(wl: QkvWorkload, salt: int = 0) -> dict:
     if wl.skip:
         out["skip"] = (g(3).standard_normal(wl.input_shape, dtype=np.float32) * 0.5).astype(dt)
     return out
+
+
+# ---------------------------------------------------------------------------
+# GroupedMatMul-29 on 16-bit operands.  input ~ U[-sqrt 3, sqrt 3] (unit
+# variance); weights ~ U[-sqrt(3/K), sqrt(3/K)] (variance 1/K) so the outputs
+# stay near unit scale in f16 (uniform rather than normal draws: a billion
+# weights take seconds that way); group_indices int64: each row draws
+# S distinct groups uniformly (the QMoE layer's k distinct experts per token).
+# The prefill workload is the prefill layer's FC1 as a dense grouped product:
+# 4096 tokens, k 2 of 8 experts, hidden 4096 -> 2 x 14336 (gate and linear).
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class GmmWorkload:
+    name: str
+    index: int
+    M: int
+    K: int
+    G: int
+    N: int
+    S: int
+    dtype: str = "float16"       # float16 | bfloat16
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.S * self.K * self.N
+
+
+GMM_WORKLOADS = {
+    "gmm_tiny": GmmWorkload("gmm_tiny", 80, 300, 128, 5, 200, 2),
+    "gmm_prefill": GmmWorkload("gmm_prefill", 81, 4096, 4096, 8, 28672, 2),
+    "gmm_prefill_bf16": GmmWorkload("gmm_prefill_bf16", 82, 4096, 4096, 8, 28672, 2,
+                                    "bfloat16"),
+}
+
+
+def make_gmm_inputs(wl: GmmWorkload, salt: int = 0) -> dict:
+    """Draw input [M, K], weights [G, K, N] (float32, to be cast to the workload's
+    16-bit type by the caller) and group_indices [M, S] (int64) for ``wl``."""
+    fake = Workload(wl.name, wl.index, (wl.M, wl.K), wl.K, 1, 1, 1, 4, 0, "relu")
+
+    def g(tid):
+        return _rng(fake, tid, salt)
+
+    def uniform(tid, shape, half_width):
+        a = g(tid).random(shape, dtype=np.float32)
+        a *= np.float32(2.0 * half_width)
+        a -= np.float32(half_width)
+        return a
+
+    x = uniform(1, (wl.M, wl.K), np.sqrt(3.0))
+    w = uniform(2, (wl.G, wl.K, wl.N), np.sqrt(3.0 / wl.K))
+    keys = g(3).random((wl.M, wl.G))
+    idx = np.argsort(keys, axis=1, kind="stable")[:, :wl.S].astype(np.int64)
+    return dict(input=x, weights=w, group_indices=idx)

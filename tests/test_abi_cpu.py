@@ -145,3 +145,16 @@ def test_auto_path_of_each_config(lib, name, expected):
 def test_auto_path_boundaries(lib, T, H, I, bs, expected):
     a = A(k=2, expert_weight_bits=4, block_size=bs, activation_type="swiglu")
     assert q.PATH_NAMES[q.choose_path((T, H), (8, 2 * I, H // 2), a)] == expected
+
+
+def test_profile_kernel_ids(lib):
+    """Every kernel id of the header, GroupedMatMul's GEMM included, is accepted;
+    ids outside the enum are rejected.  No launch is recorded, so no CUDA call."""
+    for kid in (q.KERNEL_ROUTE, q.KERNEL_GROUP, q.KERNEL_FC1, q.KERNEL_FC2, q.KERNEL_COMBINE,
+                q.KERNEL_GMM):
+        assert lib.qmoe_profile_begin(kid) == 0
+        n, ms = q.profile_end()
+        assert (n, ms) == (0, 0.0)
+    assert q.KERNEL_GMM == 5
+    assert lib.qmoe_profile_begin(6) == 1
+    assert lib.qmoe_profile_begin(-1) == 1

@@ -51,7 +51,7 @@ def test_single_rank_needs_no_process_group():
     bench.ranks_done(1)
 
 
-@pytest.mark.parametrize("workload", ["decode", "float_tiny", "qkv_tiny"])
+@pytest.mark.parametrize("workload", ["decode", "float_tiny", "qkv_tiny", "gmm_tiny"])
 def test_reference_arm_runs_on_rank_zero_only(workload):
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload,

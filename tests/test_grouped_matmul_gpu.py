@@ -172,3 +172,44 @@ def test_tensor_core_path_invalid_index(dev):
     mask = np.ones((M, S), dtype=bool)
     mask[3, 1] = mask[7, 0] = False
     assert np.all(o[mask] == 1.0)
+
+
+@pytest.mark.parametrize("name", ["gmm_prefill", "gmm_prefill_bf16"])
+def test_bench_workload_sampled_vs_oracle(dev, name):
+    """The benchmark's GroupedMatMul workloads (the prefill layer's FC1 shape as a dense
+    f16/bf16 grouped product: M 4096, K 4096, G 8, N 28672, S 2) at full size through
+    the call the benchmark times.  Sampled rows and columns (the last of each
+    included) are compared with the oracle on the sampled problem: input[rows] and
+    weights[:, :, cols] give exactly those outputs under the Summary definition."""
+    import quantized_mixture_experts_gb300 as q
+    from quantized_mixture_experts_gb300.workloads import GMM_WORKLOADS, make_gmm_inputs
+    wl = GMM_WORKLOADS[name]
+    dt = "f16" if wl.dtype == "float16" else "bf16"
+    tdt = getattr(torch, DTYPES[dt])
+    inp = make_gmm_inputs(wl)
+    x = torch.from_numpy(inp["input"]).to(dev).to(tdt)
+    w = torch.from_numpy(inp["weights"]).to(dev).to(tdt)
+    del inp["weights"]
+    idx = torch.from_numpy(inp["group_indices"]).to(dev)
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(wl.M, wl.K, wl.G, wl.N,
+                                                                   wl.S, tdt), dev)
+    n0 = _launches()
+    out = q.grouped_matmul(x, w, idx, workspace=ws)
+    torch.cuda.synchronize()
+    assert _launches() - n0 == 6   # error-word clear, grouping (3), gather, tensor-core GEMM
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+    rng = np.random.default_rng(11)
+    r = np.unique(np.append(rng.choice(wl.M, 48, replace=False), wl.M - 1))
+    c = np.unique(np.append(rng.choice(wl.N, 384, replace=False), wl.N - 1))
+    rt, ct = torch.from_numpy(r).to(dev), torch.from_numpy(c).to(dev)
+    xr = x[rt].double().cpu().numpy()
+    wr = w[:, :, ct].double().cpu().numpy()
+    ix = inp["group_indices"][r]
+    got = out[rt][:, :, ct].double().cpu().numpy()
+    ref, st = oracle.grouped_matmul(xr, wr, ix)
+    assert st == oracle.OK
+    mag = np.stack([np.stack([np.abs(xr[m]) @ np.abs(wr[g]) for g in ix[m]]) for m in range(len(r))])
+    eps_out = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dt]
+    bound = 2 * (wl.K + 2) * 2.0 ** -24 * mag + eps_out * np.abs(ref) + 1e-300
+    err = np.abs(got - ref)
+    assert np.all(err <= bound), float(np.max(err / bound))
