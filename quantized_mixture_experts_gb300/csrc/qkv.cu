@@ -325,7 +325,6 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
     char* base = static_cast<char*>(ws);
     int32_t* err = reinterpret_cast<int32_t*>(base);
     float* n32 = reinterpret_cast<float*>(base + q.off_n32);
-    const unsigned rows = unsigned(p.rows);
     cudaError_t e;
     if (p.path == QKV_PATH_DECODE) {
         __half* n16 = reinterpret_cast<__half*>(base + q.off_n16);
