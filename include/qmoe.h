@@ -295,9 +295,14 @@ typedef enum {
 
 /*
  * Per-kernel device timing.  After qmoe_profile_begin(id), each launch of
- * kernel `id` (by qmoe_forward, or by grouped_matmul for QMOE_KERNEL_GMM) is
- * bracketed by CUDA events on the launching stream.  An id outside the enum
- * returns INVALID_ARGUMENT.  qmoe_profile_end synchronizes those events and returns how many
+ * kernel `id` is bracketed by CUDA events on the launching stream.  An id
+ * outside the enum returns INVALID_ARGUMENT.  The ids name steps of the
+ * library's entry points:
+ *   qmoe_forward, moe_forward: ROUTE the routing kernel, GROUP the grouping
+ *     launches, FC1 / FC2 the two expert projections, COMBINE the weighted sum;
+ *   matmul_nbits_qkv (qkv.h): ROUTE the RMSNorm kernel, FC1 the Q/K/V
+ *     projection, COMBINE the split-K reduction;
+ *   grouped_matmul: GMM its tensor-core GEMM.  qmoe_profile_end synchronizes those events and returns how many
  * launches were bracketed and their summed duration in milliseconds, then
  * stops recording.
  */
