@@ -7,6 +7,7 @@ attributeConstraints) must reject bad calls before anything is launched, so
 these calls never touch a device.
 """
 import ctypes
+import os
 
 import pytest
 
@@ -158,3 +159,45 @@ def test_profile_kernel_ids(lib):
     assert q.KERNEL_GMM == 5
     assert lib.qmoe_profile_begin(6) == 1
     assert lib.qmoe_profile_begin(-1) == 1
+
+
+def _header_enums():
+    """name -> value for every enumerator written `NAME = value` in include/*.h."""
+    import re
+    vals = {}
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    for h in ("qmoe.h", "moe.h", "qkv.h"):
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+        for body in re.findall(r"typedef enum\s*\{(.*?)\}", text, flags=re.S):
+            for name, val in re.findall(r"([A-Z][A-Z0-9_]+)\s*=\s*(-?\d+)", body):
+                vals[name] = int(val)
+    return vals
+
+
+def test_binding_constants_match_header_enums():
+    """The binding's constants carry the values the C headers give their enumerators."""
+    h = _header_enums()
+    b = q.binding
+    pairs = {
+        "QMOE_OK": b.OK, "QMOE_ERR_INVALID_ARGUMENT": b.ERR_INVALID_ARGUMENT,
+        "QMOE_ERR_NOT_SUPPORTED": b.ERR_NOT_SUPPORTED,
+        "QMOE_ERR_WORKSPACE_TOO_SMALL": b.ERR_WORKSPACE_TOO_SMALL, "QMOE_ERR_CUDA": b.ERR_CUDA,
+        "QMOE_DEVERR_NONE": b.DEVERR_NONE, "QMOE_DEVERR_INDEX": b.DEVERR_INDEX,
+        "QMOE_DEVERR_NONFINITE": b.DEVERR_NONFINITE, "QMOE_DEVERR_TIMEOUT": b.DEVERR_TIMEOUT,
+        "QMOE_ACT_RELU": b.ACTIVATIONS["relu"], "QMOE_ACT_SWIGLU": b.ACTIVATIONS["swiglu"],
+        "QMOE_PATH_AUTO": b.PATH_AUTO, "QMOE_PATH_DECODE": b.PATH_DECODE,
+        "QMOE_PATH_GROUPED": b.PATH_GROUPED, "QMOE_PATH_GENERIC": b.PATH_GENERIC,
+        "QMOE_DT_F32": b.DT_F32, "QMOE_DT_F16": b.DT_F16, "QMOE_DT_BF16": b.DT_BF16,
+        "QMOE_DT_F64": b.DT_F64, "QMOE_IDX_I32": b.IDX_I32, "QMOE_IDX_I64": b.IDX_I64,
+        "QMOE_KERNEL_ROUTE": b.KERNEL_ROUTE, "QMOE_KERNEL_GROUP": b.KERNEL_GROUP,
+        "QMOE_KERNEL_FC1": b.KERNEL_FC1, "QMOE_KERNEL_FC2": b.KERNEL_FC2,
+        "QMOE_KERNEL_COMBINE": b.KERNEL_COMBINE, "QMOE_KERNEL_GMM": b.KERNEL_GMM,
+        "MOE_PATH_AUTO": b.MOE_PATH_AUTO, "MOE_PATH_GROUPED": b.MOE_PATH_GROUPED,
+        "MOE_PATH_GENERIC": b.MOE_PATH_GENERIC,
+        "QKV_PATH_AUTO": b.QKV_PATH_AUTO, "QKV_PATH_DECODE": b.QKV_PATH_DECODE,
+        "QKV_PATH_GENERIC": b.QKV_PATH_GENERIC,
+    }
+    pairs.update({f"MOE_ACT_{a.upper()}": v for a, v in b.MOE_ACTIVATIONS.items()})
+    missing = sorted(set(pairs) - set(h))
+    assert not missing, missing
+    assert {k: h[k] for k in pairs} == pairs
