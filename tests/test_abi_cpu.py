@@ -201,3 +201,27 @@ def test_binding_constants_match_header_enums():
     missing = sorted(set(pairs) - set(h))
     assert not missing, missing
     assert {k: h[k] for k in pairs} == pairs
+
+
+def _header_prototypes():
+    """name -> parameter count for every function prototype in include/*.h."""
+    import re
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    protos = {}
+    for h in ("qmoe.h", "moe.h", "qkv.h"):
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+        text = re.sub(r"typedef\s+(enum|struct)\s*\{.*?\}\s*\w+\s*;", "", text, flags=re.S)
+        for name, params in re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(([^()]*)\)\s*;", text):
+            params = params.strip()
+            protos[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return protos
+
+
+def test_binding_argument_counts_match_prototypes(lib):
+    """Every declared function is bound with as many ctypes arguments as its C
+    prototype has parameters (a mismatch would pass garbage through the ABI)."""
+    protos = _header_prototypes()
+    assert set(protos) == set(q.declared_functions())
+    for name, n in sorted(protos.items()):
+        at = getattr(lib, name).argtypes
+        assert at is not None and len(at) == n, (name, n, at)
