@@ -225,3 +225,31 @@ def test_binding_argument_counts_match_prototypes(lib):
     for name, n in sorted(protos.items()):
         at = getattr(lib, name).argtypes
         assert at is not None and len(at) == n, (name, n, at)
+
+
+@pytest.mark.parametrize("cname,pyname", [("qmoe_attrs", "Attrs"), ("moe_attrs", "MoeAttrs"),
+                                          ("qkv_attrs", "QkvAttrs")])
+def test_attribute_struct_layouts_match_c(tmp_path, cname, pyname):
+    """The ctypes structures have the C compiler's size and field offsets for the
+    attribute structs of include/*.h (compiled here with the system C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    st = getattr(b, pyname)
+    fields = [f[0] for f in st._fields_]
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "qmoe.h"', '#include "moe.h"',
+             '#include "qkv.h"', 'int main(void) {',
+             f'  printf("%zu\\n", sizeof({cname}));']
+    lines += [f'  printf("%zu\\n", offsetof({cname}, {f}));' for f in fields]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(st)
+    assert got[1:] == [getattr(st, f).offset for f in fields]
