@@ -193,8 +193,13 @@ qmoe_status qmoe_forward_hostio(const float *host_input, const int64_t *input_sh
  * library holds that memory until the process exits.  The call allocates
  * nothing and calls no allocating routine.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
+ *    (cudaGetSymbolAddress, with that device current) and caches it with
+ *    the identity of the current CUDA context; make that first call before
+ *    any stream capture.  An address is valid in one context only: when a
+ *    later call finds another context current on the device (a host runtime
+ *    that runs it in its own context, or a new primary context after
+ *    cudaDeviceReset), it looks the address up again in that context, so
+ *    that first call in the new context should also come before any capture.
  *  - Shapes whose qmoe_workspace_size exceeds the array are rejected with
  *    QMOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (decode-sized
  *    batches fit; large prefill batches do not).
@@ -202,7 +207,8 @@ qmoe_status qmoe_forward_hostio(const float *host_input, const int64_t *input_sh
  *    contents (the layer rewrites everything it reads, including the device
  *    error word).  Calls that can overlap on the GPU -- different streams, or
  *    host threads without ordering -- race on it and must be serialized by
- *    the caller.  qmoe_get_device_error is not available for these calls.
+ *    the caller.  Their device error word is read with
+ *    qmoe_noalloc_get_device_error, not qmoe_get_device_error.
  */
 size_t qmoe_noalloc_scratch_bytes(void);
 
@@ -217,6 +223,19 @@ qmoe_status qmoe_forward_noalloc(const float *input, const int64_t *input_shape,
                                  int32_t fc2_scales_rank,
                                  float *output, const qmoe_attrs *attrs,
                                  int32_t *topk_idx_out, float *topk_w_out, void *cuda_stream);
+
+/*
+ * Device error word of the last qmoe_forward_noalloc call(s) on the current
+ * device: the kernels record a qmoe_device_error value there (an fp16
+ * intermediate out of range, a pipeline wait past its limit) instead of
+ * trapping.  The word is read and then cleared in stream order on
+ * `cuda_stream` (after the calls enqueued on it before), and the stream is
+ * synchronized before *code is set.  Allocates nothing.  Like the calls
+ * themselves it shares the fixed array: it must not overlap on the GPU with a
+ * qmoe_forward_noalloc call on another stream.  The operator pages have no
+ * counterpart to it.
+ */
+qmoe_status qmoe_noalloc_get_device_error(void *cuda_stream, int32_t *code);
 
 /* Element types of grouped_matmul (GroupedMatMul-29, Type Constraints). */
 typedef enum { QMOE_DT_F32 = 0, QMOE_DT_F16 = 1, QMOE_DT_BF16 = 2, QMOE_DT_F64 = 3 } qmoe_dtype;
@@ -268,8 +287,9 @@ qmoe_status qmoe_get_device_error(void *workspace, void *cuda_stream, int32_t *c
  * Upper bound, in nanoseconds, on any single spin-wait inside a kernel
  * (mbarrier or flag).  When a wait exceeds it the kernel records
  * QMOE_DEVERR_TIMEOUT, drains its own copies in flight, releases its tensor
- * memory and returns.  Default 2 s.  Process-wide; takes effect at the next
- * launch.
+ * memory and returns.  Default 2 s.  Per host thread: it applies to the
+ * launches the calling thread makes from its next call on, and leaves other
+ * threads' launches at their own setting.
  */
 void qmoe_set_wait_limit_ns(uint64_t ns);
 
@@ -279,7 +299,9 @@ void qmoe_set_wait_limit_ns(uint64_t ns);
  * this call skips the copies of its pipeline stage number `stage` (counted
  * from 0 per CTA), so the consumers' wait on that stage never completes and
  * must end through the wait limit with QMOE_DEVERR_TIMEOUT.  -1 (the default)
- * turns it off.  Process-wide.
+ * turns it off.  Per host thread: only the launches of the calling thread
+ * skip the stage, so a hook set by one thread cannot make a layer that another
+ * thread runs at the same time wait and fail.
  */
 void qmoe_debug_drop_stage(int64_t stage);
 

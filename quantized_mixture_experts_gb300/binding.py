@@ -129,6 +129,8 @@ def load():
     lib.qmoe_noalloc_scratch_bytes.restype = SZ
     lib.qmoe_forward_noalloc.argtypes = fwd[:-2] + [P, P, P]
     lib.qmoe_forward_noalloc.restype = ctypes.c_int
+    lib.qmoe_noalloc_get_device_error.argtypes = [P, ctypes.POINTER(I32)]
+    lib.qmoe_noalloc_get_device_error.restype = ctypes.c_int
     lib.grouped_matmul_workspace_size.argtypes = [ctypes.POINTER(SZ)]
     lib.grouped_matmul_workspace_size.restype = ctypes.c_int
     lib.grouped_matmul_workspace_size_for.argtypes = [I64, I64, I64, I64, I64, ctypes.c_int32,
@@ -381,6 +383,15 @@ def get_device_error(workspace, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(load().qmoe_get_device_error(_ptr(workspace), _stream(stream), ctypes.byref(code)),
            "qmoe_get_device_error")
+    return code.value
+
+
+def noalloc_get_device_error(stream=None) -> int:
+    """Device error word of the last qmoe_forward_noalloc call(s) on the current
+    device (read and cleared in stream order)."""
+    code = ctypes.c_int32(0)
+    _check(load().qmoe_noalloc_get_device_error(_stream(stream), ctypes.byref(code)),
+           "qmoe_noalloc_get_device_error")
     return code.value
 
 

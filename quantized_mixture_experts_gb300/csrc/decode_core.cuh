@@ -47,6 +47,13 @@ __device__ __forceinline__ void record_error(int32_t* err, int code) {
     atomicCAS(err, 0, code);
 }
 
+// The conversion is the exponent-bias method of turning small integers into
+// floating point: with the exponent of a power-of-two constant fixed, the
+// integer written into the low mantissa bits gives constant + integer exactly,
+// and subtracting the constant leaves the integer.  Its use for int4/int8
+// weight dequantisation is described by Kim et al., "Who Says Elephants Can't
+// Run: Bringing Large Scale MoE Models into Cloud Scale Production" (2022).
+//
 // Eight 4-bit codes of `w` (low nibble first, element e in bits 4e..4e+3) ->
 // four fp16 pairs, each exact and each 1160 above its weight:
 //   h[0] = 1152 + (q0, q4)         h[1] = 1152 + (q2, q6)        (low nibbles of each byte)

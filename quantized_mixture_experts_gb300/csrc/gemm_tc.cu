@@ -185,6 +185,13 @@ __device__ __forceinline__ Item decode_item(const TcArgs& a, int64_t i, int ntil
     return it;
 }
 
+// The conversion is the exponent-bias method of turning small integers into
+// floating point: with the exponent of a power-of-two constant fixed, the
+// integer written into the low mantissa bits gives constant + integer exactly,
+// and subtracting the constant leaves the integer.  Its use for int4/int8
+// weight dequantisation is described by Kim et al., "Who Says Elephants Can't
+// Run: Bringing Large Scale MoE Models into Cloud Scale Production" (2022).
+//
 // Eight packed 4-bit codes (low nibble first) -> four fp16 pairs
 // ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) of (q - 8) [* s].  The activations of the
 // 4-bit path are stored with the same order inside every group of eight, so

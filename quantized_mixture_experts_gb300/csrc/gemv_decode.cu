@@ -8,16 +8,19 @@
 // to that expert (at most 16).
 //
 // Per CTA (one per SM, persistent): warp 0 is a TMA producer that fills a
-// 3-stage ring in shared memory with
+// ring of up to 4 stages in shared memory (as many as fit) with
 //   - the unit's 128 weight rows x 256 packed bytes (two 128-byte-swizzled
 //     2-D tensor boxes),
 //   - the matching block scales (one 2-D box),
 //   - the routed tokens' fp16 activation rows for this K chunk (1-D bulk
 //     copies gathered by the expert permutation);
-// warps 1..8 each own 16 weight rows: they dequantize w = (q - mid) * scale
-// into fp16 registers (LOP3/PRMT magic-number conversion, exact for the
+// 16 consumer warps, 8 row groups of 16 weight rows x 2 halves of each
+// stage's K, dequantize w = (q - mid) * scale into fp16 registers (the
+// integer-to-half conversion by placing the code in the mantissa of a
+// power-of-two constant and subtracting it, done with LOP3/PRMT; exact for the
 // integer part) and run mma.sync m16n8k16 with the tokens as the N side,
-// accumulating in fp32.  FC1 applies ReLU / interleaved SwiGLU in the
+// accumulating in fp32; the two K halves of a row group add their partial
+// sums through shared memory.  FC1 applies ReLU / interleaved SwiGLU in the
 // epilogue and writes fp16 activations; FC2 writes fp32 per-slot partial
 // sums per K split, reduced in fixed order by the combine kernel.
 #include <algorithm>

@@ -16,8 +16,11 @@ namespace qmoe {
 // ---------------------------------------------------------------------------
 namespace {
 std::atomic<uint64_t> g_launches{0};
-std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
-std::atomic<int64_t> g_drop_stage{-1};
+// The wait limit and the dropped-stage test hook belong to the host thread that
+// sets them: they apply to the launches that thread makes, so a hook one thread
+// sets cannot make another thread's layer time out.
+thread_local uint64_t t_wait_limit_ns = 2000000000ull;
+thread_local int64_t t_drop_stage = -1;
 
 struct ProfPair {
     cudaEvent_t a = nullptr, b = nullptr;
@@ -29,8 +32,8 @@ size_t g_prof_used = 0;
 bool g_prof_open = false;
 }  // namespace
 
-uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
-int64_t drop_stage() { return g_drop_stage.load(std::memory_order_relaxed); }
+uint64_t wait_limit_ns() { return t_wait_limit_ns; }
+int64_t drop_stage() { return t_drop_stage; }
 
 void note_launch(int kernel_id, cudaStream_t stream, bool begin, int nkernels) {
     if (!begin) g_launches.fetch_add(uint64_t(nkernels), std::memory_order_relaxed);
@@ -532,9 +535,9 @@ qmoe_status qmoe_get_device_error(void* workspace, void* cuda_stream, int32_t* c
     return QMOE_OK;
 }
 
-void qmoe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+void qmoe_set_wait_limit_ns(uint64_t ns) { t_wait_limit_ns = ns ? ns : 1; }
 
-void qmoe_debug_drop_stage(int64_t stage) { g_drop_stage.store(stage < 0 ? -1 : stage); }
+void qmoe_debug_drop_stage(int64_t stage) { t_drop_stage = stage < 0 ? -1 : stage; }
 
 qmoe_status qmoe_profile_begin(int32_t kernel_id) {
     if (kernel_id < QMOE_KERNEL_ROUTE || kernel_id > QMOE_KERNEL_GMM)

@@ -110,9 +110,11 @@ constexpr int kDecodeMaxTokens = 16;  // AUTO takes the decode path up to this m
 // the number of kernels launched in between.
 void note_launch(int kernel_id, cudaStream_t stream, bool begin, int nkernels = 1);
 
-// Process-wide bound on a single in-kernel spin-wait, in nanoseconds.
+// Bound on a single in-kernel spin-wait, in nanoseconds, as set by the calling
+// host thread (each thread has its own).
 uint64_t wait_limit_ns();
-// Pipeline stage the producers skip (test hook), -1 when off.
+// Pipeline stage the producers skip (test hook of the calling host thread), -1
+// when off.
 int64_t drop_stage();
 
 // ---- launchers (return cudaGetLastError()) ----

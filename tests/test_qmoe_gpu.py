@@ -277,3 +277,43 @@ def test_wait_timeout_reports_error_and_recovers(dev, name, path):
     check_routing(sel[tokens], p[tokens], sel_ref, p_ref, name)
     check_outputs(y[tokens], y_ref, name + " after timeout")
     assert q.get_device_error(ws) == q.DEVERR_NONE
+
+
+def test_hooks_apply_to_the_setting_thread_only(dev):
+    """A short wait limit and the dropped-stage hook set by one host thread do not
+    reach a layer that another thread runs: that layer completes without a device
+    error and within the parity bar."""
+    import threading
+
+    import quantized_mixture_experts_gb300 as q
+    from quantized_mixture_experts_gb300 import binding as b
+    wl = [w for w in SMALL if w.name == "prefill_like_rank3"][0]
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(path=q.PATH_GROUPED, **wl.attrs())
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape, attrs))
+    out = {}
+
+    def other_thread():
+        try:
+            out["run"] = run_cuda(inp, wl.attrs(), q.PATH_GROUPED, dev, t=t, workspace=ws)
+            out["err"] = q.get_device_error(ws)
+        except Exception as e:   # reported in the main thread
+            out["exc"] = e
+
+    q.set_wait_limit_ns(50_000_000)
+    b.debug_drop_stage(1)
+    try:
+        th = threading.Thread(target=other_thread)
+        th.start()
+        th.join()
+    finally:
+        b.debug_drop_stage(-1)
+        q.set_wait_limit_ns(2_000_000_000)
+    assert "exc" not in out, out.get("exc")
+    assert out["err"] == q.DEVERR_NONE
+    y, sel, p = out["run"]
+    tokens = np.arange(64, dtype=np.int64)
+    y_ref, sel_ref, p_ref = _reference(wl, inp, tokens)
+    check_routing(sel[tokens], p[tokens], sel_ref, p_ref, wl.name)
+    check_outputs(y[tokens], y_ref, wl.name + " in another thread")
