@@ -18,6 +18,12 @@ logits copied in, the layer, and the output copied back, every step.
 Under torchrun each rank runs an independent replica (weak scaling; the
 layer has no cross-GPU exchange); the elapsed time is the max over ranks.
 
+Run with no --workload, the line is the decode workload's, and the same
+measurements of the prefill, many-small-experts and large-E workloads, taken
+after it in the same process, follow in its "workloads" list (--only leaves
+them out).  Each line's roofline covers the dominant kernel (FC1), with FC2 and
+the whole layer against the same peak under roofline.others.
+
 `--impl reference` times the CPU oracle (the double-precision C restatement
 of the operator pages) on the host cores on a bounded token sample of the
 same workload.
@@ -59,6 +65,8 @@ GMM_METRIC = "GroupedMatMul rows/sec"
 # dense TF32 / dense BF16 tensor throughput, nominal (1.1 and 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
 L2_BYTES = 129 * 1024 * 1024
+# measured after the decode line when no workload is named (the tensor-bound configurations)
+EXTRA_WORKLOADS = ("prefill", "many_small", "large_e")
 
 
 def _env_int(name, default):
@@ -324,7 +332,9 @@ def cpu_baseline(wl, inp):
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def run_gpu(args, wl):
+def run_gpu(args, wl, extra=()):
+    """The bench line of workload `wl`; with `extra`, the same measurements of
+    those workloads, taken after it in this process, go in its `workloads` list."""
     import torch
 
     import __graft_entry__
@@ -337,6 +347,27 @@ def run_gpu(args, wl):
         __graft_entry__.build()
     ranks_barrier(world)
     q.load()
+    line = measure_qmoe(args, wl, args.steps, world, rank, dev)
+    if extra:
+        subs = []
+        for name in extra:
+            steps = args.steps if args.steps_given else DEFAULT_STEPS[name]
+            sub = measure_qmoe(args, WORKLOADS[name], steps, world, rank, dev)
+            torch.cuda.empty_cache()
+            if rank == 0:
+                subs.append(sub)
+        if rank == 0:
+            line["workloads"] = subs
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ranks_done(world)
+
+
+def measure_qmoe(args, wl, steps, world, rank, dev):
+    """One workload's measurements (rank 0 gets the line, other ranks None)."""
+    import torch
+
+    import quantized_mixture_experts_gb300 as q
 
     inp = make_inputs(wl, salt=rank)
     t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
@@ -373,16 +404,17 @@ def run_gpu(args, wl):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid) as clocks:
         start.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         stop.record(stream)
         torch.cuda.synchronize(dev)
     launches = q.launch_count() - launches0
-    n_launch, fc1_ms = kernel_pass(q, step, min(args.steps, 1000), dominant)
+    n_launch, fc1_ms = kernel_pass(q, step, min(steps, 1000), dominant)
+    n_launch2, fc2_ms = kernel_pass(q, step, min(steps, 1000), q.KERNEL_FC2)
     ranks_barrier(world)
     elapsed_ms = start.elapsed_time(stop)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    tokens_total = wl.tokens * args.steps * world
+    tokens_total = wl.tokens * steps * world
     value = tokens_total / (elapsed_ms / 1e3)
 
     # end to end through the host-IO entry point
@@ -392,7 +424,7 @@ def run_gpu(args, wl):
     ws_io = q.alloc_workspace(q.workspace_size(wl.input_shape,
                                                tuple(t["fc1_experts_weights"].shape), attrs,
                                                hostio=True), dev)
-    e2e_steps = max(1, min(args.steps, 2000))
+    e2e_steps = max(1, min(steps, 2000))
 
     def step_io():
         q.qmoe_forward_hostio(hx, hl, t["fc1_experts_weights"], t["fc1_scales"],
@@ -413,8 +445,7 @@ def run_gpu(args, wl):
         raise RuntimeError("host-IO output differs from the device-resident output")
 
     if rank != 0:
-        ranks_done(world)
-        return
+        return None
 
     peaks = measured_peaks()
     avg_ms = fc1_ms / max(1, n_launch)
@@ -430,10 +461,28 @@ def run_gpu(args, wl):
         slots = wl.tokens * wl.k
         algo = fc1_flops(wl, slots)
         achieved = algo / (avg_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] if args.steps * avg_ms > 1000 else peaks["bf16_tflops"]
+        peak = peaks["bf16_tflops_sustained"] if steps * avg_ms > 1000 else peaks["bf16_tflops"]
         unit = "TFLOP/s"
         profile_name = f"grouped_fc1_{wl.name}.md"
         files = ["gemm_tc.cu", "ptx.cuh"]
+    # the second projection and the whole layer against the same peak
+    avg2_ms = fc2_ms / max(1, n_launch2)
+    step_ms = elapsed_ms / steps
+    if bound == "hbm":
+        algo2 = expert_bytes(wl, 2) * touched
+        layer_algo = (expert_bytes(wl, 1) + expert_bytes(wl, 2)) * touched + \
+            inp["input"].nbytes * 2 + inp["router_probs"].nbytes
+        scale = 1e9
+    else:
+        algo2 = layer_flops(wl, wl.tokens * wl.k) - algo
+        layer_algo = layer_flops(wl, wl.tokens * wl.k)
+        scale = 1e12
+    fc2_ach = algo2 / (avg2_ms / 1e3) / scale if avg2_ms > 0 else None
+    layer_ach = layer_algo / (step_ms / 1e3) / scale
+    others = {"FC2": {"kernel_ms": avg2_ms, "launches": n_launch2, "algorithmic": algo2,
+                      "achieved": fc2_ach, "frac": fc2_ach / peak if fc2_ach and peak else None},
+              "layer": {"ms": step_ms, "algorithmic": layer_algo, "achieved": layer_ach,
+                        "frac": layer_ach / peak if peak else None}}
     traffic = ncu_traffic(profile_name, files) if os.path.exists(
         os.path.join(ROOT, "quantized_mixture_experts_gb300", "csrc", files[0])) else None
 
@@ -444,14 +493,15 @@ def run_gpu(args, wl):
                 "parallelism": f"replicas{world}" if world > 1 else "single GPU",
                 "logits_sigma": wl.logit_sigma, "device_error": err})
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded; random packed weights)", "config": cfg,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak if peak else None, "traffic": traffic,
                      "kernel": "FC1", "kernel_ms": avg_ms, "launches": n_launch,
-                     "algorithmic": algo, "peak_source": peaks["source"]},
+                     "algorithmic": algo, "peak_source": peaks["source"],
+                     "others": others},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(inp["input"].nbytes + inp["router_probs"].nbytes),
                 "d2h_bytes_per_step": int(inp["input"].nbytes), "steps": e2e_steps},
@@ -460,8 +510,7 @@ def run_gpu(args, wl):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
-    print(json.dumps(line), flush=True)
-    ranks_done(world)
+    return line
 
 
 # ----------------------------------------------------------------------------
@@ -1025,12 +1074,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode",
+    ap.add_argument("--workload", default=None,
                     choices=sorted(WORKLOADS) + sorted(FLOAT_WORKLOADS) + sorted(QKV_WORKLOADS)
                     + sorted(GMM_WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="without --workload: the decode line alone, no extra workloads")
     args = ap.parse_args()
+    args.steps_given = args.steps is not None
     if args.workload in GMM_WORKLOADS:
         gwl = GMM_WORKLOADS[args.workload]
         if args.steps is None:
@@ -1061,14 +1113,17 @@ def main():
         else:
             run_gpu_float(args, fwl)
         return
-    wl = WORKLOADS[args.workload]
+    # no workload named: the decode line, with the three tensor-bound workloads measured
+    # after it in the same process and listed under "workloads"
+    extra = EXTRA_WORKLOADS if args.workload is None and not args.only else ()
+    wl = WORKLOADS[args.workload or "decode"]
     if args.steps is None:
         args.steps = 10 if args.impl == "reference" else DEFAULT_STEPS[wl.name]
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
-        run_gpu(args, wl)
+        run_gpu(args, wl, extra)
 
 
 if __name__ == "__main__":

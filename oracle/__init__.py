@@ -248,6 +248,51 @@ def moe_activation(h1, inter, act, h3=None, swiglu_fusion=0, alpha=1.0, beta=0.0
     return out
 
 
+def qmoe_batched(x, logits, w1, s1, w2, s2, *, k, expert_weight_bits=4, block_size=0,
+                 activation_type="relu", activation_alpha=1.0, activation_beta=0.0,
+                 swiglu_limit=None):
+    """QMoE layer output for every token, evaluated expert by expert.
+
+    The same steps as qmoe(), for checking whole large batches in seconds:
+    routing (route), dequantisation (dequant_rows) and the activation
+    (activation) are the C restatement's own functions, while the FC1 and FC2
+    products of the tokens routed to one expert are fp64 matrix products
+    (numpy).  A token's k weighted expert outputs are added in expert order
+    rather than in selection order, which differs from qmoe() only by fp64
+    rounding.  Returns (y [T, H] float64, sel [T, k] int32, p [T, k] float64).
+    """
+    xs = _c(x, np.float64)
+    H = xs.shape[-1]
+    xs = xs.reshape(-1, H)
+    T = xs.shape[0]
+    lg = _c(logits, np.float32)
+    E = lg.shape[1]
+    bits = int(expert_weight_bits)
+    fusion = 2 if activation_type == "swiglu" else 1
+    w1a = _c(w1, np.uint8)
+    w2a = _c(w2, np.uint8)
+    s1a = _c(s1, np.float32)
+    s2a = _c(s2, np.float32)
+    I = w1a.shape[1] // fusion
+    sel, p = route(lg, k)
+    y = np.zeros((T, H), dtype=np.float64)
+    if I == 0:
+        return y, sel, p
+    for e in range(E):
+        t_idx, i_idx = np.nonzero(sel == e)
+        if t_idx.size == 0:
+            continue
+        W1 = dequant_rows(w1a[e], s1a[e].reshape(w1a.shape[1], -1), H, bits, int(block_size))
+        W2 = dequant_rows(w2a[e], s2a[e].reshape(H, -1), I, bits, int(block_size))
+        h = xs[t_idx] @ W1.T
+        a = np.empty((t_idx.size, I), dtype=np.float64)
+        for r in range(t_idx.size):
+            a[r] = activation(h[r], I, activation_type, activation_alpha, activation_beta,
+                              swiglu_limit)
+        y[t_idx] += p[t_idx, i_idx][:, None] * (a @ W2.T)
+    return y, sel, p
+
+
 def moe(x, logits, fc1_w, fc2_w, *, k, fc1_bias=None, fc2_bias=None, fc3_w=None,
         fc3_bias=None, activation_type="relu", swiglu_fusion=0, activation_alpha=1.0,
         activation_beta=0.0, swiglu_limit=None, normalize_routing_weights=0,

@@ -138,6 +138,26 @@ def make_inputs(wl: Workload, salt: int = 0) -> dict:
                 fc2_experts_weights=w2, fc2_scales=s2)
 
 
+def tied_logits(T: int, E: int, seed: int, levels: int = 4, scale: float = 0.5) -> np.ndarray:
+    """Router logits with exact ties in almost every row, for the tie-order cases.
+
+    Each logit is ``scale * j`` with j drawn uniformly from ``0 .. levels - 1``,
+    so a row of E > levels experts holds repeated values, and with E much
+    larger than ``levels`` the k-th and (k+1)-th largest values are usually
+    equal.  A fraction of the rows gets one draw shifted by -0.0 or a large
+    margin to vary the pattern.  The values are exact in fp32.
+    """
+    rng = np.random.default_rng(seed)
+    lg = (rng.integers(0, levels, (T, E)).astype(np.float32) * np.float32(scale))
+    flip = rng.random(T) < 0.25
+    cols = rng.integers(0, E, T)
+    lg[flip, cols[flip]] = np.float32(scale * (levels + 2))   # one clear winner
+    zero = lg == 0
+    neg = zero & (rng.random((T, E)) < 0.5)
+    lg[neg] = np.float32(-0.0)                                 # -0 ties with +0
+    return np.ascontiguousarray(lg, dtype=np.float32)
+
+
 def sample_tokens(logits_sel: np.ndarray, T: int, n: int, seed: int) -> np.ndarray:
     """Seeded token subset of size >= n that touches every selected expert.
 

@@ -15,7 +15,8 @@ import pytest
 import oracle
 from helpers import check_outputs, check_routing
 from quantized_mixture_experts_gb300.workloads import (FLOAT_WORKLOADS, FloatWorkload,
-                                                       make_float_inputs, sample_tokens)
+                                                       make_float_inputs, sample_tokens,
+                                                       tied_logits)
 
 pytestmark = pytest.mark.gpu
 
@@ -122,6 +123,32 @@ def test_small_parity_all_tokens(dev, wl, path):
     y, sel, w = _run(wl, _to_dev(inp, dev), path, dev)
     check_routing(sel, w, sel_ref, w_ref, wl.name)
     check_outputs(y, y_ref, f"{wl.name} path {path}")
+
+
+# All-expert softmax routing with exact ties in the logits (so in the
+# probabilities): the oracle takes the k most probable experts ordered by
+# (probability descending, index ascending).  Register selection at 1, 2 and 8
+# slots per lane, the general selection (E > 256), the one-launch and the
+# multi-CTA routing kernels, with and without renormalisation.
+TIES = [
+    FloatWorkload("tie_e8_k2", 70, (16, 64), 64, 64, 8, 2, "relu"),
+    FloatWorkload("tie_e64_k8_norm", 71, (64, 64), 64, 64, 64, 8, "silu", normalize=1),
+    FloatWorkload("tie_e200_k8_multi", 72, (600, 64), 64, 64, 200, 8, "relu", normalize=1),
+    FloatWorkload("tie_e300_k4_general", 73, (40, 64), 64, 64, 300, 4, "gelu"),
+]
+
+
+@pytest.mark.parametrize("wl,path", [pytest.param(w, p, id=f"{w.name}-p{p}")
+                                     for w in TIES for p in _paths(w)])
+def test_tied_logits_select_like_the_oracle(dev, wl, path):
+    inp = make_float_inputs(wl)
+    inp["router_probs"] = tied_logits(wl.tokens, wl.experts, seed=wl.index)
+    srt = -np.sort(-inp["router_probs"], axis=1)
+    assert np.mean(srt[:, wl.k - 1] == srt[:, wl.k]) > 0.3
+    y_ref, sel_ref, w_ref = _reference(wl, inp)
+    y, sel, w = _run(wl, _to_dev(inp, dev), path, dev)
+    check_routing(sel, w, sel_ref, w_ref, f"{wl.name} path {path} (tied logits)")
+    check_outputs(y, y_ref, f"{wl.name} path {path} (tied logits)")
 
 
 def test_tensor_core_path_is_taken(dev):

@@ -12,7 +12,8 @@ import pytest
 
 import oracle
 from helpers import check_outputs, check_routing, run_cuda, to_dev
-from quantized_mixture_experts_gb300.workloads import WORKLOADS, Workload, make_inputs, sample_tokens
+from quantized_mixture_experts_gb300.workloads import (WORKLOADS, Workload, make_inputs,
+                                                       sample_tokens, tied_logits)
 
 pytestmark = pytest.mark.gpu
 
@@ -113,6 +114,75 @@ def test_small_parity_all_tokens(dev, wl, path):
     check_outputs(y, y_ref, f"{wl.name} path {path}")
     if wl.k == 1:
         assert np.all(p == 1.0)
+
+
+# Router logits with exact ties (including -0 against +0) on every routing form:
+# the one-launch small-batch kernel (<= 4096 slots) and the multi-CTA routing
+# kernel, each with the register selection at 1, 2, 4 and 8 slots per lane
+# (E <= 32, 64, 128, 256) and the general selection (E > 256 or k > 32).  The
+# oracle orders the selection by (logit descending, expert index ascending); the
+# selected lists must be identical.
+TIES = [
+    Workload("tie_decode_e8", 60, (8, 256), 256, 256, 8, 2, 4, 32, "swiglu"),
+    Workload("tie_e64_k8", 61, (64, 128), 128, 64, 64, 8, 8, 0, "swiglu"),
+    Workload("tie_e128_k8_multi", 62, (600, 64), 64, 64, 128, 8, 4, 64, "swiglu"),
+    Workload("tie_e150_k8_multi", 63, (600, 64), 64, 64, 150, 8, 4, 32, "swiglu"),
+    Workload("tie_e300_k4_general", 64, (40, 64), 64, 64, 300, 4, 8, 0, "relu"),
+    Workload("tie_e96_k40_general_multi", 65, (120, 64), 64, 64, 96, 40, 4, 0, "relu"),
+]
+
+
+def _tie_cases():
+    return [pytest.param(wl, path, id=f"{wl.name}-p{path}") for wl in TIES
+            for path in _paths(wl)]
+
+
+@pytest.mark.parametrize("wl,path", _tie_cases())
+def test_tied_logits_select_like_the_oracle(dev, wl, path):
+    inp = make_inputs(wl)
+    inp["router_probs"] = tied_logits(wl.tokens, wl.experts, seed=wl.index)
+    y_ref, sel_ref, p_ref = oracle.qmoe(inp["input"], inp["router_probs"],
+                                        inp["fc1_experts_weights"], inp["fc1_scales"],
+                                        inp["fc2_experts_weights"], inp["fc2_scales"],
+                                        nthreads=os.cpu_count() or 1, **wl.attrs())
+    srt = -np.sort(-inp["router_probs"], axis=1)
+    assert np.mean(srt[:, wl.k - 1] == srt[:, wl.k]) > 0.3   # ties at the top-k boundary
+    y, sel, p = run_cuda(inp, wl.attrs(), path, dev)
+    check_routing(sel, p, sel_ref, p_ref, f"{wl.name} path {path} (tied logits)")
+    check_outputs(y, y_ref, f"{wl.name} path {path} (tied logits)")
+
+
+# Scales small enough that fp16 copies of scale-multiplied weights (or of the
+# scales) fall below the fp16 normal range (6.1e-5): 8-bit block-wise scales in
+# U[1e-5, 1e-4], 4-bit in U[1e-4, 1e-3], on every path that takes each shape.
+SMALL_SCALES = [
+    Workload("small_s_8bit_bs32", 66, (300, 256), 256, 256, 8, 2, 8, 32, "swiglu",
+             scale_lo=1e-5, scale_hi=1e-4),
+    Workload("small_s_8bit_bs128_decode", 67, (8, 512), 512, 512, 8, 2, 8, 128, "swiglu",
+             scale_lo=1e-5, scale_hi=1e-4),
+    Workload("small_s_4bit_bs64", 68, (300, 256), 256, 256, 8, 2, 4, 64, "swiglu",
+             scale_lo=1e-4, scale_hi=1e-3),
+    Workload("small_s_4bit_bs16_decode", 69, (8, 512), 512, 512, 8, 2, 4, 16, "swiglu",
+             scale_lo=1e-4, scale_hi=1e-3),
+    Workload("small_s_4bit_bs32_decode", 70, (12, 1024), 1024, 512, 4, 2, 4, 32, "relu",
+             scale_lo=1e-4, scale_hi=1e-3),
+    Workload("small_s_4bit_col", 71, (300, 256), 256, 256, 8, 2, 4, 0, "swiglu",
+             scale_lo=1e-4, scale_hi=1e-3),
+]
+
+
+def _small_scale_cases():
+    return [pytest.param(wl, path, id=f"{wl.name}-p{path}") for wl in SMALL_SCALES
+            for path in _paths(wl)]
+
+
+@pytest.mark.parametrize("wl,path", _small_scale_cases())
+def test_small_scales_parity(dev, wl, path):
+    inp = make_inputs(wl)
+    y_ref, sel_ref, p_ref = _reference(wl, inp)
+    y, sel, p = run_cuda(inp, wl.attrs(), path, dev)
+    check_routing(sel, p, sel_ref, p_ref, wl.name)
+    check_outputs(y, y_ref, f"{wl.name} path {path}")
 
 
 def test_repeat_is_bit_identical(dev):
@@ -246,6 +316,27 @@ def test_full_size_parity(dev, name):
         y, sel, p = y[tokens], sel[tokens], p[tokens]
     check_routing(sel, p, sel_ref, p_ref, name)
     check_outputs(y, y_ref, name)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefill", "many_small", "large_e"])
+def test_full_size_parity_every_token(dev, name):
+    """The three large workloads at full size, in the bench's launch
+    configuration, compared with the oracle on every token (the oracle's batched
+    evaluation: per-expert fp64 matrix products, pinned to the token-by-token
+    restatement on the CPU)."""
+    import quantized_mixture_experts_gb300 as q
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    y, sel, p = run_cuda(inp, wl.attrs(), q.PATH_AUTO, dev)
+    y_ref, sel_ref, p_ref = oracle.qmoe_batched(
+        inp["input"], inp["router_probs"], inp["fc1_experts_weights"], inp["fc1_scales"],
+        inp["fc2_experts_weights"], inp["fc2_scales"], **wl.attrs())
+    check_routing(sel, p, sel_ref, p_ref, name + " (every token)")
+    check_outputs(y, y_ref, name + " (every token)")
+    # and token by token: no token's error hides in the whole-batch norms
+    err = np.linalg.norm(y - y_ref, axis=1) / np.maximum(np.linalg.norm(y_ref, axis=1), 1e-300)
+    assert err.max() <= 4 * 5e-3, f"{name}: worst token rel-L2 {err.max():.3e}"
 
 
 @pytest.mark.parametrize("name,path", [("decode", 1), ("prefill_like_rank3", 2)])
