@@ -1,0 +1,823 @@
+// Grouped path of the QMoE layer: expert-grouped GEMMs on CTA pairs of the
+// 5th-generation tensor cores (tcgen05.mma.cta_group::2), dequantising the
+// packed expert weights on the way into shared memory.
+//
+// QMoE manifest passes QMoE.FC1ActivationStageGrouped / QMoE.OutputStageGrouped
+// (tiles of one expert's routed tokens against that expert's weights,
+// derive.groupMaxTiles) and GroupedMatMul-29 Summary (a runtime should fuse
+// DequantizeLinear + GroupedMatMul so the dequantized [G, K, N] weights are
+// never materialised).
+//
+// One work item = (token tile: up to 256 expert-sorted rows of one expert,
+// 256-row weight tile of that expert), computed by a cluster of two CTAs:
+//   D[256 tokens, 256 weight rows] = X[256, K] * deq(W)[256, K]^T
+// The tokens are the MMA's A operand (M = 256: 128 rows in each CTA's shared
+// memory), the dequantised weights its B operand (N = 256: each CTA
+// dequantises 128 of the rows), and each CTA's tensor memory receives its 128
+// token rows x 256 columns.  Two 256-column accumulators alternate between
+// items, so the epilogue of one item runs while the next item's MMAs run, and
+// a thread of the epilogue owns one token row: its outputs leave as whole
+// 16-byte pieces of that row without a transpose.
+//
+// Per CTA (persistent, one per SM), warp-specialised, a ring of stages each
+// holding the K = 64 slice of the CTA's 128 token rows, its 128 packed weight
+// rows with their block scales, and the dequantised fp16 weight rows:
+//   warp 0      TMA producer: packed weights and staged block scales (2-D
+//               tensor boxes), the token rows (one 1-D bulk copy: the rows are
+//               stored K-blocked with the 128-byte swizzle already applied);
+//   warp 1      tensor-memory allocation; in CTA 0 of the pair, one lane
+//               issues the MMAs of both CTAs and commits their completion to
+//               both CTAs' barriers;
+//   warps 2-9   dequantisers: (q - mid) * scale in fp16, written in the
+//               128-byte-swizzled K-major layout; two groups of four warps take
+//               alternate stages (one thread per weight row), so two stages are
+//               converted at once; they arrive on CTA 0's operand barrier;
+//   warps 10-17 epilogue: FC1 ReLU / SwiGLU to fp16 activations in the
+//               K-blocked layout FC2 reads; FC2 rows per routing slot, already
+//               multiplied by the slot's routing weight (fp16; the combine adds
+//               a token's k rows in fixed order).
+// Every wait is bounded; on expiry the CTA records QMOE_DEVERR_TIMEOUT, stops,
+// and both CTAs meet at the final cluster barrier before freeing tensor memory.
+#include <algorithm>
+#include <cstring>
+
+#include "ptx.cuh"
+#include "qmoe_internal.h"
+#include "tma_host.h"
+
+namespace qmoe {
+namespace {
+
+constexpr int kRowsCta = 128;         // token rows and weight rows per CTA of a pair
+constexpr int kTileRows = 2 * kRowsCta;
+constexpr int kK = 64;                // K per stage: one 128-byte row of fp16
+constexpr int kMaxStages = 6;        // ring depth upper bound (the launch picks what fits)
+constexpr int kDeqWarps = 8;          // two groups of four: one thread per weight row of the CTA
+constexpr int kDeqGroupWarps = 4;     // warps of a group (the group takes every other stage)
+constexpr int kEpiWarps = 8;          // two per TMEM lane quadrant (one per column half)
+constexpr int kWarps = 2 + kDeqWarps + kEpiWarps;
+constexpr int kThreads = 32 * kWarps;
+constexpr uint32_t kAccCols = 256;    // accumulator columns (N) of one item
+constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr uint32_t kABytes = kRowsCta * 128;   // token rows of one stage
+constexpr uint32_t kBBytes = kRowsCta * 128;   // dequantised weight rows of one stage
+constexpr uint32_t kSBytes = kRowsCta * 16;    // four staged scale blocks per row
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint64_t kDrainWaitNs = 200000000ull;
+
+struct PairArgs {
+    CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
+    CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 128}
+    const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
+    const int32_t* tiles;       // header + (expert, first sorted row, rows, expert's first tile)
+    const int32_t* counts;      // slots per expert
+    const int32_t* perm;        // sorted position -> slot
+    const float* pw;            // routing weight of each slot
+    const __half* bsrc;         // token rows, K-blocked [K/64][srows][64], pre-swizzled
+    int64_t srows;
+    int64_t N, K;               // weight rows per expert, reduction length
+    int64_t n_out;              // valid output columns: I (FC1 activations) or H (FC2)
+    int nb, lbs;                // scale blocks per row; log2(block size) (-1: column-wise)
+    int n_mt, gm;               // weight tiles per expert; weight tiles per item group
+    __half* act_out;            // FC1 output, K-blocked like bsrc
+    int act, has_limit;
+    float alpha, beta, limit;
+    __half* slot16;             // FC2 output: [slots, n_out] fp16, weighted by routing weight
+    int32_t* err;
+    uint64_t wait_ns;
+    int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
+    int scale_vec;              // column-wise scales 16-byte aligned (read four at a time)
+    int64_t drop_it;            // test hook: stage whose copies the producer skips
+    uint32_t stage_bytes, off_b, off_raw, off_s, raw_bytes, nstages;
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t(1) << 16;                 // leading byte offset (unused for this layout)
+    d |= uint64_t(1024 >> 4) << 32;         // stride byte offset between 8-row atoms
+    d |= uint64_t(1) << 46;                 // descriptor version
+    d |= uint64_t(2) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: fp16 A and B (K-major), fp32 accumulator, M x N.
+__device__ __forceinline__ uint32_t f16_idesc(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// One MMA of the pair (issued by CTA 0): A = 256 token rows, 128 from each
+// CTA's shared memory at the same offset; B = 256 weight rows, 128 from each.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` (same offset in both CTAs) when the issuing thread's MMAs complete.
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(ptx::smem_u32(bar)), "h"(uint16_t(3))
+        : "memory");
+}
+
+__device__ __forceinline__ void commit_local(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(ptx::smem_u32(bar))
+        : "memory");
+}
+
+// Arrive with the default (release, CTA scope) semantics on the barrier at
+// shared::cluster address `addr` (CTA 0's copy).  The dequantisers publish
+// their shared-memory writes to the tensor core with fence.proxy.async before
+// arriving.
+__device__ __forceinline__ void arrive_remote(uint32_t addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float swiglu(float g, float u, float alpha, float beta, int has_limit,
+                                        float limit) {
+    if (has_limit) {
+        g = fminf(g, limit);
+        u = fminf(fmaxf(u, -limit), limit);
+    }
+    return __fdividef(g, 1.f + __expf(-alpha * g)) * (u + beta);
+}
+
+__device__ __forceinline__ float pick4(float4 v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// The integer-to-half conversions below use the exponent-bias method: with the
+// exponent of a power-of-two constant fixed, an integer written into the low
+// mantissa bits gives constant + integer exactly, and subtracting the
+// constant leaves the integer.  Its use for int4/int8 weight dequantisation is
+// described by Kim et al., "Who Says Elephants Can't Run: Bringing Large Scale
+// MoE Models into Cloud Scale Production" (2022).
+//
+// Eight packed 4-bit codes (low nibble first) -> four fp16 pairs
+// ((q0,q4),(q1,q5),(q2,q6),(q3,q7)) of (q - 8) [* s]: one 16-byte piece of a
+// row in the order the 4-bit path stores its activations in every group of
+// eight.  A low nibble in the mantissa of fp16 1024 gives 1024 + q; a high
+// nibble left in place gives 1024 + 16 q, whose pairs are scaled by s / 16
+// (1/16 when unscaled), which is exact.
+template <bool SCALE>
+__device__ __forceinline__ void deq4(uint32_t w, __half2 s, __half2 s16, uint32_t* out) {
+    const __half2 lo_bias = ptx::u32_as_h2(0x64086408u);   // 1032
+    const __half2 hi_bias = ptx::u32_as_h2(0x64806480u);   // 1152 = 1024 + 16 * 8
+    const uint32_t w8 = w >> 8;
+    const __half2 d0 = __hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x000F000Fu, 0x64006400u)), lo_bias);
+    const __half2 d1 = __hsub2(ptx::u32_as_h2(ptx::and_or(w, 0x00F000F0u, 0x64006400u)), hi_bias);
+    const __half2 d2 = __hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x000F000Fu, 0x64006400u)), lo_bias);
+    const __half2 d3 = __hsub2(ptx::u32_as_h2(ptx::and_or(w8, 0x00F000F0u, 0x64006400u)), hi_bias);
+    out[0] = ptx::h2_as_u32(SCALE ? __hmul2(d0, s) : d0);
+    out[1] = ptx::h2_as_u32(__hmul2(d1, s16));
+    out[2] = ptx::h2_as_u32(SCALE ? __hmul2(d2, s) : d2);
+    out[3] = ptx::h2_as_u32(__hmul2(d3, s16));
+}
+
+// Four 8-bit codes -> natural-order fp16 pairs ((q0,q1),(q2,q3)) of (q - 128) [* s].
+template <bool SCALE>
+__device__ __forceinline__ void deq8(uint32_t w, __half2 s, uint32_t* out) {
+    const __half2 bias = ptx::u32_as_h2(0x64806480u);
+    const __half2 d0 = __hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4140u)), bias);
+    const __half2 d1 = __hsub2(ptx::u32_as_h2(ptx::prmt(w, 0x64646464u, 0x4342u)), bias);
+    out[0] = ptx::h2_as_u32(SCALE ? __hmul2(d0, s) : d0);
+    out[1] = ptx::h2_as_u32(SCALE ? __hmul2(d1, s) : d1);
+}
+
+// Two fp32 values -> one fp16 pair (round to nearest even).
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    return ptx::h2_as_u32(__floats2half2_rn(a, b));
+}
+
+struct Item {
+    int e, row0, rows, m;       // expert, first sorted row of the tile, its rows, weight tile
+};
+
+// Position in a ring of n stages: slot and the parity of its current phase,
+// advanced without divisions (the issuing thread's per-stage work is on the
+// tensor pipe's critical path).
+struct Ring {
+    uint32_t sl = 0, ph = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++sl == n) {
+            sl = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Work item i.  An expert's items are contiguous: with its token tiles
+// tau0 .. tau0 + nt - 1, they are items tau0 * n_mt .. (tau0 + nt) * n_mt - 1,
+// in groups of gm weight tiles, inside a group token tile by token tile, so
+// that the items running at the same time share weight tiles and token tiles
+// in L2 and each weight tile is read from DRAM about once.
+__device__ __forceinline__ Item pair_item(const PairArgs& a, int64_t i) {
+    const int tg = int(i / a.n_mt);                    // a token tile of the same expert
+    const int e = __ldg(a.tiles + kTileHeader + 4 * tg);
+    const int tau0 = __ldg(a.tiles + kTileHeader + 4 * tg + 3);
+    const int nt = (__ldg(a.counts + e) + kTileRows - 1) / kTileRows;
+    const int64_t idx = i - int64_t(tau0) * a.n_mt;
+    const int per_group = nt * a.gm;
+    const int g = int(idx / per_group), rem = int(idx - int64_t(g) * per_group);
+    const int tau = tau0 + rem / a.gm;
+    Item it;
+    it.e = e;
+    it.row0 = __ldg(a.tiles + kTileHeader + 4 * tau + 1);
+    it.rows = __ldg(a.tiles + kTileHeader + 4 * tau + 2);
+    it.m = g * a.gm + rem % a.gm;
+    return it;
+}
+
+template <int BITS, bool FC1, bool SCOL>
+__global__ void __launch_bounds__(kThreads, 1)
+    pair_gemm_kernel(const __grid_constant__ PairArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t ld_full[kMaxStages];    // this CTA's copies landed
+    __shared__ __align__(8) uint64_t op_full[kMaxStages];    // CTA 0: both CTAs' operands ready
+    __shared__ __align__(8) uint64_t st_free[kMaxStages];    // the stage's MMAs completed
+    __shared__ __align__(8) uint64_t acc_full[2];            // an item's MMAs completed
+    __shared__ __align__(8) uint64_t acc_empty[2];           // CTA 0: both epilogues done
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_flag;
+    constexpr int PACK = BITS == 4 ? 2 : 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_rank();
+    const bool leader = rank == 0;
+    const uint32_t S = a.nstages;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            ptx::mbar_init(&ld_full[s], 1);
+            ptx::mbar_init(&op_full[s], 2 * kDeqGroupWarps);
+            ptx::mbar_init(&st_free[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], 2 * kEpiWarps);
+        }
+        ptx::mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(ptx::smem_u32(&tmem_base_s)), "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    ptx::cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_base_s;
+
+    // the combine after FC2 may start its prologue on SMs this grid leaves
+    ptx::griddep_launch_dependents();
+    const int64_t items = int64_t(__ldg(a.tiles)) * a.n_mt;
+    const int nkb = int(a.K / kK);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    const int64_t first = blockIdx.x >> 1, step = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            ptx::prefetch_tmap(&a.tm_w);
+            if (a.scale_tma) ptx::prefetch_tmap(&a.tm_s);
+        }
+        uint32_t it = 0;
+        Ring r;
+        bool ok = true;
+        for (int64_t i = first; i < items && ok; i += step) {
+            const Item w = pair_item(a, i);
+            const int n_a = min(max(w.rows - int(rank) * kRowsCta, 0), kRowsCta);
+            const int32_t wrow = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTileRows +
+                                         int(rank) * kRowsCta);
+            const __half* asrc = a.bsrc + (int64_t(w.row0) + int(rank) * kRowsCta) * kK;
+            for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
+                const uint32_t sl = r.sl;
+                if (!ptx::mbar_wait(&st_free[sl], r.ph ^ 1u, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (int64_t(it) == a.drop_it) continue;   // test hook: this stage never fills
+                if (lane == 0) {
+                    uint8_t* sp = smem + size_t(sl) * a.stage_bytes;
+                    const bool scales = a.scale_tma != 0;   // the group of four blocks of this stage
+                    ptx::mbar_arrive_expect_tx(&ld_full[sl], a.raw_bytes + (scales ? kSBytes : 0u) +
+                                                                 uint32_t(n_a) * 128u);
+                    ptx::tma_load_2d(sp + a.off_raw, &a.tm_w, kb * (kK / PACK), wrow, &ld_full[sl]);
+                    if (scales)
+                        ptx::tma_load_2d(sp + a.off_s, &a.tm_s, ((kb * kK) >> a.lbs) & ~3, wrow,
+                                         &ld_full[sl]);
+                    if (n_a > 0)
+                        ptx::bulk_g2s(sp, asrc + int64_t(kb) * a.srows * kK, uint32_t(n_a) * 128u,
+                                      &ld_full[sl]);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+            for (uint32_t j = it > S ? it - S : 0; j < it; ++j) {
+                volatile int never = 0;
+                ptx::mbar_wait(&ld_full[j % S], (j / S) & 1u, kDrainWaitNs, &never);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------- MMA issuer (CTA 0) ---------------------------
+        if (leader) {
+            uint32_t item_it = 0;
+            Ring r;
+            bool ok = true, issued = false;
+            const uint32_t idesc = f16_idesc(2 * kRowsCta, kTileRows);
+            for (int64_t i = first; i < items && ok; i += step, ++item_it) {
+                const uint32_t b = item_it & 1u;
+                // both CTAs' epilogues released this accumulator: acquire at cluster scope
+                if (!ptx::mbar_wait_cluster(&acc_empty[b], ((item_it >> 1) & 1u) ^ 1u, a.wait_ns,
+                                            &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + b * kAccCols;
+                for (int kb = 0; kb < nkb; ++kb, r.next(S)) {
+                    const uint32_t sl = r.sl;
+                    if (!ptx::mbar_wait(&op_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = sbase + sl * a.stage_bytes;
+                        const uint32_t sb = sa + a.off_b;
+#pragma unroll
+                        for (int kk = 0; kk < kK / 16; ++kk)
+                            mma_pair(d, sw128_desc(sa + 32u * kk), sw128_desc(sb + 32u * kk), idesc,
+                                     (kb | kk) != 0 ? 1u : 0u);
+                        commit_both(&st_free[sl]);
+                        issued = true;
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) commit_both(&acc_full[b]);
+                __syncwarp();
+            }
+            if (!ok && lane == 0) {
+                record_error(a.err, QMOE_DEVERR_TIMEOUT);
+                abort_flag = 1;
+            }
+            if (lane == 0 && issued) {
+                // every MMA this thread issued completes before tensor memory is released
+                commit_local(&drain_bar);
+                volatile int never = 0;
+                ptx::mbar_wait(&drain_bar, 0, kDrainWaitNs, &never);
+            }
+            __syncwarp();
+        }
+    } else if (warp < 2 + kDeqWarps) {
+        // ------------------------------ dequantisers ------------------------------
+        // two groups of four warps take alternate stages; a thread converts one whole
+        // weight row (64 K values) of its group's stages
+        const int grp = (warp - 2) / kDeqGroupWarps;                 // 0 or 1
+        const int rr = (threadIdx.x - 64) & (kRowsCta - 1);         // weight row of this CTA's 128
+        const uint32_t op_addr = ptx::leader_addr(&op_full[0]);
+        uint32_t it = 0;
+        Ring r;
+        bool ok = true;
+        for (int64_t i = first; i < items && ok; i += step) {
+            const Item w = pair_item(a, i);
+            const int64_t row = int64_t(w.m) * kTileRows + int(rank) * kRowsCta + rr;
+            const bool valid = row < a.N;
+            const float* srow = a.scales + (int64_t(w.e) * a.N + (valid ? row : 0)) * a.nb;
+            for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
+                if (int(it & 1u) != grp) continue;
+                const uint32_t sl = r.sl;
+                if (!ptx::mbar_wait(&ld_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sp = ptx::launder(sbase + sl * a.stage_bytes);
+                // block scales of the four 16-wide quarters of this stage's K range (the
+                // group of four staged blocks starting at block ((kb * 64) >> lbs) & ~3);
+                // column-wise scales are applied to the accumulator instead
+                __half2 sq[4];
+                if (SCOL) {
+                    sq[0] = sq[1] = sq[2] = sq[3] = __float2half2_rn(1.f);
+                } else {
+                    float4 s4;
+                    const int b0 = (kb * kK) >> a.lbs;                 // block of K value 0
+                    if (a.scale_tma) {
+                        s4 = ptx::ld_f32x4(sp + a.off_s + uint32_t(rr) * 16u);
+                    } else {
+                        const int g0 = b0 & ~3;
+                        s4.x = valid && g0 < a.nb ? __ldg(srow + g0) : 0.f;
+                        s4.y = valid && g0 + 1 < a.nb ? __ldg(srow + g0 + 1) : 0.f;
+                        s4.z = valid && g0 + 2 < a.nb ? __ldg(srow + g0 + 2) : 0.f;
+                        s4.w = valid && g0 + 3 < a.nb ? __ldg(srow + g0 + 3) : 0.f;
+                    }
+                    if (a.lbs >= 6) {              // one block for the whole stage
+                        const __half2 v = __float2half2_rn(pick4(s4, b0 & 3));
+                        sq[0] = sq[1] = sq[2] = sq[3] = v;
+                    } else if (a.lbs == 5) {       // blocks of 32: two per stage
+                        sq[0] = sq[1] = __float2half2_rn(pick4(s4, b0 & 3));
+                        sq[2] = sq[3] = __float2half2_rn(pick4(s4, (b0 & 3) + 1));
+                    } else {                       // blocks of 16: four per stage
+                        sq[0] = __float2half2_rn(s4.x);
+                        sq[1] = __float2half2_rn(s4.y);
+                        sq[2] = __float2half2_rn(s4.z);
+                        sq[3] = __float2half2_rn(s4.w);
+                    }
+                }
+                const uint32_t brow = sp + a.off_b + uint32_t(rr) * 128u;
+                const uint32_t rawb = sp + a.off_raw;
+                if (BITS == 4) {
+                    // 32 packed bytes (64 codes) staged with the 32-byte swizzle: 16-byte
+                    // piece c of row r sits at piece c ^ ((r >> 2) & 1)
+                    const uint32_t x = uint32_t(rr >> 2) & 1u;
+                    const uint4 p0 = ptx::lds128(rawb + uint32_t(rr) * 32u + ((0u ^ x) << 4));
+                    const uint4 p1 = ptx::lds128(rawb + uint32_t(rr) * 32u + ((1u ^ x) << 4));
+                    const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                    const __half2 inv16 = __float2half2_rn(0.0625f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {   // word q: K 8q .. 8q + 7 -> 16-byte piece q
+                        uint32_t o[4];
+                        if (SCOL) deq4<false>(wv[q], sq[0], inv16, o);
+                        else deq4<true>(wv[q], sq[q >> 1], __hmul2(sq[q >> 1], inv16), o);
+                        const uint32_t addr = brow + ((uint32_t(q) ^ uint32_t(rr & 7)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(o[0]),
+                                     "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                    }
+                } else {
+                    // 64 packed bytes staged with the 64-byte swizzle: 16-byte piece c of
+                    // row r sits at piece c ^ ((r >> 1) & 3)
+                    const uint32_t x = uint32_t(rr >> 1) & 3u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {   // piece c: K 16c .. 16c + 15
+                        const uint4 pc = ptx::lds128(rawb + uint32_t(rr) * 64u + ((uint32_t(c) ^ x) << 4));
+                        const uint32_t wv[4] = {pc.x, pc.y, pc.z, pc.w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (SCOL) deq8<false>(wv[q], sq[0], o + 2 * q);
+                            else deq8<true>(wv[q], sq[c], o + 2 * q);
+                        }
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const uint32_t addr =
+                                brow + ((uint32_t(2 * c + hh) ^ uint32_t(rr & 7)) << 4);
+                            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+                                         "r"(o[4 * hh]), "r"(o[4 * hh + 1]), "r"(o[4 * hh + 2]),
+                                         "r"(o[4 * hh + 3])
+                                         : "memory");
+                        }
+                    }
+                }
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) arrive_remote(op_addr + sl * 8u);
+            }
+        }
+        if (!ok && lane == 0) {
+            record_error(a.err, QMOE_DEVERR_TIMEOUT);
+            abort_flag = 1;
+        }
+    } else {
+        // -------------------------------- epilogue --------------------------------
+        const int ew = warp - 2 - kDeqWarps;       // 0..7
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int chalf = ew >> 2;                 // column half: weight rows 128 * chalf ..
+        const int tr = quad * 32 + lane;           // token row of this CTA's 128
+        const int grow = int(rank) * kRowsCta + tr;   // row within the token tile
+        const uint32_t empty_addr = ptx::leader_addr(&acc_empty[0]);
+        // outputs outside the fp16 range: the largest magnitude and a NaN-propagating
+        // sum of every output this lane stores, checked once at the end
+        float omax = 0.f, osum = 0.f;
+        uint32_t item_it = 0;
+        for (int64_t i = first; i < items; i += step, ++item_it) {
+            const Item w = pair_item(a, i);
+            const uint32_t b = item_it & 1u;
+            const bool valid_row = grow < w.rows;
+            const int64_t c_base = int64_t(w.m) * kTileRows + chalf * 128;   // first column
+            int slot = 0;
+            float p = 0.f;
+            if (!FC1 && valid_row) {
+                slot = __ldg(a.perm + w.row0 + grow);
+                p = __ldg(a.pw + slot);
+            }
+            if (!ptx::mbar_wait(&acc_full[b], (item_it >> 1) & 1u, a.wait_ns, &abort_flag)) {
+                if (lane == 0) {
+                    record_error(a.err, QMOE_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols +
+                                   uint32_t(chalf * 128);
+            const float* csc = a.scales + int64_t(w.e) * a.N;   // column-wise scales
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                const int64_t col0 = c_base + c0;                // weight row of column c0
+                float v[32];
+                tmem_ld32(tbase + uint32_t(c0), v);
+                if (SCOL) {
+                    // one scale per weight row (column of D), the same for the whole warp
+                    if (a.scale_vec) {
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4) {
+                            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (col0 + q < a.N)
+                                s4 = __ldg(reinterpret_cast<const float4*>(csc + col0 + q));
+                            v[q] *= s4.x;
+                            v[q + 1] *= s4.y;
+                            v[q + 2] *= s4.z;
+                            v[q + 3] *= s4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) v[q] *= col0 + q < a.N ? __ldg(csc + col0 + q) : 0.f;
+                    }
+                }
+                // rows past the tile's tokens compute (their outputs are not stored); the
+                // loop stays uniform across the warp for the collective tensor-memory loads
+                if (FC1) {
+                    if (a.act == QMOE_ACT_SWIGLU) {
+                        // columns (2j, 2j + 1) = (gate, linear) -> 16 activations j0 .. j0 + 15
+                        const int64_t j0 = col0 >> 1;
+                        if (j0 >= a.n_out) continue;
+                        float o[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            o[q] = valid_row ? swiglu(v[2 * q], v[2 * q + 1], a.alpha, a.beta,
+                                                      a.has_limit, a.limit)
+                                             : 0.f;
+                            omax = fmaxf(omax, fabsf(o[q]));
+                            osum += o[q];
+                        }
+                        uint4 pc[2];
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            const float* og = o + 8 * g;
+                            if (BITS == 4)   // the 4-bit operand order 0,4,1,5,2,6,3,7
+                                pc[g] = make_uint4(pack_h2(og[0], og[4]), pack_h2(og[1], og[5]),
+                                                   pack_h2(og[2], og[6]), pack_h2(og[3], og[7]));
+                            else
+                                pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
+                                                   pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            a.act_out + ((j0 / kK) * a.srows + w.row0 + grow) * kK);
+                        const int ch = int(j0 % kK) / 8;
+                        if (valid_row) {
+                            dst[(ch) ^ (grow & 7)] = pc[0];
+                            dst[(ch + 1) ^ (grow & 7)] = pc[1];
+                        }
+                    } else {
+                        const int64_t j0 = col0;
+                        if (j0 >= a.n_out) continue;
+                        uint4 pc[4];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            float og[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                og[q] = valid_row ? fmaxf(v[8 * g + q], 0.f) : 0.f;
+                                omax = fmaxf(omax, og[q]);
+                            }
+                            if (BITS == 4)
+                                pc[g] = make_uint4(pack_h2(og[0], og[4]), pack_h2(og[1], og[5]),
+                                                   pack_h2(og[2], og[6]), pack_h2(og[3], og[7]));
+                            else
+                                pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
+                                                   pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            a.act_out + ((j0 / kK) * a.srows + w.row0 + grow) * kK);
+                        const int ch = int(j0 % kK) / 8;
+                        if (valid_row) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) dst[(ch + g) ^ (grow & 7)] = pc[g];
+                        }
+                    }
+                } else {
+                    // FC2: 32 output columns of the slot's row, times its routing weight
+                    if (col0 >= a.n_out) continue;
+                    uint4 pc[4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float og[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            og[q] = valid_row ? v[8 * g + q] * p : 0.f;
+                            omax = fmaxf(omax, fabsf(og[q]));
+                            osum += og[q];
+                        }
+                        pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
+                                           pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(a.slot16 + int64_t(slot) * a.n_out + col0);
+                    if (valid_row) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) dst[g] = pc[g];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(empty_addr + b * 8u);
+        }
+        const bool bad = !(omax <= 65504.f) || osum != osum;
+        if (__any_sync(kFull, bad) && lane == 0) record_error(a.err, QMOE_DEVERR_NONFINITE);
+    }
+
+    tc_fence_before();
+    ptx::cluster_sync();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+template <int BITS, bool FC1, bool SCOL>
+cudaError_t launch_pair(const PairArgs& args, int pairs, size_t smem, cudaStream_t s) {
+    auto kern = pair_gemm_kernel<BITS, FC1, SCOL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * unsigned(pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, args);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int BITS, bool FC1, bool SCOL>
+int max_pairs(size_t smem) {
+    auto kern = pair_gemm_kernel<BITS, FC1, SCOL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 256);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
+    return clusters;
+}
+
+int ilog2(int64_t v) {
+    int l = 0;
+    while ((int64_t(1) << l) < v) ++l;
+    return l;
+}
+
+// Weight tiles per item group: a divisor of the expert's weight-tile count, at
+// most 16 (a group's weight tiles and the expert's token tiles stay in L2).
+int pick_group(int n_mt) {
+    for (int g = 16; g > 1; --g)
+        if (n_mt % g == 0) return g;
+    return 1;
+}
+
+}  // namespace
+
+int grouped_tile_tokens() { return kTileRows; }
+
+bool grouped_shape_ok(const Problem& p) {
+    if (p.H % kK != 0 || p.I % kK != 0) return false;
+    return true;
+}
+
+cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, bool fc1,
+                              cudaStream_t s) {
+    PairArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const uint8_t* wt = fc1 ? p.w1 : p.w2;
+    a.N = fc1 ? p.fusion * p.I : p.H;
+    a.K = fc1 ? p.H : p.I;
+    a.n_out = fc1 ? p.I : p.H;
+    a.nb = int(fc1 ? p.nb1 : p.nb2);
+    a.lbs = p.bs ? ilog2(p.bs) : -1;
+    a.scales = fc1 ? p.s1 : p.s2;
+    const int pack = p.pack;
+    // packed rows: 32 bytes per stage (4-bit) or 64 (8-bit), staged with the 32- or
+    // 64-byte swizzle so that the dequantisers' reads of a row's pieces spread over
+    // all banks
+    if (!encode_tmap_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wt, uint64_t(a.K / pack),
+                        uint64_t(p.E * a.N), uint64_t(a.K / pack), uint32_t(kK / pack), kRowsCta,
+                        pack == 1 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B))
+        return cudaErrorInvalidValue;
+    a.bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
+    a.srows = pl.srows;
+    a.scale_tma = (p.bs != 0 && a.nb % 4 == 0) ? 1 : 0;
+    a.scale_vec = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 ? 1 : 0;
+    if (a.scale_tma &&
+        !encode_tmap_2d(&a.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, uint64_t(a.nb),
+                        uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kRowsCta,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    a.tiles = w.tiles;
+    a.counts = w.counts;
+    a.perm = w.perm;
+    a.pw = w.pw;
+    a.n_mt = int((a.N + kTileRows - 1) / kTileRows);
+    a.gm = pick_group(a.n_mt);
+    a.act_out = static_cast<__half*>(w.act);
+    a.act = p.act;
+    a.has_limit = p.has_limit;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.limit = p.limit;
+    a.slot16 = reinterpret_cast<__half*>(w.slot_out);
+    a.err = w.ctrl;
+    a.wait_ns = wait_limit_ns();
+    a.drop_it = drop_stage();
+    // stage: token rows | dequantised weight rows | packed rows | staged scales
+    a.raw_bytes = uint32_t(kRowsCta * (kK / pack));
+    a.off_b = kABytes;
+    a.off_raw = kABytes + kBBytes;
+    a.off_s = a.off_raw + a.raw_bytes;
+    a.stage_bytes = (a.off_s + kSBytes + 1023u) & ~1023u;
+    const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
+    a.nstages = uint32_t(std::min<size_t>(kMaxStages, (smem_cap - 1024) / a.stage_bytes));
+    if (a.nstages < 2) return cudaErrorInvalidValue;
+    const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes;
+    const bool scol = p.bs == 0;
+    int cap = 0;
+#define QMOE_PAIR_CAP(B, C) (fc1 ? max_pairs<B, true, C>(smem) : max_pairs<B, false, C>(smem))
+    if (p.bits == 4) cap = scol ? QMOE_PAIR_CAP(4, true) : QMOE_PAIR_CAP(4, false);
+    else cap = scol ? QMOE_PAIR_CAP(8, true) : QMOE_PAIR_CAP(8, false);
+#undef QMOE_PAIR_CAP
+    if (cap <= 0) cap = device_sm_count() / 2;
+    const int64_t items_max = pl.max_tiles * a.n_mt;
+    const int pairs = int(std::max<int64_t>(1, std::min<int64_t>(items_max, cap)));
+    const int kid = fc1 ? QMOE_KERNEL_FC1 : QMOE_KERNEL_FC2;
+    note_launch(kid, s, true);
+    cudaError_t e;
+#define QMOE_PAIR_LAUNCH(B, C) \
+    (fc1 ? launch_pair<B, true, C>(a, pairs, smem, s) : launch_pair<B, false, C>(a, pairs, smem, s))
+    if (p.bits == 4) e = scol ? QMOE_PAIR_LAUNCH(4, true) : QMOE_PAIR_LAUNCH(4, false);
+    else e = scol ? QMOE_PAIR_LAUNCH(8, true) : QMOE_PAIR_LAUNCH(8, false);
+#undef QMOE_PAIR_LAUNCH
+    note_launch(kid, s, false);
+    return e;
+}
+
+}  // namespace qmoe

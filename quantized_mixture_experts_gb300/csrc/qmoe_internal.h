@@ -88,7 +88,7 @@ struct Work {
     int32_t* rank;        // [T*k] stable rank of a slot within its chunk and expert
     int32_t* perm;        // [T*k] sorted position -> slot (t*k+i)
     int32_t* inv;         // [T*k] slot -> sorted position
-    int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, 0)
+    int32_t* tiles;       // [4 + 4*max_tiles] header + (expert, row0, rows, expert's first tile)
     int32_t* active;      // [E] experts with at least one slot, ascending
     __half* x16;          // [T*Hp] fp16 copy of the activations (decode path)
     __half* xs16;         // grouped path: fp16 activations in expert-sorted slot order,

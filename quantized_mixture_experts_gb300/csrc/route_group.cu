@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(1024) route_group_small_kernel(
                 tt[0] = e;
                 tt[1] = s_off[e] + j * tile_tokens;
                 tt[2] = min(tile_tokens, cnt - j * tile_tokens);
-                tt[3] = 0;
+                tt[3] = s_tb[e];
             }
         }
     }
@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(
         }
     }
     __syncthreads();
-    // Phase 5: tile table entries (expert, first sorted row, rows, 0).
+    // Phase 5: tile table entries (expert, first sorted row, rows, the expert's first tile).
     if (tile_tokens > 0) {
         for (int e = tid; e < E; e += nthr) {
             const int32_t cnt = counts[e];
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(
                 tt[0] = e;
                 tt[1] = row0 + j * tile_tokens;
                 tt[2] = min(tile_tokens, cnt - j * tile_tokens);
-                tt[3] = 0;
+                tt[3] = base;
             }
         }
     }
