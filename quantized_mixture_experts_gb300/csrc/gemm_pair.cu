@@ -28,11 +28,13 @@
 //   warp 1      tensor-memory allocation; in CTA 0 of the pair, one lane
 //               issues the MMAs of both CTAs and commits their completion to
 //               both CTAs' barriers;
-//   warps 2-9   dequantisers: (q - mid) * scale in fp16, written in the
+//   warps 2-4, 6-8, 10-11
+//               dequantisers: (q - mid) * scale in fp16, written in the
 //               128-byte-swizzled K-major layout; two groups of four warps take
 //               alternate stages (one thread per weight row), so two stages are
-//               converted at once; they arrive on CTA 0's operand barrier;
-//   warps 10-17 epilogue: FC1 ReLU / SwiGLU to fp16 activations in the
+//               converted at once; they arrive on CTA 0's operand barrier
+//               (warps 5 and 9 stay idle: see kEpiWarp0);
+//   warps 12-19 epilogue: FC1 ReLU / SwiGLU to fp16 activations in the
 //               K-blocked layout FC2 reads; FC2 rows per routing slot, already
 //               multiplied by the slot's routing weight (fp16; the combine adds
 //               a token's k rows in fixed order).
@@ -55,7 +57,11 @@ constexpr int kMaxStages = 6;        // ring depth upper bound (the launch picks
 constexpr int kDeqWarps = 8;          // two groups of four: one thread per weight row of the CTA
 constexpr int kDeqGroupWarps = 4;     // warps of a group (the group takes every other stage)
 constexpr int kEpiWarps = 8;          // two per TMEM lane quadrant (one per column half)
-constexpr int kWarps = 2 + kDeqWarps + kEpiWarps;
+// Warp roles.  A warp runs on scheduler (warp % 4); the MMA-issuing warp 1
+// shares scheduler 1 only with epilogue warps and two idle warps (5, 9), so
+// the dequantisers' arithmetic does not delay the issue of the next stage.
+constexpr int kEpiWarp0 = 12;         // warps 12-19: epilogue
+constexpr int kWarps = kEpiWarp0 + kEpiWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr uint32_t kAccCols = 256;    // accumulator columns (N) of one item
 constexpr uint32_t kTmemCols = 2 * kAccCols;
@@ -413,12 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-    } else if (warp < 2 + kDeqWarps) {
+    } else if (warp < kEpiWarp0 && warp != 5 && warp != 9) {
         // ------------------------------ dequantisers ------------------------------
         // two groups of four warps take alternate stages; a thread converts one whole
         // weight row (64 K values) of its group's stages
-        const int grp = (warp - 2) / kDeqGroupWarps;                 // 0 or 1
-        const int rr = (threadIdx.x - 64) & (kRowsCta - 1);         // weight row of this CTA's 128
+        const int d = warp - 2 - (warp > 5 ? 1 : 0) - (warp > 9 ? 1 : 0);   // 0..7
+        const int grp = d / kDeqGroupWarps;                          // 0 or 1
+        const int rr = (d % kDeqGroupWarps) * 32 + lane;             // weight row of this CTA's 128
         const uint32_t op_addr = ptx::leader_addr(&op_full[0]);
         uint32_t it = 0;
         Ring r;
@@ -521,9 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             record_error(a.err, QMOE_DEVERR_TIMEOUT);
             abort_flag = 1;
         }
-    } else {
+    } else if (warp >= kEpiWarp0) {
         // -------------------------------- epilogue --------------------------------
-        const int ew = warp - 2 - kDeqWarps;       // 0..7
+        const int ew = warp - kEpiWarp0;           // 0..7
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int chalf = ew >> 2;                 // column half: weight rows 128 * chalf ..
         const int tr = quad * 32 + lane;           // token row of this CTA's 128
