@@ -95,6 +95,7 @@ struct PairArgs {
     int scale_vec;              // column-wise scales 16-byte aligned (read four at a time)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t stage_bytes, off_b, off_raw, off_s, raw_bytes, nstages;
+    uint32_t off_epi;           // FC2 epilogue staging: 2 KB per epilogue warp, after the ring
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -647,9 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 } else {
-                    // FC2: 32 output columns of the slot's row, times its routing weight
+                    // FC2: 32 output columns (64 bytes) of the slot's row, times its routing
+                    // weight.  The warp's 32 rows go through its staging tile (16-byte piece
+                    // j of row r at piece j ^ ((r >> 1) & 3), conflict-free both ways) so
+                    // that each store instruction writes 8 rows x 64 contiguous bytes.
                     if (col0 >= a.n_out) continue;
-                    uint4 pc[4];
+                    const uint32_t stg = sbase + a.off_epi + uint32_t(ew) * 2048u;
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         float og[8];
@@ -659,14 +663,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             omax = fmaxf(omax, fabsf(og[q]));
                             osum += og[q];
                         }
-                        pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
-                                           pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
+                        const uint32_t addr =
+                            stg + uint32_t(lane) * 64u + ((uint32_t(g) ^ ((uint32_t(lane) >> 1) & 3u)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+                                     "r"(pack_h2(og[0], og[1])), "r"(pack_h2(og[2], og[3])),
+                                     "r"(pack_h2(og[4], og[5])), "r"(pack_h2(og[6], og[7]))
+                                     : "memory");
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(a.slot16 + int64_t(slot) * a.n_out + col0);
-                    if (valid_row) {
+                    __syncwarp();
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) dst[g] = pc[g];
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 8 * i + (lane >> 2);          // row of the warp's 32
+                        const int j = lane & 3;                     // its 16-byte piece
+                        const uint4 val = ptx::lds128(
+                            stg + uint32_t(r) * 64u + ((uint32_t(j) ^ ((uint32_t(r) >> 1) & 3u)) << 4));
+                        const int rslot = __shfl_sync(kFull, slot, r);
+                        const bool rvalid = __shfl_sync(kFull, valid_row ? 1 : 0, r) != 0;
+                        if (rvalid)
+                            reinterpret_cast<uint4*>(a.slot16 + int64_t(rslot) * a.n_out + col0)[j] = val;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -796,16 +812,19 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.err = w.ctrl;
     a.wait_ns = wait_limit_ns();
     a.drop_it = drop_stage();
-    // stage: token rows | dequantised weight rows | packed rows | staged scales
+    // stage: token rows | dequantised weight rows | packed rows | staged scales (block-wise
+    // only); after the ring, the FC2 epilogue's staging tiles
     a.raw_bytes = uint32_t(kRowsCta * (kK / pack));
     a.off_b = kABytes;
     a.off_raw = kABytes + kBBytes;
     a.off_s = a.off_raw + a.raw_bytes;
-    a.stage_bytes = (a.off_s + kSBytes + 1023u) & ~1023u;
+    a.stage_bytes = (a.off_s + (p.bs != 0 ? kSBytes : 0u) + 1023u) & ~1023u;
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
-    a.nstages = uint32_t(std::min<size_t>(kMaxStages, (smem_cap - 1024) / a.stage_bytes));
+    const size_t epi = fc1 ? 0 : size_t(kEpiWarps) * 2048;
+    a.nstages = uint32_t(std::min<size_t>(kMaxStages, (smem_cap - 1024 - epi) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;
-    const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes;
+    a.off_epi = a.nstages * a.stage_bytes;
+    const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes + epi;
     const bool scol = p.bs == 0;
     int cap = 0;
 #define QMOE_PAIR_CAP(B, C) (fc1 ? max_pairs<B, true, C>(smem) : max_pairs<B, false, C>(smem))
