@@ -173,16 +173,31 @@ struct Proj3 {
     void* out[3];
 };
 
-// out_p[r, n] = sum over the K splits of the GEMV's partial sums, in split order
-// (every split's load issued before the sum).
+// Where the GEMV's range split shares a row block among CTAs, out_p[r, n] =
+// the sum of their partial sums in slot order (every slot's load issued before
+// the sum); the GEMV stored the other row blocks itself.  The sharing follows
+// the GEMV's split: CTA c of G holds flat (row block, K chunk) pairs
+// [c * total / G, (c + 1) * total / G).
+struct QkvSplit {
+    int64_t nkc, total, grid;
+    int64_t nrb0, nrb1;     // row blocks of projections 0 and 1
+};
+
+__device__ __forceinline__ int qkv_cta_of(int64_t f, const QkvSplit& sp) {
+    return int(((f + 1) * sp.grid - 1) / sp.total);
+}
+
 template <typename T>
 __global__ void qkv_reduce_kernel(Proj3 pj, const float* __restrict__ p0, const float* __restrict__ p1,
-                                  const float* __restrict__ p2, int splits, int64_t rows) {
+                                  const float* __restrict__ p2, QkvSplit sp, int64_t rows) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     int p = 0;
     while (p < 3 && idx >= rows * pj.N[p]) idx -= rows * pj.N[p++];
     if (p >= 3) return;
+    const int64_t rbg = (idx % pj.N[p]) / kQkvRowBlock + (p > 0 ? sp.nrb0 : 0) + (p > 1 ? sp.nrb1 : 0);
+    const int splits = qkv_cta_of(rbg * sp.nkc + sp.nkc - 1, sp) - qkv_cta_of(rbg * sp.nkc, sp) + 1;
+    if (splits == 1) return;   // stored by the GEMV
     const float* part = p == 0 ? p0 : (p == 1 ? p1 : p2);
     const int64_t stride = rows * pj.N[p];
     float s = 0.f;
@@ -350,13 +365,18 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
         g.splits = q.splits;
         g.err = err;
         if ((e = launch_qkv_gemv(g, s)) != cudaSuccess) return e;
-        if (q.splits == 1) return cudaSuccess;   // the GEMV wrote the results
+        if (q.splits == 1) return cudaSuccess;   // every row block inside one CTA: stored
         const int64_t total = p.rows * (p.N[0] + p.N[1] + p.N[2]);
+        QkvSplit sp;
+        int64_t n_rb = 0;
+        qkv_gemv_geometry(p.N, p.K, &sp.nkc, &n_rb, &sp.total, &sp.grid);
+        sp.nrb0 = (p.N[0] + kQkvRowBlock - 1) / kQkvRowBlock;
+        sp.nrb1 = (p.N[1] + kQkvRowBlock - 1) / kQkvRowBlock;
         note_launch(QMOE_KERNEL_COMBINE, s, true);
         e = launch_dependent(qkv_reduce_kernel<T>, dim3(unsigned((total + 255) / 256)), dim3(256), 0,
                              s, pj, static_cast<const float*>(g.part[0]),
                              static_cast<const float*>(g.part[1]),
-                             static_cast<const float*>(g.part[2]), q.splits, p.rows);
+                             static_cast<const float*>(g.part[2]), sp, p.rows);
         note_launch(QMOE_KERNEL_COMBINE, s, false);
         return e != cudaSuccess ? e : cudaGetLastError();
     }

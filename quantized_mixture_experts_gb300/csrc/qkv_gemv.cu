@@ -16,8 +16,14 @@ namespace {
 // ---------------------------------------------------------------------------
 // The same GEMV over the three weight tensors of a Q/K/V projection
 // (com.microsoft.MatMulNBitsQkv manifest, pass MatMulNBitsQkv.Projection):
-// every row of the input is "routed" to each projection.  A work unit is
-// (projection, 128-row block, K split); units of projection 0 come first.
+// every row of the input is "routed" to each projection.
+//
+// Work split (stream-K): the (128-row block, K chunk) pairs of the three
+// projections, row block by row block, form one flat range that the CTAs cut
+// into equal contiguous pieces, so every SM streams the same number of K chunks
+// with one pipeline ramp.  A row block inside one CTA's range is stored
+// directly; one that two or three CTAs share leaves a partial sum per CTA (slot
+// = the CTA's position among them), added in slot order by the reduction.
 // ---------------------------------------------------------------------------
 struct QkvArgs {
     CUtensorMap tm_w[3];        // packed weights [N_p rows, K/2 bytes], 128-byte swizzle
@@ -26,19 +32,44 @@ struct QkvArgs {
     int64_t b_pitch;
     int64_t N[3];
     int n_rb[3];
-    int64_t ubound[2];          // first unit of projection 1 and of projection 2
-    int64_t units;
+    int64_t total;              // flat (row block, K chunk) pairs of the three projections
     int64_t K;
-    int rows, nkc, splits, cps, nsc;
+    int rows, nkc, nsc;
     uint32_t stage_bytes, off_s, off_b, pitch_b, nstages, ssize;
-    float* part[3];             // [splits][rows][N_p] partial sums (splits > 1)
-    void* out[3];               // [rows][N_p] results, fp32 or fp16 (out_f16), splits == 1
+    float* part[3];             // [slots][rows][N_p] partial sums of shared row blocks
+    void* out[3];               // [rows][N_p] results, fp32 or fp16 (out_f16)
     int out_f16;
     int32_t* err;
     uint64_t wait_ns;
 };
 
-// Result element idx of projection p (K not split).
+// CTA (of G) whose range holds flat chunk f: the last c with floor(c * total / G) <= f.
+__device__ __forceinline__ int cta_of(int64_t f, int64_t total, int64_t G) {
+    return int(((f + 1) * G - 1) / total);
+}
+
+// The part of flat range [f, fend) inside the row block of chunk f.
+struct Piece {
+    int p, rb;        // projection, row block within it
+    int c0, c1;       // K chunks
+    int slot, n;      // this CTA's position among the CTAs sharing the row block; their count
+};
+
+__device__ __forceinline__ Piece piece_at(const QkvArgs& a, int64_t f, int64_t fend) {
+    const int64_t rbg = f / a.nkc;
+    Piece pc;
+    pc.p = rbg < a.n_rb[0] ? 0 : (rbg < a.n_rb[0] + a.n_rb[1] ? 1 : 2);
+    pc.rb = int(rbg - (pc.p > 0 ? a.n_rb[0] : 0) - (pc.p > 1 ? a.n_rb[1] : 0));
+    const int64_t f0 = rbg * a.nkc;
+    pc.c0 = int(f - f0);
+    pc.c1 = int(min(int64_t(a.nkc), fend - f0));
+    const int clo = cta_of(f0, a.total, gridDim.x);
+    pc.slot = int(blockIdx.x) - clo;
+    pc.n = cta_of(f0 + a.nkc - 1, a.total, gridDim.x) - clo + 1;
+    return pc;
+}
+
+// Result element idx of projection p (row block not shared).
 __device__ __forceinline__ void qkv_store(const QkvArgs& a, int p, int64_t idx, float v) {
     if (a.out_f16) static_cast<__half*>(a.out[p])[idx] = __float2half_rn(v);
     else static_cast<float*>(a.out[p])[idx] = v;
@@ -74,12 +105,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
     }
     __syncthreads();
     ptx::griddep_launch_dependents();
-    const int64_t units = a.units;
-    auto unit_proj = [&](int64_t u, int64_t* v) {
-        const int p = u < a.ubound[0] ? 0 : (u < a.ubound[1] ? 1 : 2);
-        *v = u - (p == 0 ? 0 : a.ubound[p - 1]);
-        return p;
-    };
+    // this CTA's flat chunk range
+    const int64_t fbeg = int64_t(blockIdx.x) * a.total / gridDim.x;
+    const int64_t fend = (int64_t(blockIdx.x) + 1) * a.total / gridDim.x;
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
@@ -109,13 +137,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
             held = 0;
             dep_done = true;
         };
-        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int64_t v;
-            const int p = unit_proj(u, &v);
-            const int ks = int(v % a.splits);
-            const int rb = int(v / a.splits);
-            const int c0 = ks * a.cps, c1 = min(a.nkc, c0 + a.cps);
-            const int32_t row0 = rb * kDecRows;
+        for (int64_t f = fbeg; f < fend && ok;) {
+            const Piece pc = piece_at(a, f, fend);
+            f += pc.c1 - pc.c0;
+            const int p = pc.p;
+            const int c0 = pc.c0, c1 = pc.c1;
+            const int32_t row0 = pc.rb * kDecRows;
             for (int kc = c0; kc < c1; ++kc, ++it, ring.advance(a.nstages)) {
                 const uint32_t st = ring.st;
                 if (!dep_done && it >= a.nstages) release_held();
@@ -190,13 +217,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
     const int ne = a.rows;
     Ring ring;
     uint32_t un = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++un) {
-        int64_t v;
-        const int p = unit_proj(u, &v);
-        const int ks = int(v % a.splits);
-        const int rb = int(v / a.splits);
-        const int c0 = ks * a.cps, c1 = min(a.nkc, c0 + a.cps);
-        const int64_t rg = int64_t(rb) * kDecRows + r_g;
+    for (int64_t f = fbeg; f < fend; ++un) {
+        const Piece pc = piece_at(a, f, fend);
+        f += pc.c1 - pc.c0;
+        const int p = pc.p;
+        const int c0 = pc.c0, c1 = pc.c1;
+        const int64_t rg = int64_t(pc.rb) * kDecRows + r_g;
         const int64_t rg8 = rg + 8;
         float acc[2][4];
         const bool ok = ne > 8
@@ -236,7 +262,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
             if (lane == 0) ptx::mbar_arrive(&red_empty[rb_buf]);
         }
         const int64_t Np = a.N[p];
-        if (a.splits == 1) {
+        if (pc.n == 1) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -248,7 +274,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
                 }
             continue;
         }
-        float* part = a.part[p] + int64_t(ks) * a.rows * Np;
+        float* part = a.part[p] + int64_t(pc.slot) * a.rows * Np;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -269,30 +295,33 @@ bool qkv_gemv_shape_ok(int64_t K, bool scales_f16) {
     return true;
 }
 
-// Split K so that the units (projection x 128-row block x K split) spread evenly
-// over the SMs: minimise the K chunks of the most loaded SM, counting 1.5 chunks
-// of fixed cost per unit (pipeline ramp, K-half hand-off, stores) and 2 chunks
-// for the partial-sum reduction that any split needs.
-int qkv_gemv_splits(const int64_t N[3], int64_t K) {
+static_assert(kDecRows == kQkvRowBlock, "row block of the GEMV and of its reduction");
+
+// (row block, K chunk) pairs of the three projections and the GEMV's grid.
+void qkv_gemv_geometry(const int64_t N[3], int64_t K, int64_t* nkc, int64_t* n_rb,
+                       int64_t* total, int64_t* grid) {
     const int64_t KC = int64_t(kChunkBytes) * 2;
-    const int64_t nkc = (K + KC - 1) / KC;
-    int64_t n_rb = 0;
-    for (int p = 0; p < 3; ++p) n_rb += (N[p] + kDecRows - 1) / kDecRows;
-    const int64_t sms = device_sm_count();
-    int64_t best = 1;
-    double best_cost = 0.0;
-    for (int64_t cps = nkc; cps >= 1; --cps) {
-        const int64_t splits = (nkc + cps - 1) / cps;
-        if ((nkc + splits - 1) / splits != cps) continue;   // same cps as the launch derives
-        const int64_t units = n_rb * splits;
-        const double cost = double((units + sms - 1) / sms) * (double(cps) + 1.5) +
-                            (splits > 1 ? 2.0 : 0.0);
-        if (best_cost == 0.0 || cost < best_cost) {
-            best_cost = cost;
-            best = splits;
-        }
-    }
-    return int(best);
+    *nkc = (K + KC - 1) / KC;
+    *n_rb = 0;
+    for (int p = 0; p < 3; ++p) *n_rb += (N[p] + kDecRows - 1) / kDecRows;
+    *total = *n_rb * *nkc;
+    *grid = std::max<int64_t>(1, std::min<int64_t>(*total, device_sm_count()));
+}
+
+namespace {
+int host_cta_of(int64_t f, int64_t total, int64_t G) { return int(((f + 1) * G - 1) / total); }
+}  // namespace
+
+// Partial-sum slots the GEMV needs: the most CTAs that share one row block
+// (1 when every row block lies inside one CTA's range).
+int qkv_gemv_splits(const int64_t N[3], int64_t K) {
+    int64_t nkc, n_rb, total, G;
+    qkv_gemv_geometry(N, K, &nkc, &n_rb, &total, &G);
+    int most = 1;
+    for (int64_t rb = 0; rb < n_rb; ++rb)
+        most = std::max(most, host_cta_of(rb * nkc + nkc - 1, total, G) -
+                                  host_cta_of(rb * nkc, total, G) + 1);
+    return most;
 }
 
 cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
@@ -322,13 +351,11 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
     a.b_pitch = q.b_pitch;
     a.K = q.K;
     a.rows = q.rows;
-    a.nkc = int((q.K + KC - 1) / KC);
-    a.cps = (a.nkc + q.splits - 1) / q.splits;
-    a.splits = (a.nkc + a.cps - 1) / a.cps;
-    if (a.splits != q.splits) return cudaErrorInvalidValue;   // every split must own K chunks
-    a.ubound[0] = int64_t(a.n_rb[0]) * a.splits;
-    a.ubound[1] = a.ubound[0] + int64_t(a.n_rb[1]) * a.splits;
-    a.units = a.ubound[1] + int64_t(a.n_rb[2]) * a.splits;
+    int64_t nkc, n_rb, total, grid;
+    qkv_gemv_geometry(q.N, q.K, &nkc, &n_rb, &total, &grid);
+    if (qkv_gemv_splits(q.N, q.K) > q.splits) return cudaErrorInvalidValue;   // slots planned
+    a.nkc = int(nkc);
+    a.total = total;
     const uint32_t bytes_a = 2 * kBoxTile;
     const uint32_t bytes_s = uint32_t(kDecRows) * a.nsc * a.ssize;
     a.pitch_b = uint32_t(KC * 2 + 64);
@@ -342,7 +369,7 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
     a.nstages = uint32_t(std::min<size_t>(kDecStages, (smem_cap - 1024 - kDecRedBytes) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;
     const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes + kDecRedBytes;
-    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(a.units, device_sm_count())));
+
     auto kern = q.scales_f16 ? qkv_gemv_kernel<true> : qkv_gemv_kernel<false>;
     // the shared-memory limit is raised once per kernel (not inside a stream capture)
     static std::atomic<size_t> smem_set[2] = {{0}, {0}};
@@ -354,7 +381,7 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
         cur.store(smem);
     }
     note_launch(QMOE_KERNEL_FC1, s, true);
-    e = launch_dependent(kern, dim3(grid), dim3(kDecThreads), smem, s, a);
+    e = launch_dependent(kern, dim3(unsigned(grid)), dim3(kDecThreads), smem, s, a);
     note_launch(QMOE_KERNEL_FC1, s, false);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -35,8 +35,15 @@ struct QkvGemvParams {
 };
 
 constexpr int kQkvDecodeRows = 16;   // rows the GEMV path takes
+constexpr int kQkvRowBlock = 128;    // weight rows per GEMV work piece
+
+// The GEMV's flat work range: K chunks per row, (row block, K chunk) pairs of the
+// three projections, and its grid (each CTA takes an equal contiguous piece).
+void qkv_gemv_geometry(const int64_t N[3], int64_t K, int64_t* nkc, int64_t* n_rb,
+                       int64_t* total, int64_t* grid);
 
 bool qkv_gemv_shape_ok(int64_t K, bool scales_f16);
+// Partial-sum slots of the GEMV: the most CTAs that share one row block.
 int qkv_gemv_splits(const int64_t N[3], int64_t K);
 cudaError_t launch_qkv_gemv(const QkvGemvParams& p, cudaStream_t s);
 
