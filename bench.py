@@ -58,12 +58,14 @@ DEFAULT_STEPS = {"tiny": 2000, "decode": 8000, "prefill": 100, "many_small": 100
                  "large_e": 100, "float_tiny": 2000, "float_decode": 1000, "float_prefill": 40,
                  "float_prefill_e4": 100, "qkv_tiny": 2000, "qkv_decode": 5000,
                  "qkv_decode_f32": 5000, "qkv_decode_wide": 2000, "gmm_tiny": 2000,
-                 "gmm_prefill": 200, "gmm_prefill_bf16": 200}
+                 "gmm_prefill": 200, "gmm_prefill_bf16": 200, "gmm_prefill_f32": 40, "gmm_prefill_f64": 3}
 QKV_METRIC = "QKV projection rows/sec"
 FLOAT_METRIC = "MoE layer tokens/sec"
 GMM_METRIC = "GroupedMatMul rows/sec"
 # dense TF32 / dense BF16 tensor throughput, nominal (1.1 and 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
+# nominal dense fp64 rate of the part (TFLOP/s)
+FP64_TFLOPS_NOMINAL = 1.25
 L2_BYTES = 129 * 1024 * 1024
 # measured after the decode line when no workload is named (the tensor-bound configurations)
 EXTRA_WORKLOADS = ("prefill", "many_small", "large_e")
@@ -920,8 +922,10 @@ def gmm_config(wl):
 
 
 def gmm_rounded(a, dtype):
-    """float32 host array -> float64 holding the values of the workload's 16-bit type."""
+    """float32 host array -> float64 holding the values of the workload's type."""
     import torch
+    if dtype in ("float32", "float64"):
+        return np.asarray(a, dtype=np.float64)
     tdt = torch.float16 if dtype == "float16" else torch.bfloat16
     return torch.from_numpy(np.ascontiguousarray(a)).to(tdt).double().numpy()
 
@@ -983,7 +987,8 @@ def run_gpu_gmm(args, wl):
     ranks_barrier(world)
     q.load()
     inp = make_gmm_inputs(wl, salt=rank)
-    tdt = torch.float16 if wl.dtype == "float16" else torch.bfloat16
+    tdt = {"float16": torch.float16, "bfloat16": torch.bfloat16, "float32": torch.float32,
+           "float64": torch.float64}[wl.dtype]
     x = torch.from_numpy(inp["input"]).to(dev).to(tdt)
     w = torch.from_numpy(inp["weights"]).to(dev).to(tdt)
     idx = torch.from_numpy(inp["group_indices"]).to(dev)
@@ -1049,8 +1054,17 @@ def run_gpu_gmm(args, wl):
     peaks = measured_peaks()
     avg_ms = gemm_ms / max(1, n_launch)
     achieved = wl.flops / (avg_ms / 1e3) / 1e12
-    # f16 and bf16 have the same nominal dense rate: the measured bf16 peak serves both
+    # f16 and bf16 have the same nominal dense rate: the measured bf16 peak serves both.
+    # f32 runs as three TF32 products per step: its peak is the measured bf16 peak x the
+    # nominal TF32 / BF16 ratio (1.1 / 2.25), and a third of that bounds the f32 rate.
     peak = peaks["bf16_tflops_sustained"] if args.steps * avg_ms > 1000 else peaks["bf16_tflops"]
+    bound = "tensor"
+    if wl.dtype == "float32":
+        peak = peak * TF32_PER_BF16
+    elif wl.dtype == "float64":
+        # fp64 runs on the general kernel (GB300's fp64 tensor rate is no faster): its
+        # ceiling is the nominal fp64 rate, no measured figure exists for it
+        peak, bound = FP64_TFLOPS_NOMINAL, "alu"
     cfg = gmm_config(wl)
     cfg.update({"l2": f"weights {w.numel() * 2 / 1e9:.2f} GB per step exceed the 129 MB L2; "
                       "no flush",
@@ -1060,13 +1074,15 @@ def run_gpu_gmm(args, wl):
         "metric": GMM_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16" if wl.dtype == "float16" else "bf16",
+        "dtype": {"float16": "f16", "bfloat16": "bf16", "float32": "f32 (3 x tf32)",
+                  "float64": "f64"}[wl.dtype],
         "data": "synthetic (seeded; uniform activations and weights)", "config": cfg,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak if peak else None,
                      "traffic": ncu_traffic(f"gmm_tc_{wl.name}.md", ["gemm_f16.cu", "ptx.cuh"]),
                      "kernel": "GroupedMatMul GEMM", "kernel_ms": avg_ms, "launches": n_launch,
-                     "algorithmic": wl.flops, "peak_source": peaks["source"]},
+                     "algorithmic": wl.flops,
+                     "peak_source": ("nominal fp64" if wl.dtype == "float64" else peaks["source"])},
         "e2e": {"value": e2e_value, "unit": "rows/s",
                 "h2d_bytes_per_step": int(hx.numel() * 2 + hi.numel() * 8),
                 "d2h_bytes_per_step": int(ho.numel() * 2), "steps": e2e_steps},

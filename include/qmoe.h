@@ -312,7 +312,7 @@ typedef enum {
     QMOE_KERNEL_FC1 = 2,
     QMOE_KERNEL_FC2 = 3,
     QMOE_KERNEL_COMBINE = 4,
-    QMOE_KERNEL_GMM = 5              /* grouped_matmul's tensor-core GEMM        */
+    QMOE_KERNEL_GMM = 5              /* grouped_matmul's GEMM                    */
 } qmoe_kernel_id;
 
 /*
@@ -324,7 +324,8 @@ typedef enum {
  *     launches, FC1 / FC2 the two expert projections, COMBINE the weighted sum;
  *   matmul_nbits_qkv (qkv.h): ROUTE the RMSNorm kernel, FC1 the Q/K/V
  *     projection, COMBINE the split-K reduction;
- *   grouped_matmul: GMM its tensor-core GEMM.  qmoe_profile_end synchronizes those events and returns how many
+ *   grouped_matmul: GMM its GEMM (the tensor-core kernel or the general one).
+ * qmoe_profile_end synchronizes those events and returns how many
  * launches were bracketed and their summed duration in milliseconds, then
  * stops recording.
  */

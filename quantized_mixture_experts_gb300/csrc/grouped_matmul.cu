@@ -135,7 +135,7 @@ cudaError_t launch_grouped_matmul(const void* input, int64_t M, int64_t K, const
                                   int64_t G, int64_t N, const void* idx, int64_t S, int idx64,
                                   const void* bias, void* out, int dtype, int32_t* err,
                                   cudaStream_t s) {
-    note_launch(-1, s, true);
+    note_launch(QMOE_KERNEL_GMM, s, true);
     cudaError_t e;
     switch (dtype) {
         case QMOE_DT_F32: e = run_t<float>(input, M, K, weights, G, N, idx, S, idx64, bias, out, err, s); break;
@@ -143,7 +143,7 @@ cudaError_t launch_grouped_matmul(const void* input, int64_t M, int64_t K, const
         case QMOE_DT_BF16: e = run_t<__nv_bfloat16>(input, M, K, weights, G, N, idx, S, idx64, bias, out, err, s); break;
         default: e = run_t<double>(input, M, K, weights, G, N, idx, S, idx64, bias, out, err, s); break;
     }
-    note_launch(-1, s, false);
+    note_launch(QMOE_KERNEL_GMM, s, false);
     return e;
 }
 

@@ -352,7 +352,7 @@ class GmmWorkload:
     G: int
     N: int
     S: int
-    dtype: str = "float16"       # float16 | bfloat16
+    dtype: str = "float16"       # float16 | bfloat16 | float32 | float64
 
     @property
     def flops(self) -> int:
@@ -364,6 +364,8 @@ GMM_WORKLOADS = {
     "gmm_prefill": GmmWorkload("gmm_prefill", 81, 4096, 4096, 8, 28672, 2),
     "gmm_prefill_bf16": GmmWorkload("gmm_prefill_bf16", 82, 4096, 4096, 8, 28672, 2,
                                     "bfloat16"),
+    "gmm_prefill_f32": GmmWorkload("gmm_prefill_f32", 83, 4096, 4096, 8, 28672, 2, "float32"),
+    "gmm_prefill_f64": GmmWorkload("gmm_prefill_f64", 84, 4096, 4096, 8, 28672, 2, "float64"),
 }
 
 

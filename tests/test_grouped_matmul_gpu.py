@@ -152,6 +152,70 @@ def test_tensor_core_path_vs_oracle(dev, dt, shape, idt):
     _oracle_check(out2, x, w, idx, b, dt, K)
 
 
+def _oracle_check_f32(out, x, w, idx, b, K):
+    xr, wr = x.double().cpu().numpy(), w.double().cpu().numpy()
+    br = None if b is None else b.double().cpu().numpy()
+    ix = idx.cpu().numpy()
+    ref, st = oracle.grouped_matmul(xr, wr, ix, br)
+    assert st == oracle.OK
+    mag = np.einsum("mk,mskn->msn", np.abs(xr), np.abs(wr)[ix])
+    if br is not None:
+        mag = mag + np.abs(br)[ix]
+    bound = 2 * (K + 2) * 2.0 ** -24 * mag + 2.0 ** -24 * np.abs(ref) + 1e-300
+    err = np.abs(out.double().cpu().numpy() - ref)
+    assert np.all(err <= bound), float(np.max(err / bound))
+
+
+@pytest.mark.parametrize("shape,idt", [((600, 512, 7, 384, 2), "int32"),
+                                       ((300, 128, 40, 200, 3), "int64"),
+                                       ((17, 64, 3, 8, 1), "int32"),
+                                       ((257, 96, 2, 100, 2), "int64")],
+                         ids=["tiles_bias", "ragged_n_i64", "tiny", "partial_tile"])
+def test_f32_tensor_core_path_vs_oracle(dev, shape, idt):
+    """f32 with K % 32 == 0 and N % 4 == 0 takes the tensor-core path (three TF32
+    products per step) and is held to the same fp32 bound as the general kernel."""
+    import quantized_mixture_experts_gb300 as q
+    M, K, G, N, S = shape
+    rng = np.random.default_rng(sum(shape) + 32)
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(dev)
+    w = torch.from_numpy(rng.standard_normal((G, K, N)).astype(np.float32)).to(dev)
+    b = torch.from_numpy(rng.standard_normal((G, N)).astype(np.float32)).to(dev)
+    idx = torch.from_numpy(rng.integers(0, G, (M, S))).to(getattr(torch, idt)).to(dev)
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(M, K, G, N, S, torch.float32))
+    n0 = _launches()
+    out = q.grouped_matmul(x, w, idx, b, workspace=ws)
+    torch.cuda.synchronize()
+    assert _launches() - n0 > 2   # grouping, gather, GEMM
+    assert q.get_device_error(ws) == q.DEVERR_NONE
+    _oracle_check_f32(out, x, w, idx, b, K)
+    # without bias, and against the general kernel's result under the same bound
+    out_nb = q.grouped_matmul(x, w, idx, workspace=ws)
+    torch.cuda.synchronize()
+    _oracle_check_f32(out_nb, x, w, idx, None, K)
+
+
+def test_f32_tensor_core_path_invalid_index(dev):
+    import quantized_mixture_experts_gb300 as q
+    M, K, G, N, S = 40, 64, 3, 64, 2
+    x = torch.ones((M, K), dtype=torch.float32, device=dev)
+    w = torch.ones((G, K, N), dtype=torch.float32, device=dev) / 64
+    idx = torch.zeros((M, S), dtype=torch.int64, device=dev)
+    idx[3, 1] = G
+    idx[7, 0] = -5
+    ws = q.alloc_workspace(q.binding.grouped_matmul_workspace_size(M, K, G, N, S, torch.float32))
+    out = torch.full((M, S, N), float("nan"), dtype=torch.float32, device=dev)
+    n0 = _launches()
+    q.grouped_matmul(x, w, idx, output=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert _launches() - n0 > 2
+    assert q.get_device_error(ws) == q.DEVERR_INDEX
+    o = out.cpu().numpy()
+    assert np.all(o[3, 1] == 0.0) and np.all(o[7, 0] == 0.0)
+    mask = np.ones((M, S), dtype=bool)
+    mask[3, 1] = mask[7, 0] = False
+    assert np.all(o[mask] == 1.0)
+
+
 def test_tensor_core_path_invalid_index(dev):
     import quantized_mixture_experts_gb300 as q
     M, K, G, N, S = 40, 64, 3, 64, 2
@@ -174,17 +238,18 @@ def test_tensor_core_path_invalid_index(dev):
     assert np.all(o[mask] == 1.0)
 
 
-@pytest.mark.parametrize("name", ["gmm_prefill", "gmm_prefill_bf16"])
+@pytest.mark.parametrize("name", ["gmm_prefill", "gmm_prefill_bf16", "gmm_prefill_f32",
+                                  "gmm_prefill_f64"])
 def test_bench_workload_sampled_vs_oracle(dev, name):
     """The benchmark's GroupedMatMul workloads (the prefill layer's FC1 shape as a dense
-    f16/bf16 grouped product: M 4096, K 4096, G 8, N 28672, S 2) at full size through
+    grouped product in f16, bf16, f32 and f64: M 4096, K 4096, G 8, N 28672, S 2) at full size through
     the call the benchmark times.  Sampled rows and columns (the last of each
     included) are compared with the oracle on the sampled problem: input[rows] and
     weights[:, :, cols] give exactly those outputs under the Summary definition."""
     import quantized_mixture_experts_gb300 as q
     from quantized_mixture_experts_gb300.workloads import GMM_WORKLOADS, make_gmm_inputs
     wl = GMM_WORKLOADS[name]
-    dt = "f16" if wl.dtype == "float16" else "bf16"
+    dt = {"float16": "f16", "bfloat16": "bf16", "float32": "f32", "float64": "f64"}[wl.dtype]
     tdt = getattr(torch, DTYPES[dt])
     inp = make_gmm_inputs(wl)
     x = torch.from_numpy(inp["input"]).to(dev).to(tdt)
@@ -196,7 +261,8 @@ def test_bench_workload_sampled_vs_oracle(dev, name):
     n0 = _launches()
     out = q.grouped_matmul(x, w, idx, workspace=ws)
     torch.cuda.synchronize()
-    assert _launches() - n0 == 6   # error-word clear, grouping (3), gather, tensor-core GEMM
+    # error-word clear, grouping (3), gather, tensor-core GEMM; f64: clear, general kernel
+    assert _launches() - n0 == (2 if dt == "f64" else 6)
     assert q.get_device_error(ws) == q.DEVERR_NONE
     rng = np.random.default_rng(11)
     r = np.unique(np.append(rng.choice(wl.M, 48, replace=False), wl.M - 1))
@@ -209,7 +275,8 @@ def test_bench_workload_sampled_vs_oracle(dev, name):
     ref, st = oracle.grouped_matmul(xr, wr, ix)
     assert st == oracle.OK
     mag = np.stack([np.stack([np.abs(xr[m]) @ np.abs(wr[g]) for g in ix[m]]) for m in range(len(r))])
-    eps_out = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}[dt]
-    bound = 2 * (wl.K + 2) * 2.0 ** -24 * mag + eps_out * np.abs(ref) + 1e-300
+    eps_out = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8, "f32": 2.0 ** -24, "f64": 2.0 ** -53}[dt]
+    eps_acc = 2.0 ** -53 if dt == "f64" else 2.0 ** -24
+    bound = 2 * (wl.K + 2) * eps_acc * mag + eps_out * np.abs(ref) + 1e-300
     err = np.abs(got - ref)
     assert np.all(err <= bound), float(np.max(err / bound))
