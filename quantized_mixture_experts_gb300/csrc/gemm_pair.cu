@@ -19,6 +19,18 @@
 // a thread of the epilogue owns one token row: its outputs leave as whole
 // 16-byte pieces of that row without a transpose.
 //
+// A token tile with at most tmax rows (an expert with few routed tokens, or
+// the last tile of one) runs the other way round, so that the tensor cores do
+// work in proportion to its tokens instead of a full 256 rows:
+//   D[256 weight rows, n] = deq(W)[256, K] * X[n, K]^T,  n = rows rounded up to 32
+// The dequantised weights are then the A operand (M = 256, each CTA's own 128
+// rows), the tokens the B operand (N = n: rows [rank * n/2, rank * n/2 + n/2)
+// of the tile in each CTA), and each CTA's tensor memory receives its 128
+// weight rows x n token columns.  Both operands keep their shared-memory
+// layout (K-major, 128-byte swizzle); only the descriptors, the instruction's
+// N and the token rows each CTA copies change.  The epilogue transposes its
+// 32 x 32 blocks through a per-warp shared tile.
+//
 // Per CTA (persistent, one per SM), warp-specialised, a ring of stages each
 // holding the K = 64 slice of the CTA's 128 token rows, its 128 packed weight
 // rows with their block scales, and the dequantised fp16 weight rows:
@@ -70,6 +82,9 @@ constexpr uint32_t kBBytes = kRowsCta * 128;   // dequantised weight rows of one
 constexpr uint32_t kSBytes = kRowsCta * 16;    // four staged scale blocks per row
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint64_t kDrainWaitNs = 200000000ull;
+// Token tiles of at most this many rows run with the tokens as the MMA's N.
+constexpr int kTokensAsNMaxRows = 192;
+static_assert(kTokensAsNMaxRows <= kTileRows, "tokens-as-N columns fit one accumulator");
 
 struct PairArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
@@ -95,7 +110,8 @@ struct PairArgs {
     int scale_vec;              // column-wise scales 16-byte aligned (read four at a time)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t stage_bytes, off_b, off_raw, off_s, raw_bytes, nstages;
-    uint32_t off_epi;           // FC2 epilogue staging: 2 KB per epilogue warp, after the ring
+    uint32_t off_epi;           // epilogue staging: 2 KB per epilogue warp, after the ring
+    int tmax;                   // token tiles of at most this many rows run tokens-as-N
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -235,6 +251,130 @@ struct Item {
     int e, row0, rows, m;       // expert, first sorted row of the tile, its rows, weight tile
 };
 
+// Token columns of a tokens-as-N item (a multiple of 32: N / 2 rows per CTA, a
+// multiple of the 16 rows the instruction takes with M = 256 on a pair), or 0
+// for an item that runs with the tokens as M.
+__device__ __forceinline__ int item_ncols(const PairArgs& a, const Item& w) {
+    return w.rows <= a.tmax ? (w.rows + 31) & ~31 : 0;
+}
+
+// Byte offset of output column c (of a warp's 32) of token row t in the
+// epilogue's 2 KB staging tile: 64 bytes per token row, 16-byte piece g of
+// row t at piece g ^ ((t >> 1) & 3) (conflict-free for a warp writing one row
+// and for a warp reading 16-byte pieces of eight rows).  PERM4 places the
+// eight values of a piece in the 4-bit operand order 0,4,1,5,2,6,3,7.
+template <bool PERM4>
+__device__ __forceinline__ uint32_t stage_off(int t, int c) {
+    const int q = c & 7;
+    const int pos = PERM4 ? (q < 4 ? 2 * q : 2 * (q - 4) + 1) : q;
+    return uint32_t(t) * 64u + ((uint32_t(c >> 3) ^ ((uint32_t(t) >> 1) & 3u)) << 4) +
+           uint32_t(pos) * 2u;
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, float v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(__half_as_ushort(__float2half_rn(v)))
+                 : "memory");
+}
+
+// Epilogue of a tokens-as-N item.  The warp's tensor-memory lane quadrant
+// holds 32 weight rows (lane = weight row) x nc token columns; the two warps
+// of a quadrant take alternate blocks of 32 tokens (at most four each).  A
+// block is scaled (column-wise scales: one per lane), activated (FC1) or
+// multiplied by each slot's routing weight (FC2), written transposed into the
+// warp's staging tile, and stored from there as whole 16-byte pieces of each
+// token's output row, in the layouts the tokens-as-M epilogue writes.  The
+// lanes of a pair (weight rows 2i, 2i + 1) trade values so that every lane
+// works: for SwiGLU a lane computes activation i for every other token, for
+// FC2 it stores columns (2i, 2i + 1) of every other token as one 32-bit word.
+// slot[m], p[m]: FC2 routing slot and weight of token chalf*32 + 64m + lane,
+// loaded by the caller before the accumulator is ready.
+template <int BITS, bool FC1, bool SCOL>
+__device__ __forceinline__ void epilogue_tokens_as_n(const PairArgs& a, const Item& w, int nc,
+                                                     uint32_t tq, uint32_t stg, int rank,
+                                                     int quad, int chalf, int lane,
+                                                     const int* slot, const float* p, float& omax,
+                                                     float& osum) {
+    const int64_t wcol = int64_t(w.m) * kTileRows + rank * kRowsCta + quad * 32;   // lane 0's row
+    const int64_t wrow = wcol + lane;
+    const bool glu = FC1 && a.act == QMOE_ACT_SWIGLU;
+    const int odd = lane & 1;
+    // the warp's run of output columns: 16 activations (SwiGLU: weight rows 2j, 2j + 1 are
+    // gate and linear of activation j) or 32 columns; n_out is a multiple of 64, so the
+    // run is wholly valid or wholly past the end
+    const int64_t c_first = glu ? (wcol >> 1) : wcol;
+    const bool cols_ok = c_first < a.n_out;
+    float cs = 1.f;
+    if (SCOL) cs = wrow < a.N ? __ldg(a.scales + int64_t(w.e) * a.N + wrow) : 0.f;
+#pragma unroll
+    for (int m = 0; m < kTileRows / 64; ++m) {
+        const int tb = chalf * 32 + 64 * m;
+        if (tb >= nc) break;
+        float v[32];
+        tmem_ld32(tq + uint32_t(tb), v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            float x0 = v[j], x1 = v[j + 1];
+            if (SCOL) {
+                x0 *= cs;
+                x1 *= cs;
+            }
+            // even lane: token j; odd lane: token j + 1
+            const int t = j + odd;
+            const bool tv = tb + t < w.rows;
+            const float recv = __shfl_xor_sync(kFull, odd ? x0 : x1, 1);
+            if (glu) {
+                // even: gate x0 with the odd lane's linear of token j; odd: the even
+                // lane's gate of token j + 1 with linear x1
+                const float o = tv ? swiglu(odd ? recv : x0, odd ? x1 : recv, a.alpha, a.beta,
+                                            a.has_limit, a.limit)
+                                   : 0.f;
+                if (cols_ok) {
+                    omax = fmaxf(omax, fabsf(o));
+                    osum += o;
+                }
+                st_shared_u16(stg + stage_off<BITS == 4>(t, lane >> 1), o);
+            } else if (FC1) {
+                // values of columns (lane & ~1, lane | 1) for token t
+                const float o0 = tv ? fmaxf(odd ? recv : x0, 0.f) : 0.f;
+                const float o1 = tv ? fmaxf(odd ? x1 : recv, 0.f) : 0.f;
+                if (cols_ok) omax = fmaxf(omax, fmaxf(o0, o1));
+                st_shared_u16(stg + stage_off<BITS == 4>(t, lane & ~1), o0);
+                st_shared_u16(stg + stage_off<BITS == 4>(t, lane | 1), o1);
+            } else {
+                const float pt = __shfl_sync(kFull, p[m], t);
+                const float o0 = tv ? (odd ? recv : x0) * pt : 0.f;
+                const float o1 = tv ? (odd ? x1 : recv) * pt : 0.f;
+                if (cols_ok) {
+                    omax = fmaxf(omax, fmaxf(fabsf(o0), fabsf(o1)));
+                    osum += o0 + o1;
+                }
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(stg + stage_off<false>(t, lane & ~1)),
+                             "r"(pack_h2(o0, o1))
+                             : "memory");
+            }
+        }
+        __syncwarp();
+        const int tok = tb + lane;                 // the token row this lane stores
+        if (tok < w.rows && cols_ok) {
+            const int npc = glu ? 2 : 4;
+            for (int g = 0; g < npc; ++g) {
+                const uint4 val = ptx::lds128(
+                    stg + uint32_t(lane) * 64u + ((uint32_t(g) ^ ((uint32_t(lane) >> 1) & 3u)) << 4));
+                if (FC1) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        a.act_out + ((c_first / kK) * a.srows + w.row0 + tok) * kK);
+                    const int ch = int(c_first % kK) / 8 + g;
+                    dst[ch ^ (tok & 7)] = val;
+                } else {
+                    reinterpret_cast<uint4*>(a.slot16 + int64_t(slot[m]) * a.n_out + c_first)[g] =
+                        val;
+                }
+            }
+        }
+        __syncwarp();   // the tile is read before the next block overwrites it
+    }
+}
+
 // Position in a ring of n stages: slot and the parity of its current phase,
 // advanced without divisions (the issuing thread's per-stage work is on the
 // tensor pipe's critical path).
@@ -284,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_flag;
+    __shared__ int stage_nc[kMaxStages];                     // token columns of the stage's item
     constexpr int PACK = BITS == 4 ? 2 : 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,15 +469,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::prefetch_tmap(&a.tm_w);
             if (a.scale_tma) ptx::prefetch_tmap(&a.tm_s);
         }
+        // Item descriptions for 32 items at a time, one per lane (their table lookups
+        // run in parallel); the current one is read by shuffle.
+        Item lw = Item{0, 0, 0, 0};
+        auto shfl_item = [&](int src) {
+            Item w;
+            w.e = __shfl_sync(kFull, lw.e, src);
+            w.row0 = __shfl_sync(kFull, lw.row0, src);
+            w.rows = __shfl_sync(kFull, lw.rows, src);
+            w.m = __shfl_sync(kFull, lw.m, src);
+            return w;
+        };
+        // where item w's packed rows, scales and this CTA's token rows are
+        auto wrow_of = [&](const Item& w) {
+            return int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTileRows + int(rank) * kRowsCta);
+        };
+        auto half_of = [&](const Item& w) {
+            const int nc = item_ncols(a, w);
+            return nc > 0 ? nc >> 1 : kRowsCta;
+        };
         uint32_t it = 0;
         Ring r;
         bool ok = true;
-        for (int64_t i = first; i < items && ok; i += step) {
-            const Item w = pair_item(a, i);
-            const int n_a = min(max(w.rows - int(rank) * kRowsCta, 0), kRowsCta);
-            const int32_t wrow = int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTileRows +
-                                         int(rank) * kRowsCta);
-            const __half* asrc = a.bsrc + (int64_t(w.row0) + int(rank) * kRowsCta) * kK;
+        int64_t j = 0;   // this CTA's items so far
+        for (int64_t i = first; i < items && ok; i += step, ++j) {
+            const int lj = int(j & 31);
+            if (lj == 0) {
+                const int64_t ii = i + int64_t(lane) * step;
+                if (ii < items) lw = pair_item(a, ii);
+            }
+            const Item w = shfl_item(lj);
+            // token rows of this CTA: its 128 of the 256 (tokens as M) or its n/2 of the
+            // n token columns (tokens as N)
+            const int nc = item_ncols(a, w);
+            const int half = half_of(w);
+            const int n_a = min(max(w.rows - int(rank) * half, 0), half);
+            const int32_t wrow = wrow_of(w);
+            const __half* asrc = a.bsrc + (int64_t(w.row0) + int(rank) * half) * kK;
             for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
                 const uint32_t sl = r.sl;
                 if (!ptx::mbar_wait(&st_free[sl], r.ph ^ 1u, a.wait_ns, &abort_flag)) {
@@ -347,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     uint8_t* sp = smem + size_t(sl) * a.stage_bytes;
                     const bool scales = a.scale_tma != 0;   // the group of four blocks of this stage
+                    // the item's form for the MMA issuer, released with the stage's
+                    // barrier (and, through the dequantisers' arrival, its operand barrier)
+                    stage_nc[sl] = nc;
                     ptx::mbar_arrive_expect_tx(&ld_full[sl], a.raw_bytes + (scales ? kSBytes : 0u) +
                                                                  uint32_t(n_a) * 128u);
                     ptx::tma_load_2d(sp + a.off_raw, &a.tm_w, kb * (kK / PACK), wrow, &ld_full[sl]);
@@ -374,12 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t item_it = 0;
             Ring r;
             bool ok = true, issued = false;
-            const uint32_t idesc = f16_idesc(2 * kRowsCta, kTileRows);
             for (int64_t i = first; i < items && ok; i += step, ++item_it) {
                 const uint32_t b = item_it & 1u;
+                // tokens as M: A = token rows (stage offset 0), B = weight rows; tokens as
+                // N: A = weight rows, B = the nc token rows (nc from the item's first stage)
+                uint32_t idesc = 0, a_off = 0, b_off = 0;
                 // both CTAs' epilogues released this accumulator: acquire at cluster scope
-                if (!ptx::mbar_wait_cluster(&acc_empty[b], ((item_it >> 1) & 1u) ^ 1u, a.wait_ns,
-                                            &abort_flag)) {
+                if (!ptx::mbar_wait_cluster(&acc_empty[b], ((item_it >> 1) & 1u) ^ 1u,
+                                                              a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -392,9 +566,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (kb == 0) {
+                        const int nc = *reinterpret_cast<volatile int*>(&stage_nc[sl]);
+                        idesc = f16_idesc(2 * kRowsCta, nc > 0 ? nc : kTileRows);
+                        a_off = nc > 0 ? a.off_b : 0u;
+                        b_off = nc > 0 ? 0u : a.off_b;
+                    }
                     if (lane == 0) {
-                        const uint32_t sa = sbase + sl * a.stage_bytes;
-                        const uint32_t sb = sa + a.off_b;
+                        const uint32_t sp = sbase + sl * a.stage_bytes;
+                        const uint32_t sa = sp + a_off;
+                        const uint32_t sb = sp + b_off;
 #pragma unroll
                         for (int kk = 0; kk < kK / 16; ++kk)
                             mma_pair(d, sw128_desc(sa + 32u * kk), sw128_desc(sb + 32u * kk), idesc,
@@ -544,14 +725,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t i = first; i < items; i += step, ++item_it) {
             const Item w = pair_item(a, i);
             const uint32_t b = item_it & 1u;
+            const int nc = item_ncols(a, w);
             const bool valid_row = grow < w.rows;
             const int64_t c_base = int64_t(w.m) * kTileRows + chalf * 128;   // first column
             int slot = 0;
             float p = 0.f;
-            if (!FC1 && valid_row) {
+            if (!FC1 && valid_row && nc == 0) {
                 slot = __ldg(a.perm + w.row0 + grow);
                 p = __ldg(a.pw + slot);
             }
+            // tokens as N: the slots and routing weights of this lane's tokens in the
+            // warp's blocks
+            int tslot[kTileRows / 64];
+            float tp[kTileRows / 64];
+#pragma unroll
+            for (int m = 0; m < kTileRows / 64; ++m) {
+                const int tok = chalf * 32 + 64 * m + lane;
+                tslot[m] = 0;
+                tp[m] = 0.f;
+                if (!FC1 && nc > 0 && tok < w.rows) tslot[m] = __ldg(a.perm + w.row0 + tok);
+            }
+#pragma unroll
+            for (int m = 0; m < kTileRows / 64; ++m)
+                if (!FC1 && nc > 0 && chalf * 32 + 64 * m + lane < w.rows) tp[m] = __ldg(a.pw + tslot[m]);
             if (!ptx::mbar_wait(&acc_full[b], (item_it >> 1) & 1u, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -563,8 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols +
                                    uint32_t(chalf * 128);
             const float* csc = a.scales + int64_t(w.e) * a.N;   // column-wise scales
+            if (nc > 0)
+                epilogue_tokens_as_n<BITS, FC1, SCOL>(
+                    a, w, nc, tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols,
+                    sbase + a.off_epi + uint32_t(ew) * 2048u, int(rank), quad, chalf, lane, tslot,
+                    tp, omax, osum);
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 0; c0 < (nc > 0 ? 0 : 128); c0 += 32) {
                 const int64_t col0 = c_base + c0;                // weight row of column c0
                 float v[32];
                 tmem_ld32(tbase + uint32_t(c0), v);
@@ -813,14 +1014,15 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.wait_ns = wait_limit_ns();
     a.drop_it = drop_stage();
     // stage: token rows | dequantised weight rows | packed rows | staged scales (block-wise
-    // only); after the ring, the FC2 epilogue's staging tiles
+    // only); after the ring, the epilogue's staging tiles
     a.raw_bytes = uint32_t(kRowsCta * (kK / pack));
     a.off_b = kABytes;
     a.off_raw = kABytes + kBBytes;
     a.off_s = a.off_raw + a.raw_bytes;
     a.stage_bytes = (a.off_s + (p.bs != 0 ? kSBytes : 0u) + 1023u) & ~1023u;
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
-    const size_t epi = fc1 ? 0 : size_t(kEpiWarps) * 2048;
+    const size_t epi = size_t(kEpiWarps) * 2048;
+    a.tmax = kTokensAsNMaxRows;
     a.nstages = uint32_t(std::min<size_t>(kMaxStages, (smem_cap - 1024 - epi) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;
     a.off_epi = a.nstages * a.stage_bytes;
