@@ -52,6 +52,9 @@
 //               a token's k rows in fixed order).
 // Every wait is bounded; on expiry the CTA records QMOE_DEVERR_TIMEOUT, stops,
 // and both CTAs meet at the final cluster barrier before freeing tensor memory.
+// The producer, the dequantisers and the epilogue wait inside mbarrier.try_wait
+// with a suspend-time hint (they are woken when the phase completes), so that
+// waiting warps leave their schedulers' issue slots to the working ones.
 #include <algorithm>
 #include <cstring>
 
@@ -456,7 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = tmem_base_s;
 
-    // the combine after FC2 may start its prologue on SMs this grid leaves
+    // launched as a programmatic dependent of the kernel that writes its operands and
+    // tile table: the prologue above overlaps that kernel's end
+    ptx::griddep_wait();
+    // the kernel after this one may start its prologue on SMs this grid leaves
     ptx::griddep_launch_dependents();
     const int64_t items = int64_t(__ldg(a.tiles)) * a.n_mt;
     const int nkb = int(a.K / kK);
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __half* asrc = a.bsrc + (int64_t(w.row0) + int(rank) * half) * kK;
             for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
                 const uint32_t sl = r.sl;
-                if (!ptx::mbar_wait(&st_free[sl], r.ph ^ 1u, a.wait_ns, &abort_flag)) {
+                if (!ptx::mbar_wait_sleep(&st_free[sl], r.ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
                 if (int(it & 1u) != grp) continue;
                 const uint32_t sl = r.sl;
-                if (!ptx::mbar_wait(&ld_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                if (!ptx::mbar_wait_sleep(&ld_full[sl], r.ph, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -748,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int m = 0; m < kTileRows / 64; ++m)
                 if (!FC1 && nc > 0 && chalf * 32 + 64 * m + lane < w.rows) tp[m] = __ldg(a.pw + tslot[m]);
-            if (!ptx::mbar_wait(&acc_full[b], (item_it >> 1) & 1u, a.wait_ns, &abort_flag)) {
+            if (!ptx::mbar_wait_sleep(&acc_full[b], (item_it >> 1) & 1u, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
                     abort_flag = 1;
@@ -913,13 +919,15 @@ cudaError_t launch_pair(const PairArgs& args, int pairs, size_t smem, cudaStream
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, args);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -287,6 +287,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(
     float* __restrict__ pw, int32_t* __restrict__ hist, int32_t* __restrict__ rank,
     const float* __restrict__ x, int64_t H, __half* __restrict__ x16, int64_t Hp,
     int x16_mode, int full, int32_t* __restrict__ ctrl, int chunks) {
+    // the grouping kernels launched after this one may be scheduled now (they wait
+    // for its completion before reading anything)
+    ptx::griddep_launch_dependents();
     if (int(blockIdx.x) >= chunks) {
         convert_all(x, T, H, x16, Hp, x16_mode, int(blockIdx.x) - chunks, int(gridDim.x) - chunks);
         return;
@@ -469,6 +472,9 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(
     int32_t* __restrict__ hist, int64_t chunks, int E, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tiles, int32_t* __restrict__ active,
     int tile_tokens) {
+    // launched as a programmatic dependent of the routing kernel
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     extern __shared__ int32_t sh[];
     const int tid = threadIdx.x, nthr = blockDim.x;
     // Phase 1: parts x experts partial sums.  P parts split the chunk range.
@@ -593,6 +599,9 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ sel,
                                      const int32_t* __restrict__ offsets, int64_t slots, int k,
                                      int E, int32_t* __restrict__ perm,
                                      int32_t* __restrict__ inv) {
+    // launched as a programmatic dependent of the scan
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     const int64_t s = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (s >= slots) return;
     const int e = sel[s];
@@ -620,6 +629,10 @@ __global__ void sort_convert_kernel(const float* __restrict__ x, int64_t T, int6
                                     const int32_t* __restrict__ sel,
                                     const int32_t* __restrict__ offsets, int k, int64_t srows,
                                     uint4* __restrict__ xs16) {
+    // launched as a programmatic dependent of the grouping kernels; the grouped GEMM
+    // after it may start its prologue on SMs this grid leaves
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     constexpr int U = 4;
     const int lane = threadIdx.x & 31;
     const int64_t wpb = blockDim.x >> 5;
@@ -763,13 +776,18 @@ cudaError_t launch_group(const Problem& p, const Plan& pl, const Work& w, cudaSt
         if (e != cudaSuccess) return e;
     }
     note_launch(QMOE_KERNEL_GROUP, s, true);
-    group_scan_kernel<<<1, nthr, smem, s>>>(w.hist, pl.route_chunks, E, w.counts, w.offsets,
-                                            w.tiles, w.active, pl.tile_tokens);
+    // each a programmatic dependent of the kernel before it
+    cudaError_t e = launch_dependent(group_scan_kernel, dim3(1), dim3(nthr), smem, s, w.hist,
+                                     int64_t(pl.route_chunks), E, w.counts, w.offsets, w.tiles,
+                                     w.active, int(pl.tile_tokens));
     const int64_t slots = pl.slots;
-    group_scatter_kernel<<<unsigned((slots + 255) / 256), 256, 0, s>>>(
-        w.sel, w.rank, w.hist, w.offsets, slots, int(p.k), E, w.perm, w.inv);
+    if (e == cudaSuccess)
+        e = launch_dependent(group_scatter_kernel, dim3(unsigned((slots + 255) / 256)), dim3(256),
+                             0, s, (const int32_t*)w.sel, (const int32_t*)w.rank,
+                             (const int32_t*)w.hist, (const int32_t*)w.offsets, slots, int(p.k),
+                             E, w.perm, w.inv);
     note_launch(QMOE_KERNEL_GROUP, s, false, 2);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_sort_convert(const Problem& p, const Plan& pl, const Work& w, cudaStream_t s) {
@@ -781,11 +799,13 @@ cudaError_t launch_sort_convert(const Problem& p, const Plan& pl, const Work& w,
     const int blocks = int(std::min<int64_t>((warps + 7) / 8, int64_t(device_sm_count()) * 8));
     const int vec = (p.H % 8 == 0 && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0) ? 1 : 0;
     note_launch(QMOE_KERNEL_GROUP, s, true);
-    sort_convert_kernel<<<std::max(blocks, 1), 256, 0, s>>>(
-        p.x, p.T, p.H, pl.Hp, vec, p.bits == 4 ? 1 : 0, parts, w.inv, w.sel, w.offsets, int(p.k),
-        pl.srows, reinterpret_cast<uint4*>(w.xs16));
+    const cudaError_t e = launch_dependent(
+        sort_convert_kernel, dim3(unsigned(std::max(blocks, 1))), dim3(256), 0, s, p.x,
+        int64_t(p.T), int64_t(p.H), int64_t(pl.Hp), vec, p.bits == 4 ? 1 : 0, parts,
+        (const int32_t*)w.inv, (const int32_t*)w.sel, (const int32_t*)w.offsets, int(p.k),
+        int64_t(pl.srows), reinterpret_cast<uint4*>(w.xs16));
     note_launch(QMOE_KERNEL_GROUP, s, false);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace qmoe
