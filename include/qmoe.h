@@ -162,8 +162,16 @@ qmoe_status qmoe_forward(const float *input, const int64_t *input_shape, int32_t
  * pointers as in qmoe_forward.  The call enqueues the host-to-device copies
  * into the workspace, the layer, and the device-to-host copy of the output on
  * `cuda_stream`; host_output is valid after the stream synchronizes.
+ * When all three buffers are page-locked memory mapped into the device's
+ * address space (cudaHostAlloc / cudaHostRegister, or any pinned allocation
+ * under unified addressing) and the activations are at most
+ * QMOE_HOSTIO_DIRECT_BYTES, no copy is enqueued: the routing and conversion
+ * kernels read the inputs and the combine writes the output in place over the
+ * host link (decode-sized calls, where each copy's fixed cost exceeds its
+ * transfer time).  The results are the same.
  * The workspace must hold qmoe_hostio_workspace_size bytes.
  */
+#define QMOE_HOSTIO_DIRECT_BYTES (1u << 20)
 qmoe_status qmoe_hostio_workspace_size(const int64_t *input_shape, int32_t input_rank,
                                        const int64_t *fc1_w_shape, const qmoe_attrs *attrs,
                                        size_t *bytes);

@@ -222,6 +222,9 @@ def _stream(stream) -> Optional[int]:
 
 
 ACTIVATIONS = {"relu": 0, "swiglu": 1}
+# include/qmoe.h QMOE_HOSTIO_DIRECT_BYTES: host-IO activations up to this size in mapped
+# page-locked memory are read and written in place by the kernels
+HOSTIO_DIRECT_BYTES = 1 << 20
 
 
 def make_attrs(k: int = 1, expert_weight_bits: int = 4, block_size: int = 0,

@@ -314,6 +314,22 @@ qmoe_status run_forward(Problem& p, const Plan& pl, void* workspace, int32_t* to
 }  // namespace
 }  // namespace qmoe
 
+namespace qmoe {
+namespace {
+// Device address of page-locked host memory mapped into the current device's
+// address space, or null (pageable memory, or memory the device cannot map).
+void* mapped_host(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // clear the (non-sticky) error of an unknown pointer
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return at.devicePointer;
+}
+}  // namespace
+}  // namespace qmoe
+
 using namespace qmoe;
 
 extern "C" {
@@ -452,16 +468,29 @@ qmoe_status qmoe_forward_hostio(const float* host_input, const int64_t* input_sh
     float* d_l = reinterpret_cast<float*>(base + pl.bytes + xb);
     float* d_y = reinterpret_cast<float*>(base + pl.bytes + xb + lb);
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    p.w1 = fc1_w;
+    p.s1 = fc1_scales;
+    p.w2 = fc2_w;
+    p.s2 = fc2_scales;
+    // small activations in mapped page-locked memory: the kernels read and write them in
+    // place over the host link, without the copies' fixed costs
+    if (xbytes <= QMOE_HOSTIO_DIRECT_BYTES) {
+        void* mx = mapped_host(host_input);
+        void* ml = mapped_host(host_router_probs);
+        void* my = mapped_host(host_output);
+        if (mx && ml && my) {
+            p.x = static_cast<const float*>(mx);
+            p.logits = static_cast<const float*>(ml);
+            p.y = static_cast<float*>(my);
+            return run_forward(p, pl, workspace, nullptr, nullptr, s);
+        }
+    }
     if (cudaMemcpyAsync(d_x, host_input, xbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return QMOE_ERR_CUDA;
     if (cudaMemcpyAsync(d_l, host_router_probs, lbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return QMOE_ERR_CUDA;
     p.x = d_x;
     p.logits = d_l;
-    p.w1 = fc1_w;
-    p.s1 = fc1_scales;
-    p.w2 = fc2_w;
-    p.s2 = fc2_scales;
     p.y = d_y;
     st = run_forward(p, pl, workspace, nullptr, nullptr, s);
     if (st != QMOE_OK) return st;

@@ -253,3 +253,13 @@ def test_attribute_struct_layouts_match_c(tmp_path, cname, pyname):
                                           text=True).stdout.split()]
     assert got[0] == ctypes.sizeof(st)
     assert got[1:] == [getattr(st, f).offset for f in fields]
+
+
+def test_hostio_direct_limit_matches_header():
+    """The binding's host-IO in-place limit is the header's QMOE_HOSTIO_DIRECT_BYTES."""
+    import re
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    text = open(os.path.join(inc, "qmoe.h")).read()
+    m = re.search(r"#define\s+QMOE_HOSTIO_DIRECT_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "QMOE_HOSTIO_DIRECT_BYTES not found"
+    assert int(m.group(1)) << int(m.group(2)) == q.binding.HOSTIO_DIRECT_BYTES

@@ -255,6 +255,38 @@ def test_hostio_matches_device_path(dev):
     assert np.array_equal(hy.numpy(), y_dev.cpu().numpy())
 
 
+@pytest.mark.parametrize("wl", [SMALL[6], SMALL[1],
+                                Workload("hostio_over_limit", 29, (600, 512), 512, 256, 8, 2, 4,
+                                         32, "swiglu")],
+                         ids=lambda w: w.name)
+def test_hostio_in_place_and_copied_agree(dev, wl):
+    """Host-IO with mapped page-locked buffers (read and written in place by the kernels
+    when the activations fit QMOE_HOSTIO_DIRECT_BYTES, copied otherwise) and with pageable
+    buffers (always copied) give the device path's output bit for bit."""
+    import quantized_mixture_experts_gb300 as q
+    inp = make_inputs(wl)
+    t = to_dev(inp, dev)
+    attrs = q.make_attrs(**wl.attrs())
+    y_dev = q.qmoe_forward(t["input"], t["router_probs"], t["fc1_experts_weights"],
+                           t["fc1_scales"], t["fc2_experts_weights"], t["fc2_scales"],
+                           attrs=attrs).cpu().numpy()
+    ws = q.alloc_workspace(q.workspace_size(wl.input_shape, t["fc1_experts_weights"].shape,
+                                            attrs, hostio=True))
+    for pinned in (True, False):
+        hx = torch.from_numpy(inp["input"].copy())
+        hl = torch.from_numpy(inp["router_probs"].copy())
+        hy = torch.full_like(hx, float("nan"))
+        if pinned:
+            hx, hl, hy = hx.pin_memory(), hl.pin_memory(), hy.pin_memory()
+        for _ in range(2):
+            q.qmoe_forward_hostio(hx, hl, t["fc1_experts_weights"], t["fc1_scales"],
+                                  t["fc2_experts_weights"], t["fc2_scales"], hy, attrs=attrs,
+                                  workspace=ws)
+            torch.cuda.synchronize()
+            assert np.array_equal(hy.numpy(), y_dev), (wl.name, pinned)
+    assert (wl.name == "hostio_over_limit") == (inp["input"].nbytes > q.binding.HOSTIO_DIRECT_BYTES)
+
+
 def test_device_error_clean_after_forward(dev):
     import quantized_mixture_experts_gb300 as q
     wl = SMALL[1]
