@@ -707,7 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                ptx::fence_proxy_async();
+                // the tensor cores of both CTAs read this CTA's rows (the pair exchanges
+                // operand halves): make the writes visible to the async proxy at cluster
+                // scope (with CTA scope about one call in a few hundred computed an item
+                // from stale operands)
+                asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) arrive_remote(op_addr + sl * 8u);
             }
