@@ -10,33 +10,33 @@
 //
 // One work item = (token tile: up to 256 expert-sorted rows of one expert,
 // 256-row weight tile of that expert), computed by a cluster of two CTAs:
-//   D[256 tokens, 256 weight rows] = X[256, K] * deq(W)[256, K]^T
-// The tokens are the MMA's A operand (M = 256: 128 rows in each CTA's shared
-// memory), the dequantised weights its B operand (N = 256: each CTA
-// dequantises 128 of the rows), and each CTA's tensor memory receives its 128
-// token rows x 256 columns.  Two 256-column accumulators alternate between
-// items, so the epilogue of one item runs while the next item's MMAs run, and
-// a thread of the epilogue owns one token row: its outputs leave as whole
-// 16-byte pieces of that row without a transpose.
-//
-// A token tile with at most tmax rows (an expert with few routed tokens, or
-// the last tile of one) runs the other way round, so that the tensor cores do
-// work in proportion to its tokens instead of a full 256 rows:
 //   D[256 weight rows, n] = deq(W)[256, K] * X[n, K]^T,  n = rows rounded up to 32
-// The dequantised weights are then the A operand (M = 256, each CTA's own 128
-// rows), the tokens the B operand (N = n: rows [rank * n/2, rank * n/2 + n/2)
-// of the tile in each CTA), and each CTA's tensor memory receives its 128
-// weight rows x n token columns.  Both operands keep their shared-memory
-// layout (K-major, 128-byte swizzle); only the descriptors, the instruction's
-// N and the token rows each CTA copies change.  The epilogue transposes its
-// 32 x 32 blocks through a per-warp shared tile.
+// The dequantised weights are the MMA's A operand (M = 256: each CTA converts
+// and holds its own 128 rows), the tokens its B operand (N = n: rows
+// [rank * n/2, rank * n/2 + n/2) of the tile in each CTA), and each CTA's
+// tensor memory receives its 128 weight rows x n token columns, so the tensor
+// cores work in proportion to the routed tokens.  Two 256-column accumulators
+// alternate between items: the epilogue of one item runs while the next
+// item's MMAs run, transposing its 32 x 32 blocks through a per-warp shared
+// tile into token rows.
+//
+// Operand exchange within the pair.  Each CTA's tensor core reads the other
+// CTA's token rows, and only its own dequantised rows.  The token rows are
+// therefore copied by the tensor-copy engine with completion counted on CTA 0's
+// barrier (.cta_group::2), which orders them for both tensor cores, while the
+// rows the dequantisers write in the generic proxy stay CTA-local (fenced to
+// the async proxy at CTA scope).  The earlier arrangement (tokens as A, the
+// dequantised weights as B, whose halves each tensor core reads from both
+// CTAs, with the token copies completing on each CTA's own barrier) let about
+// one call in a few hundred compute an item from stale operands.
 //
 // Per CTA (persistent, one per SM), warp-specialised, a ring of stages each
-// holding the K = 64 slice of the CTA's 128 token rows, its 128 packed weight
+// holding the K = 64 slice of the CTA's n/2 token rows, its 128 packed weight
 // rows with their block scales, and the dequantised fp16 weight rows:
 //   warp 0      TMA producer: packed weights and staged block scales (2-D
-//               tensor boxes), the token rows (one 1-D bulk copy: the rows are
-//               stored K-blocked with the 128-byte swizzle already applied);
+//               tensor boxes, on this CTA's barrier), the token rows (one 3-D
+//               box of 128 rows: the rows are stored K-blocked with the
+//               128-byte swizzle already applied; on CTA 0's barrier);
 //   warp 1      tensor-memory allocation; in CTA 0 of the pair, one lane
 //               issues the MMAs of both CTAs and commits their completion to
 //               both CTAs' barriers;
@@ -69,7 +69,6 @@ constexpr int kRowsCta = 128;         // token rows and weight rows per CTA of a
 constexpr int kTileRows = 2 * kRowsCta;
 constexpr int kK = 64;                // K per stage: one 128-byte row of fp16
 constexpr int kMaxStages = 6;        // ring depth upper bound (the launch picks what fits)
-constexpr int kDeqWarps = 8;          // two groups of four: one thread per weight row of the CTA
 constexpr int kDeqGroupWarps = 4;     // warps of a group (the group takes every other stage)
 constexpr int kEpiWarps = 8;          // two per TMEM lane quadrant (one per column half)
 // Warp roles.  A warp runs on scheduler (warp % 4); the MMA-issuing warp 1
@@ -86,11 +85,11 @@ constexpr uint32_t kSBytes = kRowsCta * 16;    // four staged scale blocks per r
 constexpr unsigned kFull = 0xffffffffu;
 constexpr uint64_t kDrainWaitNs = 200000000ull;
 // Token tiles of at most this many rows run with the tokens as the MMA's N.
-constexpr int kTokensAsNMaxRows = 192;
-static_assert(kTokensAsNMaxRows <= kTileRows, "tokens-as-N columns fit one accumulator");
+constexpr int kTokBox = kRowsCta;     // token rows per tensor-copy box (one box per CTA and stage)
 
 struct PairArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
+    CUtensorMap tm_b;           // token rows [K/64][srows][64] fp16 (pre-swizzled), box {64, 16, 1}
     CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 128}
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, expert's first tile)
@@ -110,11 +109,9 @@ struct PairArgs {
     int32_t* err;
     uint64_t wait_ns;
     int scale_tma;              // block scales staged by TMA (nb % 4 == 0)
-    int scale_vec;              // column-wise scales 16-byte aligned (read four at a time)
     int64_t drop_it;            // test hook: stage whose copies the producer skips
     uint32_t stage_bytes, off_b, off_raw, off_s, raw_bytes, nstages;
     uint32_t off_epi;           // epilogue staging: 2 KB per epilogue warp, after the ring
-    int tmax;                   // token tiles of at most this many rows run tokens-as-N
 };
 
 __device__ __forceinline__ void record_error(int32_t* err, int code) { atomicCAS(err, 0, code); }
@@ -174,6 +171,17 @@ __device__ __forceinline__ void commit_local(uint64_t* bar) {
 // arriving.
 __device__ __forceinline__ void arrive_remote(uint32_t addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Token rows box (64 fp16 x kTokBox rows of K block kb) into this CTA's shared
+// memory, completion counted on CTA 0's barrier at shared::cluster address `bar`.
+__device__ __forceinline__ void tma_tokens(void* dst, const CUtensorMap* map, int32_t row, int32_t kb,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(ptx::smem_u32(dst)), "l"(map), "r"(0), "r"(row), "r"(kb), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -257,8 +265,8 @@ struct Item {
 // Token columns of a tokens-as-N item (a multiple of 32: N / 2 rows per CTA, a
 // multiple of the 16 rows the instruction takes with M = 256 on a pair), or 0
 // for an item that runs with the tokens as M.
-__device__ __forceinline__ int item_ncols(const PairArgs& a, const Item& w) {
-    return w.rows <= a.tmax ? (w.rows + 31) & ~31 : 0;
+__device__ __forceinline__ int item_ncols(const Item& w) {
+    return (w.rows + 31) & ~31;
 }
 
 // Byte offset of output column c (of a warp's 32) of token row t in the
@@ -419,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t ld_full[kMaxStages];    // this CTA's copies landed
+    __shared__ __align__(8) uint64_t ld_full[kMaxStages];    // this CTA's packed rows and scales landed
+    __shared__ __align__(8) uint64_t tok_full[kMaxStages];   // CTA 0: both CTAs' token rows landed
     __shared__ __align__(8) uint64_t op_full[kMaxStages];    // CTA 0: both CTAs' operands ready
     __shared__ __align__(8) uint64_t st_free[kMaxStages];    // the stage's MMAs completed
     __shared__ __align__(8) uint64_t acc_full[2];            // an item's MMAs completed
@@ -437,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; ++s) {
             ptx::mbar_init(&ld_full[s], 1);
+            ptx::mbar_init(&tok_full[s], 1);
             ptx::mbar_init(&op_full[s], 2 * kDeqGroupWarps);
             ptx::mbar_init(&st_free[s], 1);
         }
@@ -473,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             ptx::prefetch_tmap(&a.tm_w);
+            ptx::prefetch_tmap(&a.tm_b);
             if (a.scale_tma) ptx::prefetch_tmap(&a.tm_s);
         }
         // Item descriptions for 32 items at a time, one per lane (their table lookups
@@ -490,14 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wrow_of = [&](const Item& w) {
             return int32_t(int64_t(w.e) * a.N + int64_t(w.m) * kTileRows + int(rank) * kRowsCta);
         };
-        auto half_of = [&](const Item& w) {
-            const int nc = item_ncols(a, w);
-            return nc > 0 ? nc >> 1 : kRowsCta;
-        };
         uint32_t it = 0;
         Ring r;
         bool ok = true;
         int64_t j = 0;   // this CTA's items so far
+        const uint32_t tok_addr = ptx::leader_addr(&tok_full[0]);
         for (int64_t i = first; i < items && ok; i += step, ++j) {
             const int lj = int(j & 31);
             if (lj == 0) {
@@ -505,13 +513,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ii < items) lw = pair_item(a, ii);
             }
             const Item w = shfl_item(lj);
-            // token rows of this CTA: its 128 of the 256 (tokens as M) or its n/2 of the
-            // n token columns (tokens as N)
-            const int nc = item_ncols(a, w);
-            const int half = half_of(w);
-            const int n_a = min(max(w.rows - int(rank) * half, 0), half);
+            // token rows of this CTA: its n/2 of the item's n token columns, copied in boxes
+            // of kTokBox rows that complete on CTA 0's token barrier (the other CTA's tensor
+            // core reads them: the copy engine's completion orders them for both)
+            const int nc = item_ncols(w);
+            const int half = nc >> 1;
+            auto rows_of = [&](int rk) { return min(max(w.rows - rk * half, 0), half); };
+            // one box of kTokBox rows per CTA that has rows (rows past the tile's are read
+            // too and never stored; past the buffer the copy fills zeros)
+            const int nbox = rows_of(int(rank)) > 0 ? 1 : 0;
+            const uint32_t tok_bytes =
+                uint32_t((rows_of(0) > 0 ? 1 : 0) + (rows_of(1) > 0 ? 1 : 0)) * kTokBox * 128u;
+            const int32_t ty0 = w.row0 + int(rank) * half;
             const int32_t wrow = wrow_of(w);
-            const __half* asrc = a.bsrc + (int64_t(w.row0) + int(rank) * half) * kK;
             for (int kb = 0; kb < nkb; ++kb, ++it, r.next(S)) {
                 const uint32_t sl = r.sl;
                 if (!ptx::mbar_wait_sleep(&st_free[sl], r.ph ^ 1u, a.wait_ns, &abort_flag)) {
@@ -525,15 +539,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the item's form for the MMA issuer, released with the stage's
                     // barrier (and, through the dequantisers' arrival, its operand barrier)
                     stage_nc[sl] = nc;
-                    ptx::mbar_arrive_expect_tx(&ld_full[sl], a.raw_bytes + (scales ? kSBytes : 0u) +
-                                                                 uint32_t(n_a) * 128u);
+                    ptx::mbar_arrive_expect_tx(&ld_full[sl], a.raw_bytes + (scales ? kSBytes : 0u));
                     ptx::tma_load_2d(sp + a.off_raw, &a.tm_w, kb * (kK / PACK), wrow, &ld_full[sl]);
                     if (scales)
                         ptx::tma_load_2d(sp + a.off_s, &a.tm_s, ((kb * kK) >> a.lbs) & ~3, wrow,
                                          &ld_full[sl]);
-                    if (n_a > 0)
-                        ptx::bulk_g2s(sp, asrc + int64_t(kb) * a.srows * kK, uint32_t(n_a) * 128u,
-                                      &ld_full[sl]);
+                    if (leader) ptx::mbar_arrive_expect_tx(&tok_full[sl], tok_bytes);
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_tokens(sp + bx * (kTokBox * 128), &a.tm_b, ty0 + bx * kTokBox, kb,
+                                   tok_addr + sl * 8u);
                 }
                 __syncwarp();
             }
@@ -544,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t j = it > S ? it - S : 0; j < it; ++j) {
                 volatile int never = 0;
                 ptx::mbar_wait(&ld_full[j % S], (j / S) & 1u, kDrainWaitNs, &never);
+                if (leader) ptx::mbar_wait(&tok_full[j % S], (j / S) & 1u, kDrainWaitNs, &never);
             }
         }
     } else if (warp == 1) {
@@ -567,16 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem_base + b * kAccCols;
                 for (int kb = 0; kb < nkb; ++kb, r.next(S)) {
                     const uint32_t sl = r.sl;
-                    if (!ptx::mbar_wait(&op_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                    if (!ptx::mbar_wait(&op_full[sl], r.ph, a.wait_ns, &abort_flag) ||
+                        !ptx::mbar_wait(&tok_full[sl], r.ph, a.wait_ns, &abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (kb == 0) {
                         const int nc = *reinterpret_cast<volatile int*>(&stage_nc[sl]);
-                        idesc = f16_idesc(2 * kRowsCta, nc > 0 ? nc : kTileRows);
-                        a_off = nc > 0 ? a.off_b : 0u;
-                        b_off = nc > 0 ? 0u : a.off_b;
+                        idesc = f16_idesc(2 * kRowsCta, nc);
+                        a_off = a.off_b;   // A: the dequantised weight rows
+                        b_off = 0u;        // B: the nc token columns
                     }
                     if (lane == 0) {
                         const uint32_t sp = sbase + sl * a.stage_bytes;
@@ -707,11 +723,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // the tensor cores of both CTAs read this CTA's rows (the pair exchanges
-                // operand halves): make the writes visible to the async proxy at cluster
-                // scope (with CTA scope about one call in a few hundred computed an item
-                // from stale operands)
-                asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+                // the dequantised weight rows are the A operand: only this CTA's tensor core
+                // reads them
+                ptx::fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) arrive_remote(op_addr + sl * 8u);
             }
@@ -725,8 +739,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - kEpiWarp0;           // 0..7
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int chalf = ew >> 2;                 // column half: weight rows 128 * chalf ..
-        const int tr = quad * 32 + lane;           // token row of this CTA's 128
-        const int grow = int(rank) * kRowsCta + tr;   // row within the token tile
         const uint32_t empty_addr = ptx::leader_addr(&acc_empty[0]);
         // outputs outside the fp16 range: the largest magnitude and a NaN-propagating
         // sum of every output this lane stores, checked once at the end
@@ -735,17 +747,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t i = first; i < items; i += step, ++item_it) {
             const Item w = pair_item(a, i);
             const uint32_t b = item_it & 1u;
-            const int nc = item_ncols(a, w);
-            const bool valid_row = grow < w.rows;
-            const int64_t c_base = int64_t(w.m) * kTileRows + chalf * 128;   // first column
-            int slot = 0;
-            float p = 0.f;
-            if (!FC1 && valid_row && nc == 0) {
-                slot = __ldg(a.perm + w.row0 + grow);
-                p = __ldg(a.pw + slot);
-            }
-            // tokens as N: the slots and routing weights of this lane's tokens in the
-            // warp's blocks
+            const int nc = item_ncols(w);
+            // the slots and routing weights of this lane's tokens in the warp's blocks (FC2)
             int tslot[kTileRows / 64];
             float tp[kTileRows / 64];
 #pragma unroll
@@ -753,11 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tok = chalf * 32 + 64 * m + lane;
                 tslot[m] = 0;
                 tp[m] = 0.f;
-                if (!FC1 && nc > 0 && tok < w.rows) tslot[m] = __ldg(a.perm + w.row0 + tok);
+                if (!FC1 && tok < w.rows) tslot[m] = __ldg(a.perm + w.row0 + tok);
             }
 #pragma unroll
             for (int m = 0; m < kTileRows / 64; ++m)
-                if (!FC1 && nc > 0 && chalf * 32 + 64 * m + lane < w.rows) tp[m] = __ldg(a.pw + tslot[m]);
+                if (!FC1 && chalf * 32 + 64 * m + lane < w.rows) tp[m] = __ldg(a.pw + tslot[m]);
             if (!ptx::mbar_wait_sleep(&acc_full[b], (item_it >> 1) & 1u, a.wait_ns, &abort_flag)) {
                 if (lane == 0) {
                     record_error(a.err, QMOE_DEVERR_TIMEOUT);
@@ -766,136 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols +
-                                   uint32_t(chalf * 128);
-            const float* csc = a.scales + int64_t(w.e) * a.N;   // column-wise scales
-            if (nc > 0)
-                epilogue_tokens_as_n<BITS, FC1, SCOL>(
-                    a, w, nc, tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols,
-                    sbase + a.off_epi + uint32_t(ew) * 2048u, int(rank), quad, chalf, lane, tslot,
-                    tp, omax, osum);
-#pragma unroll 1
-            for (int c0 = 0; c0 < (nc > 0 ? 0 : 128); c0 += 32) {
-                const int64_t col0 = c_base + c0;                // weight row of column c0
-                float v[32];
-                tmem_ld32(tbase + uint32_t(c0), v);
-                if (SCOL) {
-                    // one scale per weight row (column of D), the same for the whole warp
-                    if (a.scale_vec) {
-#pragma unroll
-                        for (int q = 0; q < 32; q += 4) {
-                            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (col0 + q < a.N)
-                                s4 = __ldg(reinterpret_cast<const float4*>(csc + col0 + q));
-                            v[q] *= s4.x;
-                            v[q + 1] *= s4.y;
-                            v[q + 2] *= s4.z;
-                            v[q + 3] *= s4.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) v[q] *= col0 + q < a.N ? __ldg(csc + col0 + q) : 0.f;
-                    }
-                }
-                // rows past the tile's tokens compute (their outputs are not stored); the
-                // loop stays uniform across the warp for the collective tensor-memory loads
-                if (FC1) {
-                    if (a.act == QMOE_ACT_SWIGLU) {
-                        // columns (2j, 2j + 1) = (gate, linear) -> 16 activations j0 .. j0 + 15
-                        const int64_t j0 = col0 >> 1;
-                        if (j0 >= a.n_out) continue;
-                        float o[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            o[q] = valid_row ? swiglu(v[2 * q], v[2 * q + 1], a.alpha, a.beta,
-                                                      a.has_limit, a.limit)
-                                             : 0.f;
-                            omax = fmaxf(omax, fabsf(o[q]));
-                            osum += o[q];
-                        }
-                        uint4 pc[2];
-#pragma unroll
-                        for (int g = 0; g < 2; ++g) {
-                            const float* og = o + 8 * g;
-                            if (BITS == 4)   // the 4-bit operand order 0,4,1,5,2,6,3,7
-                                pc[g] = make_uint4(pack_h2(og[0], og[4]), pack_h2(og[1], og[5]),
-                                                   pack_h2(og[2], og[6]), pack_h2(og[3], og[7]));
-                            else
-                                pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
-                                                   pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            a.act_out + ((j0 / kK) * a.srows + w.row0 + grow) * kK);
-                        const int ch = int(j0 % kK) / 8;
-                        if (valid_row) {
-                            dst[(ch) ^ (grow & 7)] = pc[0];
-                            dst[(ch + 1) ^ (grow & 7)] = pc[1];
-                        }
-                    } else {
-                        const int64_t j0 = col0;
-                        if (j0 >= a.n_out) continue;
-                        uint4 pc[4];
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            float og[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                og[q] = valid_row ? fmaxf(v[8 * g + q], 0.f) : 0.f;
-                                omax = fmaxf(omax, og[q]);
-                            }
-                            if (BITS == 4)
-                                pc[g] = make_uint4(pack_h2(og[0], og[4]), pack_h2(og[1], og[5]),
-                                                   pack_h2(og[2], og[6]), pack_h2(og[3], og[7]));
-                            else
-                                pc[g] = make_uint4(pack_h2(og[0], og[1]), pack_h2(og[2], og[3]),
-                                                   pack_h2(og[4], og[5]), pack_h2(og[6], og[7]));
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(
-                            a.act_out + ((j0 / kK) * a.srows + w.row0 + grow) * kK);
-                        const int ch = int(j0 % kK) / 8;
-                        if (valid_row) {
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) dst[(ch + g) ^ (grow & 7)] = pc[g];
-                        }
-                    }
-                } else {
-                    // FC2: 32 output columns (64 bytes) of the slot's row, times its routing
-                    // weight.  The warp's 32 rows go through its staging tile (16-byte piece
-                    // j of row r at piece j ^ ((r >> 1) & 3), conflict-free both ways) so
-                    // that each store instruction writes 8 rows x 64 contiguous bytes.
-                    if (col0 >= a.n_out) continue;
-                    const uint32_t stg = sbase + a.off_epi + uint32_t(ew) * 2048u;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float og[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            og[q] = valid_row ? v[8 * g + q] * p : 0.f;
-                            omax = fmaxf(omax, fabsf(og[q]));
-                            osum += og[q];
-                        }
-                        const uint32_t addr =
-                            stg + uint32_t(lane) * 64u + ((uint32_t(g) ^ ((uint32_t(lane) >> 1) & 3u)) << 4);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr),
-                                     "r"(pack_h2(og[0], og[1])), "r"(pack_h2(og[2], og[3])),
-                                     "r"(pack_h2(og[4], og[5])), "r"(pack_h2(og[6], og[7]))
-                                     : "memory");
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = 8 * i + (lane >> 2);          // row of the warp's 32
-                        const int j = lane & 3;                     // its 16-byte piece
-                        const uint4 val = ptx::lds128(
-                            stg + uint32_t(r) * 64u + ((uint32_t(j) ^ ((uint32_t(r) >> 1) & 3u)) << 4));
-                        const int rslot = __shfl_sync(kFull, slot, r);
-                        const bool rvalid = __shfl_sync(kFull, valid_row ? 1 : 0, r) != 0;
-                        if (rvalid)
-                            reinterpret_cast<uint4*>(a.slot16 + int64_t(rslot) * a.n_out + col0)[j] = val;
-                    }
-                    __syncwarp();
-                }
-            }
+            epilogue_tokens_as_n<BITS, FC1, SCOL>(
+                a, w, nc, tmem_base + (uint32_t(quad * 32) << 16) + b * kAccCols,
+                sbase + a.off_epi + uint32_t(ew) * 2048u, int(rank), quad, chalf, lane, tslot, tp,
+                omax, osum);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(empty_addr + b * 8u);
@@ -1002,8 +879,15 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
         return cudaErrorInvalidValue;
     a.bsrc = fc1 ? w.xs16 : static_cast<const __half*>(w.act);
     a.srows = pl.srows;
+    {
+        const uint64_t dims[3] = {uint64_t(kK), uint64_t(pl.srows), uint64_t(a.K / kK)};
+        const uint64_t strides[2] = {uint64_t(kK) * 2, uint64_t(pl.srows) * kK * 2};
+        const uint32_t box[3] = {uint32_t(kK), uint32_t(kTokBox), 1u};
+        if (!encode_tmap_3d(&a.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.bsrc, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     a.scale_tma = (p.bs != 0 && a.nb % 4 == 0) ? 1 : 0;
-    a.scale_vec = (reinterpret_cast<uintptr_t>(a.scales) & 15) == 0 ? 1 : 0;
     if (a.scale_tma &&
         !encode_tmap_2d(&a.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.scales, uint64_t(a.nb),
                         uint64_t(p.E * a.N), uint64_t(a.nb) * 4, 4, kRowsCta,
@@ -1034,7 +918,6 @@ cudaError_t launch_grouped_fc(const Problem& p, const Plan& pl, const Work& w, b
     a.stage_bytes = (a.off_s + (p.bs != 0 ? kSBytes : 0u) + 1023u) & ~1023u;
     const size_t smem_cap = 232448 - 1024;   // 227 KB per CTA, minus static shared memory
     const size_t epi = size_t(kEpiWarps) * 2048;
-    a.tmax = kTokensAsNMaxRows;
     a.nstages = uint32_t(std::min<size_t>(kMaxStages, (smem_cap - 1024 - epi) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;
     a.off_epi = a.nstages * a.stage_bytes;
