@@ -365,21 +365,31 @@ __device__ __forceinline__ void epilogue_tokens_as_n(const PairArgs& a, const It
             }
         }
         __syncwarp();
-        const int tok = tb + lane;                 // the token row this lane stores
-        if (tok < w.rows && cols_ok) {
-            const int npc = glu ? 2 : 4;
-            for (int g = 0; g < npc; ++g) {
-                const uint4 val = ptx::lds128(
-                    stg + uint32_t(lane) * 64u + ((uint32_t(g) ^ ((uint32_t(lane) >> 1) & 3u)) << 4));
-                if (FC1) {
+        if (FC1) {
+            const int tok = tb + lane;             // the token row this lane stores
+            if (tok < w.rows && cols_ok) {
+                const int npc = glu ? 2 : 4;
+                for (int g = 0; g < npc; ++g) {
+                    const uint4 val = ptx::lds128(
+                        stg + uint32_t(lane) * 64u + ((uint32_t(g) ^ ((uint32_t(lane) >> 1) & 3u)) << 4));
                     uint4* dst = reinterpret_cast<uint4*>(
                         a.act_out + ((c_first / kK) * a.srows + w.row0 + tok) * kK);
                     const int ch = int(c_first % kK) / 8 + g;
                     dst[ch ^ (tok & 7)] = val;
-                } else {
-                    reinterpret_cast<uint4*>(a.slot16 + int64_t(slot[m]) * a.n_out + c_first)[g] =
-                        val;
                 }
+            }
+        } else if (cols_ok) {
+            // each store instruction writes 8 token rows x 64 contiguous bytes: lane
+            // (r, j) stores 16-byte piece j of token row r of the block
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 8 * i + (lane >> 2);
+                const int j = lane & 3;
+                const int rslot = __shfl_sync(kFull, slot[m], r);
+                const uint4 val = ptx::lds128(
+                    stg + uint32_t(r) * 64u + ((uint32_t(j) ^ ((uint32_t(r) >> 1) & 3u)) << 4));
+                if (tb + r < w.rows)
+                    reinterpret_cast<uint4*>(a.slot16 + int64_t(rslot) * a.n_out + c_first)[j] = val;
             }
         }
         __syncwarp();   // the tile is read before the next block overwrites it
