@@ -592,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem_base + b * kAccCols;
                 for (int kb = 0; kb < nkb; ++kb, r.next(S)) {
                     const uint32_t sl = r.sl;
-                    if (!ptx::mbar_wait(&op_full[sl], r.ph, a.wait_ns, &abort_flag) ||
-                        !ptx::mbar_wait(&tok_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                    // both CTAs' weight rows converted and (through CTA 0's dequantisers,
+                    // which wait for them) both CTAs' token rows landed
+                    if (!ptx::mbar_wait(&op_full[sl], r.ph, a.wait_ns, &abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -737,6 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // reads them
                 ptx::fence_proxy_async();
                 __syncwarp();
+                // CTA 0's arrival also stands for the token rows of both CTAs, whose copies
+                // complete on CTA 0's token barrier
+                if (leader && !ptx::mbar_wait(&tok_full[sl], r.ph, a.wait_ns, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) arrive_remote(op_addr + sl * 8u);
             }
         }
