@@ -3,7 +3,7 @@
 // host side of the C ABI (validation per attributeConstraints and
 // derive.weightShapeOk / scaleShapeOk / ioShapeOk / normContractOk, workspace
 // planning, dispatch).  The few-row projection runs in the weight-streaming
-// GEMV of gemv_decode.cu.
+// GEMV of qkv_gemv.cu (over the QMoE decode path's consumer core).
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -173,45 +173,6 @@ struct Proj3 {
     void* out[3];
 };
 
-// Where the GEMV's range split shares a row block among CTAs, out_p[r, n] =
-// the sum of their partial sums in slot order (every slot's load issued before
-// the sum); the GEMV stored the other row blocks itself.  The sharing follows
-// the GEMV's split: CTA c of G holds flat (row block, K chunk) pairs
-// [c * total / G, (c + 1) * total / G).
-struct QkvSplit {
-    int64_t nkc, total, grid;
-    int64_t nrb0, nrb1;     // row blocks of projections 0 and 1
-};
-
-__device__ __forceinline__ int qkv_cta_of(int64_t f, const QkvSplit& sp) {
-    return int(((f + 1) * sp.grid - 1) / sp.total);
-}
-
-template <typename T>
-__global__ void qkv_reduce_kernel(Proj3 pj, const float* __restrict__ p0, const float* __restrict__ p1,
-                                  const float* __restrict__ p2, QkvSplit sp, int64_t rows) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    int p = 0;
-    while (p < 3 && idx >= rows * pj.N[p]) idx -= rows * pj.N[p++];
-    if (p >= 3) return;
-    const int64_t rbg = (idx % pj.N[p]) / kQkvRowBlock + (p > 0 ? sp.nrb0 : 0) + (p > 1 ? sp.nrb1 : 0);
-    const int splits = qkv_cta_of(rbg * sp.nkc + sp.nkc - 1, sp) - qkv_cta_of(rbg * sp.nkc, sp) + 1;
-    if (splits == 1) return;   // stored by the GEMV
-    const float* part = p == 0 ? p0 : (p == 1 ? p1 : p2);
-    const int64_t stride = rows * pj.N[p];
-    float s = 0.f;
-    for (int sp0 = 0; sp0 < splits; sp0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = sp0 + j < splits ? part[int64_t(sp0 + j) * stride + idx] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (sp0 + j < splits) s += v[j];
-    }
-    st(static_cast<T*>(pj.out[p]), idx, s);
-}
-
 // Scalar path: one warp per (projection, output n, row); the codes are
 // dequantised on the fly (zero point 8, block-32 scales).
 template <typename T>
@@ -251,7 +212,7 @@ struct QkvProblem {
 struct QkvPlan {
     int splits = 1;
     int64_t pitch16 = 0;
-    size_t off_n16 = 0, off_n32 = 0, off_part = 0, bytes = 0;
+    size_t off_n16 = 0, off_n32 = 0, off_part = 0, off_flags = 0, bytes = 0;
 };
 
 qmoe_status qderive(const int64_t* a_shape, int32_t a_rank, const qkv_attrs* at, int32_t dtype,
@@ -302,6 +263,7 @@ QkvPlan qplan(const QkvProblem& p) {
         q.pitch16 = p.K;
         q.off_n16 = take(2 * size_t(p.rows) * size_t(q.pitch16));
         q.off_part = take(4 * size_t(q.splits) * size_t(p.rows) * size_t(p.N[0] + p.N[1] + p.N[2]));
+        q.off_flags = take(8 * size_t(q.splits) * size_t(qkv_gemv_row_blocks(p.N, p.K)));
     }
     q.bytes = off;
     return q;
@@ -363,22 +325,9 @@ cudaError_t run_typed(const QkvProblem& p, const QkvPlan& q, const void* A, cons
         g.b_src = n16;
         g.b_pitch = q.pitch16;
         g.splits = q.splits;
+        g.flags = reinterpret_cast<unsigned long long*>(base + q.off_flags);
         g.err = err;
-        if ((e = launch_qkv_gemv(g, s)) != cudaSuccess) return e;
-        if (q.splits == 1) return cudaSuccess;   // every row block inside one CTA: stored
-        const int64_t total = p.rows * (p.N[0] + p.N[1] + p.N[2]);
-        QkvSplit sp;
-        int64_t n_rb = 0;
-        qkv_gemv_geometry(p.N, p.K, &sp.nkc, &n_rb, &sp.total, &sp.grid);
-        sp.nrb0 = (p.N[0] + kQkvRowBlock - 1) / kQkvRowBlock;
-        sp.nrb1 = (p.N[1] + kQkvRowBlock - 1) / kQkvRowBlock;
-        note_launch(QMOE_KERNEL_COMBINE, s, true);
-        e = launch_dependent(qkv_reduce_kernel<T>, dim3(unsigned((total + 255) / 256)), dim3(256), 0,
-                             s, pj, static_cast<const float*>(g.part[0]),
-                             static_cast<const float*>(g.part[1]),
-                             static_cast<const float*>(g.part[2]), sp, p.rows);
-        note_launch(QMOE_KERNEL_COMBINE, s, false);
-        return e != cudaSuccess ? e : cudaGetLastError();
+        return launch_qkv_gemv(g, s);
     }
     if ((e = launch_norm<T>(p, A, skip, gamma, residual, nullptr, 0, n32, err, s)) != cudaSuccess)
         return e;

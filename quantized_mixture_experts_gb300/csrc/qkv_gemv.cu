@@ -22,8 +22,15 @@ namespace {
 // projections, row block by row block, form one flat range that the CTAs cut
 // into equal contiguous pieces, so every SM streams the same number of K chunks
 // with one pipeline ramp.  A row block inside one CTA's range is stored
-// directly; one that two or three CTAs share leaves a partial sum per CTA (slot
-// = the CTA's position among them), added in slot order by the reduction.
+// directly.  A row block that several CTAs share is finished by the CTA that
+// holds its first chunks (slot 0): for that CTA it is the last piece of its
+// range, while for every other sharer (slots 1, 2, ...) it is the first.  The
+// others store their partial sums and then a flag holding the launch's grid
+// identifier (%gridid, distinct for every launch in the context, so a flag
+// left by an earlier launch, or never set, does not count); slot 0 waits for
+// the flags (bounded), adds the partial sums to its own in slot order and
+// stores the result.  A CTA waits only for CTAs of higher index that finish
+// their part before any wait of their own.
 // ---------------------------------------------------------------------------
 struct QkvArgs {
     CUtensorMap tm_w[3];        // packed weights [N_p rows, K/2 bytes], 128-byte swizzle
@@ -37,6 +44,9 @@ struct QkvArgs {
     int rows, nkc, nsc;
     uint32_t stage_bytes, off_s, off_b, pitch_b, nstages, ssize;
     float* part[3];             // [slots][rows][N_p] partial sums of shared row blocks
+    unsigned long long* flags;  // [row blocks of the three][slots]: the grid identifier
+    int slots;
+    uint32_t pre_stages;        // stages whose weights go out before griddepcontrol.wait
     void* out[3];               // [rows][N_p] results, fp32 or fp16 (out_f16)
     int out_f16;
     int32_t* err;
@@ -50,7 +60,7 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t total, int64_t G) {
 
 // The part of flat range [f, fend) inside the row block of chunk f.
 struct Piece {
-    int p, rb;        // projection, row block within it
+    int p, rb, rbg;   // projection, row block within it, row block of the three
     int c0, c1;       // K chunks
     int slot, n;      // this CTA's position among the CTAs sharing the row block; their count
 };
@@ -58,6 +68,7 @@ struct Piece {
 __device__ __forceinline__ Piece piece_at(const QkvArgs& a, int64_t f, int64_t fend) {
     const int64_t rbg = f / a.nkc;
     Piece pc;
+    pc.rbg = int(rbg);
     pc.p = rbg < a.n_rb[0] ? 0 : (rbg < a.n_rb[0] + a.n_rb[1] ? 1 : 2);
     pc.rb = int(rbg - (pc.p > 0 ? a.n_rb[0] : 0) - (pc.p > 1 ? a.n_rb[1] : 0));
     const int64_t f0 = rbg * a.nkc;
@@ -67,6 +78,23 @@ __device__ __forceinline__ Piece piece_at(const QkvArgs& a, int64_t f, int64_t f
     pc.slot = int(blockIdx.x) - clo;
     pc.n = cta_of(f0 + a.nkc - 1, a.total, gridDim.x) - clo + 1;
     return pc;
+}
+
+// Lane 0 of a slot-0 CTA: wait until sharers 1 .. n - 1 have set their flags to
+// this launch's grid identifier (bounded; false on expiry or abort).
+__device__ __forceinline__ bool flags_seen(const unsigned long long* flag, int n, unsigned long long gid,
+                                           uint64_t limit_ns, volatile int* abort) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (int s = 1; s < n; ++s) {
+        for (;;) {
+            unsigned long long v;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flag + s) : "memory");
+            if (v == gid) break;
+            if (*abort || ptx::globaltimer() - t0 > limit_ns) return false;
+            __nanosleep(64);
+        }
+    }
+    return true;
 }
 
 // Result element idx of projection p (row block not shared).
@@ -84,6 +112,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
     __shared__ __align__(8) uint64_t empty_bar[kDecStages];
     __shared__ __align__(8) uint64_t red_full[2];
     __shared__ __align__(8) uint64_t red_empty[2];
+    __shared__ __align__(8) uint64_t part_bar;      // the 8 summing warps stored a shared piece
+    __shared__ __align__(8) uint64_t last_bar;      // the other sharers' flags were seen
     __shared__ int abort_flag;
     __shared__ uint32_t held_meta[kDecStages][3];   // stage slot, bytes, K chunk
     constexpr int KC = kChunkBytes * 2;             // K values per chunk (4-bit codes)
@@ -100,6 +130,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
             ptx::mbar_init(&red_full[s], kDecRowGroups);
             ptx::mbar_init(&red_empty[s], kDecRowGroups);
         }
+        ptx::mbar_init(&part_bar, kDecRowGroups);
+        ptx::mbar_init(&last_bar, 1);
         abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -145,7 +177,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
             const int32_t row0 = pc.rb * kDecRows;
             for (int kc = c0; kc < c1; ++kc, ++it, ring.advance(a.nstages)) {
                 const uint32_t st = ring.st;
-                if (!dep_done && it >= a.nstages) release_held();
+                // a few stages' weights before the wait: more would hold up the previous
+                // kernel's completion behind this grid's copies
+                if (!dep_done && it >= a.pre_stages) release_held();
                 if (!ptx::mbar_wait_sleep(&empty_bar[st], ring.ph ^ 1u, a.wait_ns, &abort_flag)) {
                     ok = false;
                     break;
@@ -274,15 +308,75 @@ __global__ void __launch_bounds__(kDecThreads, 1) qkv_gemv_kernel(const __grid_c
                 }
             continue;
         }
-        float* part = a.part[p] + int64_t(pc.slot) * a.rows * Np;
+        // a shared row block (see the work split above)
+        const int64_t pstride = int64_t(a.rows) * Np;
+        const float* part = a.part[p];
+        unsigned long long* flag = a.flags + int64_t(pc.rbg) * a.slots;
+        unsigned long long gid;
+        asm volatile("mov.u64 %0, %%gridid;" : "=l"(gid));
+        if (pc.slot > 0) {
+            float* mine = a.part[p] + int64_t(pc.slot) * pstride;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = nt * 8 + 2 * c + q;
+                    if (n >= ne) continue;
+                    if (rg < Np) mine[int64_t(n) * Np + rg] = acc[nt][q];
+                    if (rg8 < Np) mine[int64_t(n) * Np + rg8] = acc[nt][2 + q];
+                }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&part_bar);
+            if (cw == 0) {
+                if (!ptx::mbar_wait(&part_bar, 0, a.wait_ns, &abort_flag)) {
+                    if (lane == 0) { record_error(a.err, QMOE_DEVERR_TIMEOUT); abort_flag = 1; }
+                    return;
+                }
+                if (lane == 0)
+                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flag + pc.slot), "l"(gid)
+                                 : "memory");
+                __syncwarp();
+            }
+            continue;
+        }
+        if (cw == 0) {
+            if (lane == 0) {
+                if (!flags_seen(flag, pc.n, gid, a.wait_ns, &abort_flag)) {
+                    record_error(a.err, QMOE_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                }
+                ptx::mbar_arrive(&last_bar);
+            }
+            __syncwarp();
+        }
+        if (!ptx::mbar_wait(&last_bar, 0, a.wait_ns, &abort_flag) || abort_flag) {
+            if (lane == 0) { record_error(a.err, QMOE_DEVERR_TIMEOUT); abort_flag = 1; }
+            return;
+        }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int n = nt * 8 + 2 * c + q;
                 if (n >= ne) continue;
-                if (rg < Np) part[int64_t(n) * Np + rg] = acc[nt][q];
-                if (rg8 < Np) part[int64_t(n) * Np + rg8] = acc[nt][2 + q];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t row = h ? rg8 : rg;
+                    if (row >= Np) continue;
+                    const int64_t idx = int64_t(n) * Np + row;
+                    float sum = acc[nt][2 * h + q];   // slot 0: this CTA
+                    for (int s0 = 1; s0 < pc.n; s0 += 4) {
+                        float v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[u] = s0 + u < pc.n ? __ldcg(part + (s0 + u) * pstride + idx) : 0.f;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (s0 + u < pc.n) sum += v[u];
+                    }
+                    qkv_store(a, p, idx, sum);
+                }
             }
     }
 }
@@ -295,7 +389,7 @@ bool qkv_gemv_shape_ok(int64_t K, bool scales_f16) {
     return true;
 }
 
-static_assert(kDecRows == kQkvRowBlock, "row block of the GEMV and of its reduction");
+static_assert(kDecRows == kQkvRowBlock, "row block of the GEMV and of its partial sums");
 
 // (row block, K chunk) pairs of the three projections and the GEMV's grid.
 void qkv_gemv_geometry(const int64_t N[3], int64_t K, int64_t* nkc, int64_t* n_rb,
@@ -313,7 +407,8 @@ int host_cta_of(int64_t f, int64_t total, int64_t G) { return int(((f + 1) * G -
 }  // namespace
 
 // Partial-sum slots the GEMV needs: the most CTAs that share one row block
-// (1 when every row block lies inside one CTA's range).
+// (1 when every row block lies inside one CTA's range).  Slot 0 keeps its sums in
+// registers; the space for it stays unused.
 int qkv_gemv_splits(const int64_t N[3], int64_t K) {
     int64_t nkc, n_rb, total, G;
     qkv_gemv_geometry(N, K, &nkc, &n_rb, &total, &G);
@@ -322,6 +417,12 @@ int qkv_gemv_splits(const int64_t N[3], int64_t K) {
         most = std::max(most, host_cta_of(rb * nkc + nkc - 1, total, G) -
                                   host_cta_of(rb * nkc, total, G) + 1);
     return most;
+}
+
+int64_t qkv_gemv_row_blocks(const int64_t N[3], int64_t K) {
+    int64_t nkc, n_rb, total, G;
+    qkv_gemv_geometry(N, K, &nkc, &n_rb, &total, &G);
+    return n_rb;
 }
 
 cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
@@ -354,6 +455,8 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
     int64_t nkc, n_rb, total, grid;
     qkv_gemv_geometry(q.N, q.K, &nkc, &n_rb, &total, &grid);
     if (qkv_gemv_splits(q.N, q.K) > q.splits) return cudaErrorInvalidValue;   // slots planned
+    a.flags = q.flags;
+    a.slots = q.splits;
     a.nkc = int(nkc);
     a.total = total;
     const uint32_t bytes_a = 2 * kBoxTile;
@@ -368,6 +471,7 @@ cudaError_t launch_qkv_gemv(const QkvGemvParams& q, cudaStream_t s) {
     const size_t smem_cap = 232448 - 1024;
     a.nstages = uint32_t(std::min<size_t>(kDecStages, (smem_cap - 1024 - kDecRedBytes) / a.stage_bytes));
     if (a.nstages < 2) return cudaErrorInvalidValue;
+    a.pre_stages = std::min<uint32_t>(a.nstages, kQkvPreStages);
     const size_t smem = 1024 + size_t(a.nstages) * a.stage_bytes + kDecRedBytes;
 
     auto kern = q.scales_f16 ? qkv_gemv_kernel<true> : qkv_gemv_kernel<false>;

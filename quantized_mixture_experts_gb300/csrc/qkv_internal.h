@@ -16,9 +16,10 @@ namespace qmoe {
 // in the 4-bit operand order of the decode path (groups of eight stored as
 // 0,4,2,6,1,5,3,7 with the odd elements divided by 16), b_pitch halves apart.
 // Writes the results out[p][row][N_p] in T1 (fp16 when scales_f16, as T1 is the
-// scales' type) when K is not split, else fp32 partial sums
-// part[p][split][row][N_p] for a reduction kernel.  Launched as a programmatic
-// dependent of the kernel that writes b_src.
+// scales' type).  Row blocks that several CTAs share pass fp32 partial sums
+// through part[p][slot][row][N_p] and completion flags flags[row block][slot]
+// (any initial content) to the CTA that finishes them.  Launched as a
+// programmatic dependent of the kernel that writes b_src.
 struct QkvGemvParams {
     const uint8_t* w[3] = {nullptr, nullptr, nullptr};
     const void* s[3] = {nullptr, nullptr, nullptr};
@@ -29,6 +30,7 @@ struct QkvGemvParams {
     const __half* b_src = nullptr;
     int64_t b_pitch = 0;
     float* part[3] = {nullptr, nullptr, nullptr};
+    unsigned long long* flags = nullptr;
     void* out[3] = {nullptr, nullptr, nullptr};
     int splits = 1;
     int32_t* err = nullptr;
@@ -36,6 +38,7 @@ struct QkvGemvParams {
 
 constexpr int kQkvDecodeRows = 16;   // rows the GEMV path takes
 constexpr int kQkvRowBlock = 128;    // weight rows per GEMV work piece
+constexpr uint32_t kQkvPreStages = 2; // stages whose weights the GEMV loads before its inputs are ready
 
 // The GEMV's flat work range: K chunks per row, (row block, K chunk) pairs of the
 // three projections, and its grid (each CTA takes an equal contiguous piece).
@@ -45,6 +48,8 @@ void qkv_gemv_geometry(const int64_t N[3], int64_t K, int64_t* nkc, int64_t* n_r
 bool qkv_gemv_shape_ok(int64_t K, bool scales_f16);
 // Partial-sum slots of the GEMV: the most CTAs that share one row block.
 int qkv_gemv_splits(const int64_t N[3], int64_t K);
+// Row blocks of the three projections (flags per slot each).
+int64_t qkv_gemv_row_blocks(const int64_t N[3], int64_t K);
 cudaError_t launch_qkv_gemv(const QkvGemvParams& p, cudaStream_t s);
 
 }  // namespace qmoe
