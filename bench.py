@@ -824,7 +824,7 @@ def run_gpu_qkv(args, wl):
     ranks_barrier(world)
     torch.cuda.synchronize(dev)
     # A decode-sized call is shorter than its host-side enqueue (argument marshalling,
-    # tensor-map encoding, three launches).  Each timed step therefore starts with an
+    # tensor-map encoding, two launches).  Each timed step therefore starts with an
     # L2 flush long enough (about 130 us of device time) for the host to enqueue the
     # whole call behind it, so that the events around the call see device time only.
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
