@@ -89,7 +89,7 @@ constexpr int kTokBox = kRowsCta;     // token rows per tensor-copy box (one box
 
 struct PairArgs {
     CUtensorMap tm_w;           // packed weights [E*N rows, K/pack bytes], box {64/pack, 128}
-    CUtensorMap tm_b;           // token rows [K/64][srows][64] fp16 (pre-swizzled), box {64, 16, 1}
+    CUtensorMap tm_b;           // token rows [K/64][srows][64] fp16 (pre-swizzled), box {64, 128, 1}
     CUtensorMap tm_s;           // block scales [E*N rows, nb] fp32, box {4, 128}
     const float* scales;        // [E*N, nb] (nb = 1 for column-wise)
     const int32_t* tiles;       // header + (expert, first sorted row, rows, expert's first tile)
