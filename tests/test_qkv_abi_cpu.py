@@ -93,3 +93,41 @@ def test_qkv_workspace_and_path(lib):
     a384 = A(K=384)
     assert q.qkv_choose_path((4, 384), a384, torch.float32) == b.QKV_PATH_DECODE
     assert q.qkv_choose_path((4, 384), a384, torch.float16) == b.QKV_PATH_GENERIC
+
+
+def _qkv_plan_bytes(rows, K, Nq, Nkv, sms=152):
+    """The GEMV path's workspace, restated: the error word, the fp32 normalised rows
+    (scalar-path fallback), the fp16 operand rows, fp32 partial sums for every slot
+    of a shared row block and a 64-bit completion flag per slot and row block; each
+    region rounded up to 256 bytes.  The flat (128-row block, 512-wide K chunk)
+    range is cut into min(total, sms) equal pieces."""
+    def up(x):
+        return (max(x, 1) + 255) // 256 * 256
+    N = (Nq, Nkv, Nkv)
+    nkc = -(-K // 512)
+    n_rb = sum(-(-n // 128) for n in N)
+    total = n_rb * nkc
+    G = max(1, min(total, sms))
+    cta = lambda f: ((f + 1) * G - 1) // total
+    splits = max(cta(rb * nkc + nkc - 1) - cta(rb * nkc) + 1 for rb in range(n_rb))
+    off = 256
+    off += up(4 * rows * K)
+    off += up(2 * rows * K)
+    off += up(4 * splits * rows * sum(N))
+    off += up(8 * splits * n_rb)
+    return off, splits
+
+
+@pytest.mark.parametrize("rows,K,Nq,Nkv,splits", [
+    (8, 8192, 8192, 1024, 3),      # 1280 chunks over 152 CTAs: 8-9 each, 16 per row block
+    (4, 4096, 128, 64, 8),         # 24 chunks, one per CTA: eight CTAs share each row block
+    (11, 2048, 200, 72, 4),        # 16 chunks: four CTAs a row block
+    (16, 768, 256, 256, 2),
+])
+def test_qkv_workspace_covers_partials_and_flags(lib, rows, K, Nq, Nkv, splits):
+    import torch
+    a = A(K=K, Nq=Nq, Nkv=Nkv)
+    assert q.qkv_choose_path((rows, K), a, torch.float16) == b.QKV_PATH_DECODE
+    want, got_splits = _qkv_plan_bytes(rows, K, Nq, Nkv)
+    assert got_splits == splits
+    assert q.qkv_workspace_size((rows, K), a, torch.float16) == want
